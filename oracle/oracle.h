@@ -1,0 +1,137 @@
+/*
+ * oracle.h -- plain CPU oracle for the DDTree tree-verify step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or
+ * calls this code: only the tests, the package's smoke check and the
+ * benchmark's CPU-baseline leg do.  It shares no code, header, table or
+ * helper with the CUDA library; the two agree on array layouts because both
+ * follow the same written conventions, not because they share a definition.
+ *
+ * What it computes (sources are the pages "Luce DFlash" server README and
+ * lucebox PR #606 "add SpecLA factor-capture speculative decoding"):
+ *
+ *   - Tree verify of a gated-DeltaNet layer: every draft-tree node's
+ *     recurrent state is its parent's state advanced by one gated delta-rule
+ *     step ("Luce DFlash" README, "Architecture note": ggml_gated_delta_net
+ *     and its _tree variant; "How it works": one target forward verifies the
+ *     whole tree via a causal mask derived from parent pointers).  The
+ *     recurrence itself is not written on the pages; the oracle uses the
+ *     standard gated delta rule
+ *         S' = alpha * S * (I - beta k k^T) + beta v k^T,   o = S' q.
+ *   - Tree verify of a full-attention layer over a block-quantised KV cache
+ *     (README "Asymmetric K/V quantization": q8_0 default, q4_0 at 4.5 bpv),
+ *     optionally restricted to a sliding window ("--fa-window N", 0 = full).
+ *   - Greedy acceptance ("Scope and limits": the DDTree verify skeleton stays
+ *     argmax; "Results": AL = committed tokens per draft/verify step).
+ *   - Commit / rollback ("How it works", "Per-step rollback"): after accept
+ *     the recurrent state and KV cache equal those of decoding only the
+ *     accepted path.
+ *
+ * Precision: fp64 arithmetic for everything the method computes in floating
+ * point; the committed recurrent state is stored as fp32 between steps.  The
+ * block quantiser decides integer codes, so it runs in fp32 with correctly
+ * rounded operations only (IEEE division, round-half-away, fp16 round to
+ * nearest even): the same precision the kernels decide them in.
+ *
+ * Parity status: every function here is pinned by the "not gpu" tests in
+ * tests/test_oracle_*.py (closed forms, invariants, brute force and a
+ * library cross-check); none is "parity unpinned".
+ *
+ * Layouts (row-major, outermost first):
+ *   parent   [B][N]   int32, parent[0] = -1, 0 <= parent[i] < i
+ *   n_nodes  [B]      int32, 1 <= n_nodes[b] <= N
+ *   GDN q,k  [B][N][Hk][dk]  bf16 bits; v [B][N][Hv][dv] bf16 bits
+ *   beta, log_alpha [B][N][Hv] f32;  state [B][Hv][dv][dk] f32
+ *   GDN out  [B][N][Hv][dv] f32
+ *   attention q [B][N][Hq][D] bf16; k_new, v_new [B][N][Hkv][D] bf16
+ *   cache planes per layer: quants [B][Hkv][cap][D] (int8, q8_0),
+ *       [B][Hkv][cap][D/2] (uint8 nibbles, q4_0) or [B][Hkv][cap][D] f32;
+ *       scales [B][Hkv][cap][D/32] fp16 bits (unused for f32)
+ *   attention out [B][N][Hq][D] f32
+ *   logits [B][N][V] f32; tokens [B][N] int32
+ */
+#ifndef DFLV_ORACLE_H
+#define DFLV_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { ORC_OK = 0, ORC_ERR_ARG = 1, ORC_ERR_TOPOLOGY = 2, ORC_ERR_CAPACITY = 4 };
+enum { ORC_KV_Q8_0 = 0, ORC_KV_Q4_0 = 1, ORC_KV_F32 = 2 };
+
+/* ---- scalar conversions (the oracle's own) ---- */
+double orc_bf16_to_double(uint16_t h);
+float orc_half_to_float(uint16_t h);
+uint16_t orc_float_to_half_rn(float f);
+
+/* ---- tree topology ---- */
+/* Validates parent[0..n) and fills depth[n] and the ancestor-or-self sets as
+ * bitmasks (n <= 64).  Returns ORC_OK or ORC_ERR_TOPOLOGY. */
+int orc_tree_topology(int n, const int32_t* parent, int32_t* depth, uint64_t* anc_self);
+
+/* ---- gated delta rule ---- */
+/* One decode step on a dv x dk state held in fp64:
+ *   S_out = alpha * S (I - beta k k^T) + beta v k^T,  o = S_out q.
+ * S and S_out may not alias. */
+void orc_gdn_step(int dv, int dk, const double* S, const double* q, const double* k,
+                  const double* v, double beta, double alpha, double* S_out, double* o);
+
+/* Tree verify: state of node i = step(state of parent[i]), root's parent
+ * state = the committed state.  If node_states is non-NULL it receives the
+ * fp64 state of every node, [B][N][Hv][dv][dk]. */
+int orc_tree_gdn_verify(int B, int N, int Hk, int Hv, int dk, int dv,
+                        const int32_t* parent, const int32_t* n_nodes,
+                        const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                        const float* beta, const float* log_alpha, const float* state,
+                        float* out, double* node_states);
+
+/* The same outputs computed by replaying every root-to-node path from the
+ * committed state on its own (no state shared between nodes). */
+int orc_tree_gdn_verify_bruteforce(int B, int N, int Hk, int Hv, int dk, int dv,
+                                   const int32_t* parent, const int32_t* n_nodes,
+                                   const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                   const float* beta, const float* log_alpha,
+                                   const float* state, float* out);
+
+/* Commit of the recurrent state: decode the accepted nodes path[b][0..L) in
+ * order from the committed state and store the result (fp32) in place. */
+int orc_gdn_commit(int B, int N, int Hk, int Hv, int dk, int dv,
+                   const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                   const float* beta, const float* log_alpha,
+                   const int32_t* path, const int32_t* path_len, float* state);
+
+/* ---- block quantisation (32 values + one fp16 scale) ---- */
+void orc_quantize_q8_0(const float* x, int8_t* qs, uint16_t* d16);
+void orc_quantize_q4_0(const float* x, uint8_t* nib, uint16_t* d16);
+void orc_dequantize_q8_0(const int8_t* qs, uint16_t d16, double* x);
+void orc_dequantize_q4_0(const uint8_t* nib, uint16_t d16, double* x);
+
+/* ---- attention tree verify ---- */
+/* Writes the quantised tree keys/values into cache slots [P, P+n) and then
+ * attends every (node, query head) to the visible keys.  n_past[b] = P.
+ * With rows == NULL every output row is computed; otherwise only the n_rows
+ * flat rows (b * N + i) * Hq + h listed (for sampled checks at full size). */
+int orc_tree_attn_verify(int B, int N, int Hq, int Hkv, int D, int cap, int window,
+                         int kv_type, double scale,
+                         const int32_t* parent, const int32_t* n_nodes, const int32_t* n_past,
+                         const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
+                         void* kq, void* vq, uint16_t* ks, uint16_t* vs, float* out,
+                         const int32_t* rows, int n_rows);
+
+/* ---- greedy acceptance ---- */
+int orc_accept_greedy(int B, int N, int V, const float* logits, const int32_t* tokens,
+                      const int32_t* parent, const int32_t* n_nodes,
+                      int32_t* path, int32_t* path_len, int32_t* next_token, int32_t* best);
+
+/* ---- KV commit: move slot P+path[m] to P+m for m < L (all reads first) ---- */
+int orc_kv_commit(int B, int N, int Hkv, int D, int cap, int kv_type,
+                  const int32_t* path, const int32_t* path_len, const int32_t* n_past,
+                  void* kq, void* vq, uint16_t* ks, uint16_t* vs);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
