@@ -1,0 +1,237 @@
+/*
+ * dflv.h -- C ABI of libdflv, the GPU tree-verify step of DDTree speculative
+ * decoding for a hybrid gated-DeltaNet + full-attention target.
+ *
+ * Sources for what the step computes (the pages this library follows):
+ *   [README]  "Luce DFlash" server README (Luce-Org/lucebox, server/README.md)
+ *   [PR606]   lucebox PR #606 "add SpecLA factor-capture speculative decoding"
+ *
+ *   - A draft tree of n nodes is given as candidate tokens plus a parent
+ *     array in topological order; node 0 is the root (the last committed
+ *     token) and parent[i] < i.  One target pass scores every node, with a
+ *     causal mask derived from the parent pointers ([README] "How it works",
+ *     "DDTree tree verify"; [PR606] "Paper mapping": scored candidates and
+ *     parent topology, a chain being a degenerate tree).
+ *   - In the gated-DeltaNet layers each node's recurrent state is its
+ *     parent's state advanced by one gated delta-rule step ([README]
+ *     "Architecture note": ggml_gated_delta_net_tree).  The pages do not
+ *     write the recurrence; this library uses the standard gated delta rule
+ *         S_i = alpha_i S_par(i) (I - beta_i k_i k_i^T) + beta_i v_i k_i^T,
+ *         o_i = S_i q_i,
+ *     with the committed state as the root's parent state, q and k given
+ *     already L2-normalised, and no 1/sqrt(dk) factor.
+ *   - In the attention layers the tree queries attend to the block-quantised
+ *     KV cache and to their own ancestors-or-self, optionally inside a
+ *     sliding window ([README] "--fa-window N", 0 = full attention;
+ *     "Asymmetric K/V quantization": q8_0 default, Q4_0 at 4.5 bpv).
+ *   - Greedy acceptance walks the tree against the target's argmax ([README]
+ *     "Scope and limits": the DDTree verify skeleton stays argmax).
+ *   - Commit / rollback leaves the recurrent state and KV cache as if only
+ *     the accepted path had been decoded ([README] "How it works",
+ *     "Per-step rollback"; [PR606] review note naming the commit routines).
+ *
+ * General conventions
+ *   - Every array argument is a DEVICE pointer unless marked "host".  The
+ *     caller owns every buffer; the library never allocates or frees memory.
+ *   - bf16 and fp16 values are passed as uint16_t bit patterns.
+ *   - All calls are asynchronous on the given stream (0 = legacy default
+ *     stream) and never synchronise it, so a whole step can be captured in a
+ *     CUDA graph.
+ *   - The returned dflv_status reports only what the host can check before
+ *     launching (NULL or misaligned pointers, unsupported shapes).  Nothing
+ *     is launched when it is not DFLV_OK.
+ *   - Errors found on the device (a malformed parent array, a cache slot out
+ *     of capacity, an invalid accepted path) are OR-ed into *status_dev as
+ *     DFLV_DEV_* bits; the outputs of the affected sequence are then
+ *     unspecified.  status_dev points to one int32 in device memory that the
+ *     caller zeroes and reads back when it wants to check.
+ *   - Pointers to bf16/f32/int8/u8 arrays must be 16-byte aligned.
+ *   - No global state: calls are re-entrant on distinct buffers.
+ *   - Padded nodes (i >= n_nodes[b]) are ignored; their outputs are
+ *     unspecified.
+ */
+#ifndef DFLV_H
+#define DFLV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dflv_stream_t; /* a cudaStream_t */
+
+typedef enum {
+    DFLV_OK = 0,
+    DFLV_ERR_INVALID_ARG = 1, /* NULL / misaligned pointer, bad count */
+    DFLV_ERR_TOPOLOGY = 2,    /* reserved for host-visible topology errors */
+    DFLV_ERR_UNSUPPORTED = 3, /* shape or type this build does not implement */
+    DFLV_ERR_CAPACITY = 4,    /* a workspace or cache too small (host check) */
+    DFLV_ERR_CUDA = 5         /* a CUDA launch or attribute call failed */
+} dflv_status;
+
+/* Bits OR-ed into *status_dev by the kernels. */
+enum {
+    DFLV_DEV_TOPOLOGY = 1, /* parent[0] != -1, parent[i] outside [0, i), n outside [1, N_max] */
+    DFLV_DEV_CAPACITY = 2, /* P < 0 or P + n > cap in an attention layer */
+    DFLV_DEV_PATH = 4,     /* commit got path_len outside [1, N_max] or a node outside [0, N_max) */
+    DFLV_DEV_TIMEOUT = 8   /* a bounded wait for an asynchronous copy gave up */
+};
+
+typedef enum {
+    DFLV_KV_Q8_0 = 0, /* 32 int8 codes + one fp16 scale d per block: x = d * q */
+    DFLV_KV_Q4_0 = 1, /* 32 4-bit codes c + one fp16 scale d per block: x = d * (c - 8) */
+    DFLV_KV_F32 = 2   /* plain fp32 cache (small exactness checks) */
+} dflv_kv_type;
+
+/* ------------------------------------------------------------------------ */
+/* Gated-DeltaNet layer                                                      */
+/* ------------------------------------------------------------------------ */
+
+/* Shape of one gated-DeltaNet layer's verify.  Hv must be a multiple of Hk;
+ * v-head h reads q/k head h / (Hv / Hk).  Supported: 1 <= N_max <= 64,
+ * dk in {16, 32, 64, 128}, dv a multiple of 16 (<= 512). */
+typedef struct {
+    int32_t B, N_max, Hk, Hv, dk, dv;
+} dflv_gdn_desc;
+
+/* Per-node factors captured by verify for commit ([PR606]: factor capture
+ * instead of materialising every node's state; [README]: the _persist op
+ * writes these intermediates directly instead of copying states).  All
+ * caller-owned device arrays:
+ *   u     [B][N_max][Hv][dv] f32 : u_i = beta_i (v_i - alpha_i S_par(i) k_i)
+ *   g     [B][N_max][Hv]     f32 : g_i = sum of log alpha over i's ancestors-or-self
+ *   kcopy [B][N_max][Hk][dk] bf16: the node keys (so the caller may reuse k)
+ * Valid until the next verify that writes the same buffers. */
+typedef struct {
+    float* u;
+    float* g;
+    uint16_t* kcopy;
+} dflv_gdn_factors;
+
+/* Tree verify of one gated-DeltaNet layer.
+ *   parent    [B][N_max] int32; n_nodes [B] int32
+ *   q, k      [B][N_max][Hk][dk] bf16 (L2-normalised by the caller)
+ *   v         [B][N_max][Hv][dv] bf16
+ *   beta      [B][N_max][Hv] f32;  log_alpha [B][N_max][Hv] f32 (log of the decay)
+ *   state     [B][Hv][dv][dk] f32, the committed state; READ ONLY here
+ *   out       [B][N_max][Hv][dv] f32, o_i = S_i q_i
+ *   factors   host pointer to the factor buffers above (all required)
+ *   workspace reserved: dflv_gdn_workspace_size() returns 0; may be NULL
+ * The committed state is never written, so rejecting the whole tree costs
+ * nothing (rollback is free). */
+dflv_status dflv_tree_gdn_verify(const dflv_gdn_desc* desc, const int32_t* parent,
+                                 const int32_t* n_nodes, const uint16_t* q, const uint16_t* k,
+                                 const uint16_t* v, const float* beta, const float* log_alpha,
+                                 const float* state, float* out, const dflv_gdn_factors* factors,
+                                 int32_t* status_dev, void* workspace, size_t ws_bytes,
+                                 dflv_stream_t stream);
+
+size_t dflv_gdn_workspace_size(const dflv_gdn_desc* desc);
+
+/* ------------------------------------------------------------------------ */
+/* Attention layer                                                           */
+/* ------------------------------------------------------------------------ */
+
+/* Shape of one attention layer's verify.  Hq must be a multiple of Hkv;
+ * query head h reads KV head h / (Hq / Hkv).  cap = slots per (sequence, KV
+ * head) in the cache planes.  window W >= 0: a key at position j is visible
+ * to a node at position p iff j <= p and (W == 0 or j > p - W).  Node i sits
+ * at position P + depth(i).  scale multiplies q.k (usually 1/sqrt(D)).
+ * Supported: 1 <= N_max <= 64; q8_0/q4_0 with D in {64, 128, 256}; f32 with
+ * D a multiple of 4, D <= 256. */
+typedef struct {
+    int32_t B, N_max, Hq, Hkv, D, cap, window;
+    dflv_kv_type type;
+    float scale;
+} dflv_attn_desc;
+
+/* One attention layer's cache, structure-of-arrays planes:
+ *   kq, vq : q8_0: int8 [B][Hkv][cap][D]; q4_0: uint8 [B][Hkv][cap][D/2]
+ *            (element j < 16 of a 32-block in the low nibble of byte j,
+ *            element j+16 in its high nibble); f32: float [B][Hkv][cap][D]
+ *   ks, vs : fp16 [B][Hkv][cap][D/32] block scales (NULL for f32) */
+typedef struct {
+    void* kq;
+    void* vq;
+    uint16_t* ks;
+    uint16_t* vs;
+} dflv_kv_layer;
+
+/* Tree verify of one attention layer.
+ *   parent [B][N_max] int32; n_nodes [B] int32
+ *   n_past [B] int32 (device): P, the committed tokens of each sequence
+ *   q      [B][N_max][Hq][D] bf16; k_new, v_new [B][N_max][Hkv][D] bf16
+ *   cache  host pointer to the layer's planes: slots [P, P + n) are
+ *          overwritten with the tree's quantised keys/values (quantiser:
+ *          d = fp16(amax / 127) resp. fp16(amax / 7) of each 32-block,
+ *          codes = round-half-away(x / d) clamped; slots < P are only read)
+ *   out    [B][N_max][Hq][D] f32
+ *   workspace reserved: dflv_attn_workspace_size() returns 0; may be NULL
+ * Every node attends to the cached positions j < P inside its window and to
+ * the tree slots of its ancestors-or-self, reading the quantised values, so
+ * a chain tree reproduces sequential decode. */
+dflv_status dflv_tree_attn_verify(const dflv_attn_desc* desc, const int32_t* parent,
+                                  const int32_t* n_nodes, const int32_t* n_past,
+                                  const uint16_t* q, const uint16_t* k_new,
+                                  const uint16_t* v_new, const dflv_kv_layer* cache, float* out,
+                                  int32_t* status_dev, void* workspace, size_t ws_bytes,
+                                  dflv_stream_t stream);
+
+size_t dflv_attn_workspace_size(const dflv_attn_desc* desc);
+
+/* ------------------------------------------------------------------------ */
+/* Greedy acceptance                                                         */
+/* ------------------------------------------------------------------------ */
+
+/* best[b][i] = argmax_v logits[b][i][v] (ties: lowest v).  Then from the
+ * root: while a child c of the current node has tokens[b][c] == best of the
+ * current node, move to the lowest-index such c.  path[b][0..L) = visited
+ * nodes (path[b][0] = 0), path_len[b] = L >= 1 = tokens committed this
+ * step, next_token[b] = best of the last visited node.
+ *   logits [B][N_max][vocab] f32 (finite); tokens, parent [B][N_max] int32
+ *   path, best [B][N_max] int32; path_len, next_token [B] int32
+ * Everything stays on the device, so accept -> commit needs no host sync. */
+dflv_status dflv_accept_greedy(int32_t B, int32_t N_max, int32_t vocab, const float* logits,
+                               const int32_t* tokens, const int32_t* parent,
+                               const int32_t* n_nodes, int32_t* path, int32_t* path_len,
+                               int32_t* next_token, int32_t* best, int32_t* status_dev,
+                               dflv_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Commit / rollback                                                         */
+/* ------------------------------------------------------------------------ */
+
+/* Commits the accepted path of every sequence into all layers in one launch.
+ *   gdn, n_gdn      : GDN shape (may be NULL when n_gdn == 0)
+ *   states          : host array of n_gdn device state pointers (in/out)
+ *   factors         : host array of n_gdn factor sets written by verify
+ *   attn, n_attn    : attention shape (may be NULL when n_attn == 0)
+ *   caches          : host array of n_attn cache plane sets (in/out)
+ *   path, path_len  : [B][N_max], [B] int32 from dflv_accept_greedy
+ *   n_past          : [B] int32, advanced in place by path_len
+ * GDN: S <- e^{g_e} S + sum_{m<L} e^{g_e - g_{p_m}} u_{p_m} k_{p_m}^T with
+ * p_m = path[m], e = path[L-1]: the state of the path's end node.  KV: slot
+ * P + path[m] moves to P + m for every m < L (all moves read before any
+ * write).  Slots [P + L, P + N_max) are left unspecified.  Rejected nodes
+ * need no work: verify never wrote the committed state or slots < P.
+ * The path must be a root-to-node path of the verified tree (as accept
+ * produces); N_max must equal the verify calls' N_max. */
+dflv_status dflv_commit_rollback(const dflv_gdn_desc* gdn, int32_t n_gdn, float* const* states,
+                                 const dflv_gdn_factors* factors, const dflv_attn_desc* attn,
+                                 int32_t n_attn, const dflv_kv_layer* caches,
+                                 const int32_t* path, const int32_t* path_len, int32_t* n_past,
+                                 int32_t* status_dev, dflv_stream_t stream);
+
+/* Most layers one dflv_commit_rollback call takes (per kind). */
+#define DFLV_MAX_COMMIT_GDN_LAYERS 128
+#define DFLV_MAX_COMMIT_ATTN_LAYERS 64
+
+/* Human-readable name of a status code (static string). */
+const char* dflv_status_string(dflv_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DFLV_H */

@@ -1,0 +1,201 @@
+// commit.cu -- commit the accepted path into every layer, in one launch.
+//
+// After acceptance the recurrent state and the KV cache must equal those of
+// decoding only the accepted tokens ("Luce DFlash" README, "How it works",
+// per-step rollback; SpecLA PR #606 names the commit routines: compaction of
+// the walked path and the pending-factor flush).  Rejected nodes cost nothing
+// here because verify never wrote the committed state or the slots below P.
+//
+//   GDN layer, every (sequence, v-head):  with p_m = path[m], e = path[L-1],
+//       S <- e^{g_e} S + sum_{m<L} e^{g_e - g_{p_m}} u_{p_m} k_{p_m}^T,
+//   the state of the path's end node in the factor form captured by verify.
+//   Each element of S is read and written once (rank-L update in place);
+//   the L scaled factor rows sit in shared memory.
+//   Attention layer, every (sequence, KV head): slot P + path[m] moves to
+//   P + m for m < L.  A destination can be another accepted node's source
+//   (path 0, 2, 3: 2 -> 1, 3 -> 2), so the owning CTA reads every source row
+//   of a plane into shared memory before it writes any.
+// A second tiny kernel then advances n_past by path_len, after every CTA of
+// the first has read P.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dflv {
+
+namespace {
+
+constexpr int kCommitThreads = 256;
+
+DFLV_DEVINL bool path_ok(const CommitArgs& a, int b, int& L) {
+    L = __ldg(a.path_len + b);
+    if (L < 1 || L > a.N_max) return false;
+    for (int m = 0; m < L; ++m) {
+        const int p = __ldg(a.path + (size_t)b * a.N_max + m);
+        if (p < 0 || p >= a.N_max) return false;
+    }
+    return true;
+}
+
+__device__ void commit_gdn_head(const CommitArgs& a, int layer, int b, int h, unsigned char* smem) {
+    const int tid = threadIdx.x;
+    int L;
+    if (!path_ok(a, b, L)) {
+        if (tid == 0 && layer == 0 && h == 0) raise_status(a.status, DFLV_DEV_PATH);
+        return;
+    }
+    const CommitGdnLayer ly = a.gdn[layer];
+    const int dk = a.dk, dv = a.dv, N = a.N_max;
+    const int hk = h / (a.Hv / a.Hk);
+    float* wu_s = reinterpret_cast<float*>(smem);   // [L][dv]  e^{g_e-g_p} u_p
+    float* kf_s = wu_s + (size_t)N * dv;            // [L][dk]  k_p
+    __shared__ float w_s[64];
+    __shared__ float Ge_s;
+    const int e = __ldg(a.path + (size_t)b * N + L - 1);
+    const float ge = __ldg(ly.g + ((size_t)b * N + e) * a.Hv + h);
+    for (int m = tid; m < L; m += kCommitThreads) {
+        const int p = __ldg(a.path + (size_t)b * N + m);
+        w_s[m] = expf(ge - __ldg(ly.g + ((size_t)b * N + p) * a.Hv + h));
+    }
+    if (tid == 0) Ge_s = expf(ge);
+    __syncthreads();
+    for (int idx = tid; idx < L * dv; idx += kCommitThreads) {
+        const int m = idx / dv, r = idx % dv;
+        const int p = __ldg(a.path + (size_t)b * N + m);
+        wu_s[idx] = w_s[m] * __ldg(ly.u + (((size_t)b * N + p) * a.Hv + h) * dv + r);
+    }
+    for (int idx = tid; idx < L * dk; idx += kCommitThreads) {
+        const int m = idx / dk, c = idx % dk;
+        const int p = __ldg(a.path + (size_t)b * N + m);
+        kf_s[idx] = bf16_bits_to_float(__ldg(ly.kcopy + (((size_t)b * N + p) * a.Hk + hk) * dk + c));
+    }
+    __syncthreads();
+
+    const float Ge = Ge_s;
+    float4* S = reinterpret_cast<float4*>(ly.state + ((size_t)b * a.Hv + h) * dv * dk);
+    const int E4 = dv * dk / 4;
+    constexpr int U = 8;  // float4 per thread in flight
+    for (int base = 0; base < E4; base += U * kCommitThreads) {
+        float4 x[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e4 = base + u * kCommitThreads + tid;
+            if (e4 < E4) x[u] = __ldcs(S + e4);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e4 = base + u * kCommitThreads + tid;
+            if (e4 >= E4) continue;
+            const int r = (e4 * 4) / dk, c = (e4 * 4) % dk;
+            float4 acc = make_float4(Ge * x[u].x, Ge * x[u].y, Ge * x[u].z, Ge * x[u].w);
+            for (int m = 0; m < L; ++m) {
+                const float w = wu_s[m * dv + r];
+                const float4 kk = *reinterpret_cast<const float4*>(kf_s + m * dk + c);
+                acc.x = fmaf(w, kk.x, acc.x);
+                acc.y = fmaf(w, kk.y, acc.y);
+                acc.z = fmaf(w, kk.z, acc.z);
+                acc.w = fmaf(w, kk.w, acc.w);
+            }
+            __stcs(S + e4, acc);
+        }
+    }
+}
+
+__device__ void commit_kv_head(const CommitArgs& a, int layer, int b, int kvh, unsigned char* smem) {
+    const int tid = threadIdx.x;
+    int L;
+    if (!path_ok(a, b, L)) {
+        if (tid == 0 && layer == 0 && kvh == 0 && a.n_gdn == 0) raise_status(a.status, DFLV_DEV_PATH);
+        return;
+    }
+    const int P = __ldg(a.n_past + b);
+    const int N = a.N_max;
+    __shared__ int src_s[64];
+    bool bad = P < 0 || P + L > a.cap;
+    for (int m = 0; m < L; ++m) bad |= P + __ldg(a.path + (size_t)b * N + m) >= a.cap;
+    if (bad) {
+        if (tid == 0 && kvh == 0) raise_status(a.status, DFLV_DEV_CAPACITY);
+        return;
+    }
+    for (int m = tid; m < L; m += kCommitThreads) src_s[m] = P + __ldg(a.path + (size_t)b * N + m);
+    __syncthreads();
+    const CommitAttnLayer ly = a.attn[layer];
+    const size_t row0 = ((size_t)b * a.Hkv + kvh) * a.cap;
+    const int nb = a.D / 32;
+    const int code_bytes = a.type == DFLV_KV_Q8_0 ? a.D : a.type == DFLV_KV_Q4_0 ? a.D / 2 : a.D * 4;
+    // four planes: K codes, V codes, K scales, V scales (no scales for f32)
+    for (int plane = 0; plane < 4; ++plane) {
+        uint8_t* base;
+        int rb;
+        if (plane < 2) {
+            base = plane == 0 ? ly.kq : ly.vq;
+            rb = code_bytes;
+        } else {
+            if (a.type == DFLV_KV_F32) break;
+            base = reinterpret_cast<uint8_t*>(plane == 2 ? ly.ks : ly.vs);
+            rb = nb * 2;
+        }
+        // rows are 4-byte multiples (scales: D/32 halves with D >= 64)
+        const int w = rb / 4;
+        uint32_t* tmp = reinterpret_cast<uint32_t*>(smem);
+        for (int idx = tid; idx < L * w; idx += kCommitThreads) {
+            const int m = idx / w, c = idx % w;
+            tmp[idx] = reinterpret_cast<const uint32_t*>(base + (row0 + src_s[m]) * rb)[c];
+        }
+        __syncthreads();
+        for (int idx = tid; idx < L * w; idx += kCommitThreads) {
+            const int m = idx / w, c = idx % w;
+            reinterpret_cast<uint32_t*>(base + (row0 + P + m) * rb)[c] = tmp[idx];
+        }
+        __syncthreads();
+    }
+}
+
+__global__ void __launch_bounds__(kCommitThreads) commit_kernel(const __grid_constant__ CommitArgs a) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    grid_dependency_wait();
+    const int n_gdn_blocks = a.n_gdn * a.B * a.Hv;
+    int blk = blockIdx.x;
+    if (blk < n_gdn_blocks) {
+        const int layer = blk / (a.B * a.Hv), rem = blk % (a.B * a.Hv);
+        commit_gdn_head(a, layer, rem / a.Hv, rem % a.Hv, smem);
+    } else {
+        blk -= n_gdn_blocks;
+        const int layer = blk / (a.B * a.Hkv), rem = blk % (a.B * a.Hkv);
+        commit_kv_head(a, layer, rem / a.Hkv, rem % a.Hkv, smem);
+    }
+}
+
+__global__ void commit_advance_kernel(const int32_t* path_len, int32_t* n_past, int B, int N_max) {
+    grid_dependency_wait();
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    const int L = path_len[b];
+    if (L >= 1 && L <= N_max) n_past[b] += L;
+}
+
+}  // namespace
+
+cudaError_t launch_commit_rollback(const CommitArgs& a, cudaStream_t stream) {
+    const long blocks = (long)a.n_gdn * a.B * a.Hv + (long)a.n_attn * a.B * a.Hkv;
+    if (blocks > 0) {
+        size_t smem = 0;
+        if (a.n_gdn > 0) smem = (size_t)a.N_max * (a.dv + a.dk) * 4;
+        if (a.n_attn > 0) {
+            const int code_bytes = a.type == DFLV_KV_Q8_0 ? a.D : a.type == DFLV_KV_Q4_0 ? a.D / 2 : a.D * 4;
+            const size_t kv = (size_t)a.N_max * code_bytes;
+            if (kv > smem) smem = kv;
+        }
+        cudaError_t e = cudaFuncSetAttribute(commit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        commit_kernel<<<(unsigned)blocks, kCommitThreads, smem, stream>>>(a);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    if (a.n_past != nullptr) {
+        commit_advance_kernel<<<(a.B + 255) / 256, 256, 0, stream>>>(a.path_len, a.n_past, a.B, a.N_max);
+        return cudaGetLastError();
+    }
+    return cudaSuccess;
+}
+
+}  // namespace dflv

@@ -1,0 +1,149 @@
+// common.cuh -- small device helpers shared by the libdflv kernels:
+// bf16/fp16 packing, warp-level tensor-core MMA, the bulk-copy (TMA) engine
+// with mbarrier completion and bounded waits, programmatic dependent launch,
+// and the device status word.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dflv.h"
+
+#define DFLV_DEVINL __device__ __forceinline__
+
+namespace dflv {
+
+// ---------------------------------------------------------------- status
+DFLV_DEVINL void raise_status(int32_t* status_dev, int bits) {
+    if (status_dev) atomicOr(status_dev, bits);
+}
+
+// ---------------------------------------------------------------- packing
+DFLV_DEVINL float bf16_bits_to_float(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
+
+// Two floats -> packed bf16x2 (round to nearest even); lo in the low half.
+DFLV_DEVINL uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+DFLV_DEVINL uint32_t pack_f16x2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// bf16 x -> (hi, lo) with hi = bf16(x), lo = bf16(x - hi): x ~= hi + lo to
+// about 16 significant bits.
+DFLV_DEVINL void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    float2 hf = __bfloat1622float2(h);
+    __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+    hi = *reinterpret_cast<uint32_t*>(&h);
+    lo = *reinterpret_cast<uint32_t*>(&l);
+}
+
+// ---------------------------------------------------------------- MMA
+// D(16x8, f32) += A(16x16, bf16, row) * B(16x8, bf16, col).
+DFLV_DEVINL void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// D(16x8, f32) += A(16x16, f16, row) * B(16x8, f16, col).
+DFLV_DEVINL void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+DFLV_DEVINL void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t smem_addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_addr));
+}
+
+DFLV_DEVINL uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- mbarrier + bulk copy
+DFLV_DEVINL void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+DFLV_DEVINL void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+
+DFLV_DEVINL void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
+DFLV_DEVINL void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// One bulk (TMA engine) copy global -> shared, completion counted on bar.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+DFLV_DEVINL void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+DFLV_DEVINL bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on a phase of bar.  Returns false (and raises
+// DFLV_DEV_TIMEOUT) if the phase did not complete within the limit; the
+// caller then waits once more (bounded) for its copy and leaves.
+constexpr uint32_t kWaitLimit = 1u << 22;
+
+DFLV_DEVINL bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int32_t* status_dev) {
+    for (uint32_t it = 0; it < kWaitLimit; ++it)
+        if (mbar_try_wait(bar, parity)) return true;
+    raise_status(status_dev, DFLV_DEV_TIMEOUT);
+    for (uint32_t it = 0; it < kWaitLimit; ++it)
+        if (mbar_try_wait(bar, parity)) break;
+    return false;
+}
+
+// ---------------------------------------------------------------- cp.async (16 B)
+DFLV_DEVINL void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+DFLV_DEVINL void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+DFLV_DEVINL void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// ---------------------------------------------------------------- PDL
+// Waits until the grids this one depends on (programmatic dependent launch)
+// have completed and their memory is visible.  A no-op without PDL.
+DFLV_DEVINL void grid_dependency_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
+// ---------------------------------------------------------------- misc
+DFLV_DEVINL int popc64(uint64_t x) { return __popcll(x); }
+DFLV_DEVINL int ffs64(uint64_t x) { return __ffsll((long long)x) - 1; }
+
+}  // namespace dflv

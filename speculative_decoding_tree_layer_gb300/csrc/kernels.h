@@ -1,0 +1,99 @@
+// kernels.h -- internal launch interface between the C ABI (api.cu) and the
+// kernels.  Plain structs of device pointers and sizes; no torch types.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace dflv {
+
+struct GdnVerifyArgs {
+    int B, N_max, Hk, Hv, dk, dv;
+    const int32_t* parent;
+    const int32_t* n_nodes;
+    const uint16_t* q;
+    const uint16_t* k;
+    const uint16_t* v;
+    const float* beta;
+    const float* log_alpha;
+    const float* state;
+    float* out;
+    float* u;
+    float* g;
+    uint16_t* kcopy;
+    int32_t* status;
+};
+
+cudaError_t launch_gdn_tree_verify(const GdnVerifyArgs& a, cudaStream_t stream);
+size_t gdn_verify_smem_bytes(int N_max, int dk, int dv);
+
+struct AttnVerifyArgs {
+    int B, N_max, Hq, Hkv, D, cap, window, type;
+    float scale;
+    const int32_t* parent;
+    const int32_t* n_nodes;
+    const int32_t* n_past;
+    const uint16_t* q;
+    const uint16_t* k_new;
+    const uint16_t* v_new;
+    void* kq;
+    void* vq;
+    uint16_t* ks;
+    uint16_t* vs;
+    float* out;
+    int32_t* status;
+};
+
+cudaError_t launch_attn_tree_verify(const AttnVerifyArgs& a, cudaStream_t stream);
+
+struct AcceptArgs {
+    int B, N_max, vocab;
+    const float* logits;
+    const int32_t* tokens;
+    const int32_t* parent;
+    const int32_t* n_nodes;
+    int32_t* path;
+    int32_t* path_len;
+    int32_t* next_token;
+    int32_t* best;
+    int32_t* status;
+};
+
+cudaError_t launch_accept_greedy(const AcceptArgs& a, cudaStream_t stream);
+
+constexpr int kMaxCommitGdn = 128;
+constexpr int kMaxCommitAttn = 64;
+
+struct CommitGdnLayer {
+    float* state;
+    const float* u;
+    const float* g;
+    const uint16_t* kcopy;
+};
+
+struct CommitAttnLayer {
+    uint8_t* kq;
+    uint8_t* vq;
+    uint16_t* ks;
+    uint16_t* vs;
+};
+
+// Passed by value as a kernel parameter (a few KB; graph-capturable).
+struct CommitArgs {
+    int B, N_max;
+    // GDN geometry
+    int n_gdn, Hk, Hv, dk, dv;
+    // attention geometry
+    int n_attn, Hkv, D, cap, type;
+    const int32_t* path;
+    const int32_t* path_len;
+    int32_t* n_past;
+    int32_t* status;
+    CommitGdnLayer gdn[kMaxCommitGdn];
+    CommitAttnLayer attn[kMaxCommitAttn];
+};
+
+cudaError_t launch_commit_rollback(const CommitArgs& a, cudaStream_t stream);
+
+}  // namespace dflv

@@ -1,0 +1,95 @@
+"""The C-ABI library builds for sm_103a, loads, exports every symbol the
+header declares, and rejects bad arguments on the host (CPU only: no call
+here reaches a kernel)."""
+import ctypes
+
+import pytest
+
+import speculative_decoding_tree_layer_gb300 as pkg
+from speculative_decoding_tree_layer_gb300 import dflv
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pkg.build()
+    return dflv.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = dflv.header_symbols()
+    assert set(names) >= {"dflv_tree_gdn_verify", "dflv_tree_attn_verify", "dflv_accept_greedy",
+                          "dflv_commit_rollback", "dflv_gdn_workspace_size", "dflv_attn_workspace_size",
+                          "dflv_status_string"}
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert dflv.status_string(code)
+    assert dflv.status_string(0) == "ok"
+
+
+def _gdn_call(desc, **over):
+    args = dict(parent=16, n_nodes=16, q=16, k=16, v=16, beta=16, log_alpha=16, state=16, out=16,
+                factors=dflv.dflv_gdn_factors(16, 16, 16), status_dev=16)
+    args.update(over)
+    return dflv.dflv_tree_gdn_verify(desc, stream=0, **args)
+
+
+def test_gdn_host_validation(lib):
+    ok = dflv.gdn_desc(1, 22, 16, 48, 128, 128)
+    assert _gdn_call(dflv.gdn_desc(1, 65, 16, 48, 128, 128)) == dflv.DFLV_ERR_UNSUPPORTED
+    assert _gdn_call(dflv.gdn_desc(1, 22, 16, 48, 96, 128)) == dflv.DFLV_ERR_UNSUPPORTED
+    assert _gdn_call(dflv.gdn_desc(1, 22, 16, 40, 128, 128)) == dflv.DFLV_ERR_INVALID_ARG
+    assert _gdn_call(dflv.gdn_desc(0, 22, 16, 48, 128, 128)) == dflv.DFLV_ERR_INVALID_ARG
+    assert _gdn_call(ok, q=None) == dflv.DFLV_ERR_INVALID_ARG
+    assert _gdn_call(ok, state=24) == dflv.DFLV_ERR_INVALID_ARG          # misaligned
+    assert _gdn_call(ok, factors=dflv.dflv_gdn_factors(16, None, 16)) == dflv.DFLV_ERR_INVALID_ARG
+    assert dflv.dflv_gdn_workspace_size(ok) == 0
+
+
+def test_attn_host_validation(lib):
+    cache = dflv.dflv_kv_layer(16, 16, 16, 16)
+
+    def call(desc, **over):
+        args = dict(parent=16, n_nodes=16, n_past=16, q=16, k_new=16, v_new=16, cache=cache, out=16,
+                    status_dev=16)
+        args.update(over)
+        return dflv.dflv_tree_attn_verify(desc, stream=0, **args)
+
+    base = dict(B=1, N_max=22, Hq=24, Hkv=4, D=256, cap=40000, window=2048, kv_type=0, scale=0.0625)
+
+    def d(**kw):
+        x = dict(base)
+        x.update(kw)
+        return dflv.attn_desc(**x)
+
+    assert call(d(N_max=65)) == dflv.DFLV_ERR_UNSUPPORTED
+    assert call(d(D=96)) == dflv.DFLV_ERR_UNSUPPORTED
+    assert call(d(window=-1)) == dflv.DFLV_ERR_INVALID_ARG
+    assert call(d(Hq=25)) == dflv.DFLV_ERR_INVALID_ARG
+    assert call(d(cap=10)) == dflv.DFLV_ERR_CAPACITY
+    assert call(d(kv_type=7)) == dflv.DFLV_ERR_UNSUPPORTED
+    assert call(d(scale=float("nan"))) == dflv.DFLV_ERR_INVALID_ARG
+    assert call(d(), cache=dflv.dflv_kv_layer(16, 16, None, 16)) == dflv.DFLV_ERR_INVALID_ARG
+    assert call(d(), cache=dflv.dflv_kv_layer(16, 16, 18, 16)) == dflv.DFLV_ERR_INVALID_ARG  # scale rows
+    assert call(d(), q=None) == dflv.DFLV_ERR_INVALID_ARG
+    assert dflv.dflv_attn_workspace_size(d()) == 0
+
+
+def test_accept_and_commit_host_validation(lib):
+    P = 16
+    assert dflv.dflv_accept_greedy(1, 65, 100, P, P, P, P, P, P, P, P, P, stream=0) == dflv.DFLV_ERR_UNSUPPORTED
+    assert dflv.dflv_accept_greedy(0, 22, 100, P, P, P, P, P, P, P, P, P, stream=0) == dflv.DFLV_ERR_INVALID_ARG
+    assert dflv.dflv_accept_greedy(1, 22, 100, None, P, P, P, P, P, P, P, P, stream=0) == dflv.DFLV_ERR_INVALID_ARG
+    assert dflv.dflv_accept_greedy(1, 22, 100, 20, P, P, P, P, P, P, P, P, stream=0) == dflv.DFLV_ERR_INVALID_ARG
+    g = dflv.gdn_desc(1, 22, 16, 48, 128, 128)
+    fac = dflv.dflv_gdn_factors(P, P, P)
+    assert dflv.dflv_commit_rollback(g, 129, [P] * 129, [fac] * 129, None, 0, [], P, P, P, P,
+                                     stream=0) == dflv.DFLV_ERR_UNSUPPORTED
+    assert dflv.dflv_commit_rollback(g, 1, [None], [fac], None, 0, [], P, P, P, P,
+                                     stream=0) == dflv.DFLV_ERR_INVALID_ARG
+    a = dflv.attn_desc(2, 22, 24, 4, 256, 40000, 0, 0, 0.0625)
+    assert dflv.dflv_commit_rollback(g, 1, [P], [fac], a, 1, [dflv.dflv_kv_layer(P, P, P, P)], P, P, P, P,
+                                     stream=0) == dflv.DFLV_ERR_INVALID_ARG   # batch mismatch

@@ -1,0 +1,259 @@
+"""GPU parity: greedy acceptance (bit-exact), commit/rollback (state within
+tolerance, KV compaction bit-exact) and whole verify steps against the CPU
+oracle."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from gpu_util import assert_close, dev, host, zeros_status
+from test_gpu_attn import gpu_attn
+from test_gpu_gdn import gpu_gdn
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dflv():
+    import speculative_decoding_tree_layer_gb300 as pkg
+
+    pkg.build()
+    pkg.load()
+    return pkg
+
+
+def gpu_accept(dflv, logits, tokens, parent, n_nodes, expect_status=0):
+    B, N, V = logits.shape
+    keep = dict(logits=dev(logits), tokens=dev(tokens), parent=dev(parent), n_nodes=dev(n_nodes))
+    path = torch.full((B, N), -1, dtype=torch.int32, device="cuda")
+    plen = torch.zeros(B, dtype=torch.int32, device="cuda")
+    nxt = torch.zeros(B, dtype=torch.int32, device="cuda")
+    best = torch.full((B, N), -1, dtype=torch.int32, device="cuda")
+    st = zeros_status()
+    dflv.check(dflv.dflv_accept_greedy(B, N, V, keep["logits"], keep["tokens"], keep["parent"], keep["n_nodes"],
+                                       path, plen, nxt, best, st), "dflv_accept_greedy")
+    torch.cuda.synchronize()
+    assert int(st.item()) == expect_status
+    return host(path), host(plen), host(nxt), host(best)
+
+
+def _trees(rng, ns, V, kind="ddtree"):
+    parents, toks = [], []
+    for n in ns:
+        if kind == "ddtree":
+            p, t = synth.ddtree(rng, n, V)
+        else:
+            p = synth.uniform_tree(rng, n)
+            t = rng.integers(0, V, n).astype(np.int32)
+        parents.append(p)
+        toks.append(t)
+    N = max(ns)
+    parent, n_nodes = synth.batch_trees(parents, N)
+    tokens = np.zeros((len(ns), N), np.int32)
+    for b, t in enumerate(toks):
+        tokens[b, : len(t)] = t
+    return parent, n_nodes, tokens, parents
+
+
+ACCEPT = [
+    ([22], 151936, "ddtree", True),
+    ([22], 151936, "ddtree", False),
+    ([64, 5, 22], 1001, "ddtree", True),          # vocab not a multiple of 4
+    ([7, 7], 32, "uniform", True),                # tiny vocab: duplicate sibling tokens
+    ([1], 50, "uniform", False),
+]
+
+
+@pytest.mark.parametrize("case", ACCEPT)
+def test_accept_bit_exact(dflv, orc, case):
+    ns, V, kind, plant = case
+    rng = np.random.default_rng(V + sum(ns))
+    parent, n_nodes, tokens, parents = _trees(rng, ns, V, kind)
+    logits = synth.random_logits(rng, len(ns), parent.shape[1], V)
+    if plant:
+        for b, p in enumerate(parents):
+            synth.plant_path(logits, tokens, synth.deepest_path(p), b)
+    path, plen, nxt, best = gpu_accept(dflv, logits, tokens, parent, n_nodes)
+    rp, rl, rn, rb = orc.accept_greedy(logits, tokens, parent, n_nodes)
+    for b in range(len(ns)):
+        assert plen[b] == rl[b]
+        assert np.array_equal(path[b, : rl[b]], rp[b, : rl[b]])
+        assert np.array_equal(best[b, : n_nodes[b]], rb[b, : n_nodes[b]])
+        assert nxt[b] == rn[b]
+
+
+def test_accept_ties(dflv, orc):
+    V = 4096
+    parent = np.array([[-1, 0, 0, 1, 2]], np.int32)
+    tokens = np.array([[0, 7, 7, 9, 9]], np.int32)      # two children with the same token
+    logits = np.zeros((1, 5, V), np.float32)
+    logits[0, :, [7, 2000, 4000]] = 3.0                 # three-way tie in every row -> 7
+    logits[0, 1, 9] = 5.0
+    path, plen, nxt, best = gpu_accept(dflv, logits, tokens, parent, np.array([5], np.int32))
+    rp, rl, rn, rb = orc.accept_greedy(logits, tokens, parent, np.array([5], np.int32))
+    assert plen[0] == rl[0] == 3 and list(path[0, :3]) == list(rp[0, :3]) == [0, 1, 3]
+    assert np.array_equal(best, rb) and nxt[0] == rn[0] == 7
+
+
+def gpu_commit(dflv, gdn_layers, attn_layers, path, path_len, n_past, dims, expect_status=0):
+    """gdn_layers: list of dicts with device tensors state/u/g/kc; attn_layers:
+    list of dicts with device planes."""
+    B, N = path.shape
+    st = zeros_status()
+    keep = dict(path=dev(path), plen=dev(path_len), n_past=dev(n_past))
+    gd = dflv.gdn_desc(B, N, *dims["gdn"]) if gdn_layers else None
+    ad = dflv.attn_desc(B, N, *dims["attn"]) if attn_layers else None
+    rc = dflv.dflv_commit_rollback(
+        gd, len(gdn_layers), [l["state"] for l in gdn_layers],
+        [dflv.gdn_factors(l["u"], l["g"], l["kc"]) for l in gdn_layers], ad, len(attn_layers),
+        [dflv.kv_layer(l["kq"], l["vq"], l.get("ks"), l.get("vs")) for l in attn_layers],
+        keep["path"], keep["plen"], keep["n_past"], st)
+    dflv.check(rc, "dflv_commit_rollback")
+    torch.cuda.synchronize()
+    assert int(st.item()) == expect_status
+    return host(keep["n_past"])
+
+
+@pytest.mark.parametrize("kv_type", [synth.KV_Q8_0, synth.KV_Q4_0, synth.KV_F32])
+def test_commit_gdn_and_kv(dflv, orc, kv_type):
+    rng = np.random.default_rng(40 + kv_type)
+    Hk, Hv, dk, dv = 2, 6, 128, 64
+    Hq, Hkv, D = 4, 2, 64 if kv_type != synth.KV_F32 else 16
+    B, N = 3, 9
+    parents = [np.array([-1, 0, 0, 2, 3, 1, 4, 6, 6], np.int32),  # accepted path 0, 2, 3 aliases
+               synth.chain_tree(9), np.array([-1, 0, 1, 1], np.int32)]
+    parent, n_nodes = synth.batch_trees(parents, N)
+    path = np.full((B, N), -1, np.int32)
+    path[0, :5] = [0, 2, 3, 4, 6]
+    path[1, :9] = np.arange(9)
+    path[2, :1] = [0]
+    path_len = np.array([5, 9, 1], np.int32)
+    # GDN: verify on the GPU (factors), commit on the GPU; oracle decodes the path
+    ginp = synth.gdn_inputs(rng, B, N, Hk, Hv, dk, dv, state_std=0.3)
+    keep = {k: dev(v) for k, v in ginp.items()}
+    u = torch.empty((B, N, Hv, dv), device="cuda")
+    g = torch.empty((B, N, Hv), device="cuda")
+    kc = torch.empty((B, N, Hk, dk), dtype=torch.int16, device="cuda")
+    out = torch.empty((B, N, Hv, dv), device="cuda")
+    st = zeros_status()
+    dflv.check(dflv.dflv_tree_gdn_verify(dflv.gdn_desc(B, N, Hk, Hv, dk, dv), dev(parent), dev(n_nodes), keep["q"],
+                                         keep["k"], keep["v"], keep["beta"], keep["log_alpha"], keep["state"], out,
+                                         dflv.gdn_factors(u, g, kc), st))
+    # KV: a cache the tree has been written into
+    P = np.array([40, 17, 3], np.int32)
+    cap = 64
+    cache = synth.kv_cache(rng, B, Hkv, cap, D, kv_type)
+    dc = {k: (None if v is None else dev(v)) for k, v in cache.items()}
+    before = {k: (None if v is None else v.copy()) for k, v in cache.items()}
+    new_P = gpu_commit(dflv, [dict(state=keep["state"], u=u, g=g, kc=kc)],
+                       [dict(kq=dc["kq"], vq=dc["vq"], ks=dc["ks"], vs=dc["vs"])], path, path_len, P,
+                       dict(gdn=(Hk, Hv, dk, dv), attn=(Hq, Hkv, D, cap, 0, kv_type, 0.125)))
+    assert np.array_equal(new_P, P + path_len)
+    ref_state = orc.gdn_commit(ginp["q"], ginp["k"], ginp["v"], ginp["beta"], ginp["log_alpha"], path, path_len,
+                               ginp["state"])
+    assert_close(host(keep["state"]), ref_state, what="committed state")
+    orc.kv_commit(before, kv_type, path, path_len, P)
+    dt = {synth.KV_Q8_0: np.int8, synth.KV_Q4_0: np.uint8, synth.KV_F32: np.float32}[kv_type]
+    for key in ("kq", "vq", "ks", "vs"):
+        if before[key] is None:
+            continue
+        got = host(dc[key], np.uint16 if key in ("ks", "vs") else dt)
+        for b in range(B):
+            # slots below P + L are fully specified; [P + L, P + N) are not
+            hi = P[b] + path_len[b]
+            assert np.array_equal(got[b, :, :hi], before[key][b, :, :hi]), key
+            assert np.array_equal(got[b, :, P[b] + N:], before[key][b, :, P[b] + N:]), key
+
+
+def test_commit_bad_path_sets_status(dflv):
+    rng = np.random.default_rng(3)
+    B, N, Hkv, D, cap = 1, 4, 1, 64, 16
+    cache = synth.kv_cache(rng, B, Hkv, cap, D, synth.KV_Q8_0)
+    dc = {k: dev(v) for k, v in cache.items()}
+    path = np.array([[0, 1, 2, 3]], np.int32)
+    new_P = gpu_commit(dflv, [], [dict(kq=dc["kq"], vq=dc["vq"], ks=dc["ks"], vs=dc["vs"])], path,
+                       np.array([0], np.int32), np.array([2], np.int32),
+                       dict(attn=(2, Hkv, D, cap, 0, synth.KV_Q8_0, 0.125)), expect_status=dflv.DFLV_DEV_PATH)
+    assert new_P[0] == 2
+
+
+def test_tiny_case_full_step_twice(dflv, orc):
+    """The tiny end-to-end case, all on the GPU: an 8-token prefix decoded as a
+    chain from zero state and committed, then two tree verify -> accept ->
+    commit steps (7-node trees, parent[i] ~ U[0, i)), against the oracle."""
+    rng = np.random.default_rng(1234)
+    Hk = Hv = 2
+    dk = dv = 16
+    Hq = Hkv = 1
+    D, V, P0, cap = 16, 32, 64, 128
+    gdims = (Hk, Hv, dk, dv)
+    adims = (Hq, Hkv, D, cap, 0, synth.KV_F32, 0.25)
+    # ---- prefix: 8-token chain from the zero state
+    pre = synth.gdn_inputs(rng, 1, 8, Hk, Hv, dk, dv)
+    pre["state"] = np.zeros((1, Hv, dv, dk), np.float32)
+    cpar, cn = synth.batch_trees([synth.chain_tree(8)], 8)
+    _, u, g, kc = gpu_gdn(dflv, cpar, cn, pre, Hk, Hv, dk, dv)
+    state = dev(pre["state"])
+    fac = dict(state=state, u=dev(u), g=dev(g), kc=dev(kc.view(np.uint16)))
+    full = np.arange(8, dtype=np.int32)[None]
+    gpu_commit(dflv, [fac], [], full, np.array([8], np.int32), np.array([0], np.int32), dict(gdn=gdims))
+    ref_state = orc.gdn_commit(pre["q"], pre["k"], pre["v"], pre["beta"], pre["log_alpha"], full,
+                               np.array([8], np.int32), pre["state"])
+    assert_close(host(state), ref_state, what="prefix state")
+    cache = synth.kv_cache(rng, 1, Hkv, cap, D, synth.KV_F32)
+    ref_cache = synth.copy_cache(cache)
+    dcache = {k: (None if v is None else dev(v)) for k, v in cache.items()}
+    n_past = dev(np.array([P0], np.int32))
+    ref_P = P0
+    gstate_ref = ref_state
+    for step in range(2):
+        par = synth.uniform_tree(rng, 7)
+        parent, n_nodes = synth.batch_trees([par], 7)
+        tokens = rng.integers(0, V, (1, 7)).astype(np.int32)
+        gi = synth.gdn_inputs(rng, 1, 7, Hk, Hv, dk, dv, state=False)
+        ai = synth.attn_inputs(rng, 1, 7, Hq, Hkv, D)
+        logits = synth.random_logits(rng, 1, 7, V)
+        synth.plant_path(logits, tokens, synth.deepest_path(par))
+        # GPU step
+        gk = {k: dev(v) for k, v in gi.items()}
+        ak = {k: dev(v) for k, v in ai.items()}
+        kp, kn = dev(parent), dev(n_nodes)
+        go = torch.empty((1, 7, Hv, dv), device="cuda")
+        u = torch.empty_like(go)
+        g = torch.empty((1, 7, Hv), device="cuda")
+        kc = torch.empty((1, 7, Hk, dk), dtype=torch.int16, device="cuda")
+        ao = torch.empty((1, 7, Hq, D), device="cuda")
+        st = zeros_status()
+        dflv.check(dflv.dflv_tree_gdn_verify(dflv.gdn_desc(1, 7, *gdims), kp, kn, gk["q"], gk["k"], gk["v"],
+                                             gk["beta"], gk["log_alpha"], state, go, dflv.gdn_factors(u, g, kc), st))
+        dflv.check(dflv.dflv_tree_attn_verify(dflv.attn_desc(1, 7, *adims), kp, kn, n_past, ak["q"], ak["k_new"],
+                                              ak["v_new"], dflv.kv_layer(dcache["kq"], dcache["vq"]), ao, st))
+        lg, tk = dev(logits), dev(tokens)
+        path = torch.empty((1, 7), dtype=torch.int32, device="cuda")
+        plen = torch.empty(1, dtype=torch.int32, device="cuda")
+        nxt = torch.empty(1, dtype=torch.int32, device="cuda")
+        best = torch.empty((1, 7), dtype=torch.int32, device="cuda")
+        dflv.check(dflv.dflv_accept_greedy(1, 7, V, lg, tk, kp, kn, path, plen, nxt, best, st))
+        dflv.check(dflv.dflv_commit_rollback(dflv.gdn_desc(1, 7, *gdims), 1, [state], [dflv.gdn_factors(u, g, kc)],
+                                             dflv.attn_desc(1, 7, *adims), 1,
+                                             [dflv.kv_layer(dcache["kq"], dcache["vq"])], path, plen, n_past, st))
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        # oracle step
+        gi_ref = dict(gi, state=gstate_ref)
+        ref_go = orc.tree_gdn_verify(parent, n_nodes, gi["q"], gi["k"], gi["v"], gi["beta"], gi["log_alpha"],
+                                     gstate_ref)
+        ref_ao = orc.tree_attn_verify(parent, n_nodes, np.array([ref_P], np.int32), ai["q"], ai["k_new"],
+                                      ai["v_new"], ref_cache, 0, synth.KV_F32)
+        rp, rl, rn, _ = orc.accept_greedy(logits, tokens, parent, n_nodes)
+        gstate_ref = orc.gdn_commit(gi["q"], gi["k"], gi["v"], gi["beta"], gi["log_alpha"], rp, rl, gstate_ref)
+        orc.kv_commit(ref_cache, synth.KV_F32, rp, rl, np.array([ref_P], np.int32))
+        ref_P += int(rl[0])
+        assert_close(host(go), ref_go, what=f"step {step} gdn out")
+        assert_close(host(ao), ref_ao, what=f"step {step} attn out")
+        L = int(host(plen)[0])
+        assert L == rl[0] and np.array_equal(host(path)[0, :L], rp[0, :L]) and int(host(nxt)[0]) == rn[0]
+        assert int(host(n_past)[0]) == ref_P
+        assert_close(host(state), gstate_ref, what=f"step {step} state")
+        hc = host(dcache["kq"])
+        assert np.array_equal(hc[:, :, :ref_P], ref_cache["kq"][:, :, :ref_P])

@@ -1,0 +1,159 @@
+"""GPU parity: attention tree verify (libdflv) against the CPU oracle.
+
+Outputs within the float tolerance of tests/gpu_util.py; the tree's
+quantised keys/values written into cache slots [P, P + n) bit-identical to
+the oracle's quantiser, every other slot untouched; sampled rows at the full
+long-context size; capacity/topology errors through the status word.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from gpu_util import assert_close, dev, host, zeros_status
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dflv():
+    import speculative_decoding_tree_layer_gb300 as pkg
+
+    pkg.build()
+    pkg.load()
+    return pkg
+
+
+def _plane_np_dtype(key, kv_type):
+    if key in ("ks", "vs"):
+        return np.uint16
+    return {synth.KV_Q8_0: np.int8, synth.KV_Q4_0: np.uint8, synth.KV_F32: np.float32}[kv_type]
+
+
+def gpu_attn(dflv, parent, n_nodes, n_past, inp, cache, window, kv_type, Hq, Hkv, D, expect_status=0,
+             rows_only=None):
+    B, N = parent.shape
+    cap = cache["kq"].shape[2]
+    keep = {k: dev(v) for k, v in inp.items()}
+    dc = {k: (None if v is None else dev(v)) for k, v in cache.items()}
+    keep.update(parent=dev(parent), n_nodes=dev(n_nodes), n_past=dev(n_past))
+    out = torch.full((B, N, Hq, D), float("nan"), dtype=torch.float32, device="cuda")
+    st = zeros_status()
+    desc = dflv.attn_desc(B, N, Hq, Hkv, D, cap, window, kv_type, 1.0 / np.sqrt(D))
+    rc = dflv.dflv_tree_attn_verify(desc, keep["parent"], keep["n_nodes"], keep["n_past"], keep["q"],
+                                    keep["k_new"], keep["v_new"], dflv.kv_layer(dc["kq"], dc["vq"], dc["ks"], dc["vs"]),
+                                    out, st)
+    dflv.check(rc, "dflv_tree_attn_verify")
+    torch.cuda.synchronize()
+    assert int(st.item()) == expect_status
+    planes = {k: (None if v is None else host(v, _plane_np_dtype(k, kv_type))) for k, v in dc.items()}
+    return host(out), planes
+
+
+def make_case(rng, kv_type, ns, P, cap, Hq, Hkv, D, tree="ddtree", scale_std=0.02):
+    parents = []
+    for n in ns:
+        if tree == "ddtree":
+            parents.append(synth.ddtree(rng, n, 1000)[0])
+        elif tree == "chain":
+            parents.append(synth.chain_tree(n))
+        else:
+            parents.append(synth.uniform_tree(rng, n))
+    N = max(ns)
+    parent, n_nodes = synth.batch_trees(parents, N)
+    inp = synth.attn_inputs(rng, len(ns), N, Hq, Hkv, D)
+    cache = synth.kv_cache(rng, len(ns), Hkv, cap, D, kv_type, scale_std=scale_std)
+    n_past = np.asarray(P, np.int32) if np.ndim(P) else np.full(len(ns), P, np.int32)
+    return parent, n_nodes, n_past, inp, cache
+
+
+def check_against_oracle(dflv, orc, parent, n_nodes, n_past, inp, cache, window, kv_type, Hq, Hkv, D):
+    out, planes = gpu_attn(dflv, parent, n_nodes, n_past, inp, cache, window, kv_type, Hq, Hkv, D)
+    ref_cache = synth.copy_cache(cache)
+    ref = orc.tree_attn_verify(parent, n_nodes, n_past, inp["q"], inp["k_new"], inp["v_new"], ref_cache,
+                               window, kv_type)
+    e = 0.0
+    for b in range(parent.shape[0]):
+        e = max(e, assert_close(out[b, : n_nodes[b]], ref[b, : n_nodes[b]], what=f"o[b={b}]"))
+    for key in ("kq", "vq", "ks", "vs"):
+        if ref_cache[key] is None:
+            continue
+        assert np.array_equal(planes[key], ref_cache[key]), f"cache plane {key} differs"
+    return e
+
+
+SMALL = [
+    # kv_type, ns, P, cap, Hq, Hkv, D, window, tree
+    (synth.KV_Q8_0, [7], 100, 128, 4, 2, 256, 0, "uniform"),
+    (synth.KV_Q8_0, [22, 9], [300, 57], 400, 6, 1, 256, 64, "ddtree"),
+    (synth.KV_Q4_0, [22, 9], [300, 57], 400, 6, 1, 256, 64, "ddtree"),
+    (synth.KV_Q8_0, [5], 0, 16, 2, 2, 128, 0, "uniform"),          # empty prefix
+    (synth.KV_Q4_0, [13], 200, 256, 8, 2, 64, 1, "uniform"),       # window 1: only itself
+    (synth.KV_Q8_0, [64], 513, 600, 6, 1, 256, 20, "chain"),       # window shorter than the chain
+    (synth.KV_Q4_0, [64, 3], [1000, 5], 1100, 12, 2, 128, 0, "ddtree"),
+    (synth.KV_Q8_0, [1], 77, 80, 24, 4, 256, 2048, "uniform"),     # window covering everything
+]
+
+
+@pytest.mark.parametrize("case", SMALL)
+def test_attn_tree_verify_matches_oracle(dflv, orc, case):
+    kv_type, ns, P, cap, Hq, Hkv, D, window, tree = case
+    rng = np.random.default_rng(len(ns) * 1000 + cap + D + window)
+    args = make_case(rng, kv_type, ns, P, cap, Hq, Hkv, D, tree)
+    check_against_oracle(dflv, orc, *args, window, kv_type, Hq, Hkv, D)
+
+
+def test_attn_f32_cache_tiny_case(dflv, orc):
+    # 1 attention head, head size 16, fp32 cache of 64 tokens, full attention
+    rng = np.random.default_rng(1234)
+    args = make_case(rng, synth.KV_F32, [7], 64, 80, 1, 1, 16, "uniform")
+    check_against_oracle(dflv, orc, *args, 0, synth.KV_F32, 1, 1, 16)
+
+
+def test_attn_full_size_32k_q8_window(dflv, orc):
+    # full-attention layer of a 27B-class target: 24 query heads, 4 KV heads,
+    # head size 256, q8_0 cache of 32,768 tokens, window 2048, 22-node tree
+    rng = np.random.default_rng(1236)
+    args = make_case(rng, synth.KV_Q8_0, [22], 32768, 32768 + 64, 24, 4, 256, "ddtree")
+    e = check_against_oracle(dflv, orc, *args, 2048, synth.KV_Q8_0, 24, 4, 256)
+    print(f"full-size attention max rel err {e:.2e}")
+
+
+@pytest.mark.parametrize("n", [8, 22, 64])
+def test_attn_long_context_q4_full_attention_sampled(dflv, orc, n):
+    # 8 sequences, 131,072-token q4_0 cache, full attention: sampled rows
+    rng = np.random.default_rng(1239 + n)
+    B, P, Hq, Hkv, D = 8, 131072, 24, 4, 256
+    parents = [synth.ddtree(rng, n, 151936)[0] for _ in range(B)]
+    parent, n_nodes = synth.batch_trees(parents, n)
+    inp = synth.attn_inputs(rng, B, n, Hq, Hkv, D)
+    cache = synth.kv_cache(rng, B, Hkv, P + 64, D, synth.KV_Q4_0)
+    n_past = np.full(B, P, np.int32)
+    out, planes = gpu_attn(dflv, parent, n_nodes, n_past, inp, cache, 0, synth.KV_Q4_0, Hq, Hkv, D)
+    rows = []
+    for b in (0, 3, 7):
+        for i in (0, n - 1, int(rng.integers(0, n))):
+            rows.append((b * n + i) * Hq + int(rng.integers(0, Hq)))
+    rows = np.unique(np.asarray(rows, np.int32))
+    ref_cache = synth.copy_cache(cache)
+    ref = orc.tree_attn_verify(parent, n_nodes, n_past, inp["q"], inp["k_new"], inp["v_new"], ref_cache, 0,
+                               synth.KV_Q4_0, rows=rows)
+    flat_o, flat_r = out.reshape(-1, D), ref.reshape(-1, D)
+    # the tolerance's rms is taken over the sampled rows
+    assert_close(flat_o[rows], flat_r[rows], what="sampled rows")
+    for key in ("kq", "vq", "ks", "vs"):
+        sl = np.s_[:, :, P:P + n]
+        assert np.array_equal(planes[key][sl], ref_cache[key][sl]), key
+
+
+def test_attn_errors_set_status(dflv):
+    rng = np.random.default_rng(9)
+    # capacity: P + n > cap
+    parent, n_nodes, n_past, inp, cache = make_case(rng, synth.KV_Q8_0, [5], 30, 32, 2, 1, 64, "uniform")
+    gpu_attn(dflv, parent, n_nodes, n_past, inp, cache, 0, synth.KV_Q8_0, 2, 1, 64,
+             expect_status=dflv.DFLV_DEV_CAPACITY)
+    # topology
+    parent, n_nodes, n_past, inp, cache = make_case(rng, synth.KV_Q8_0, [5], 10, 32, 2, 1, 64, "uniform")
+    parent[0, 3] = 4
+    out, planes = gpu_attn(dflv, parent, n_nodes, n_past, inp, cache, 0, synth.KV_Q8_0, 2, 1, 64,
+                           expect_status=dflv.DFLV_DEV_TOPOLOGY)
