@@ -175,9 +175,7 @@ __global__ void accept_walk_kernel(AcceptArgs a) {
 }  // namespace
 
 cudaError_t launch_accept_greedy(const AcceptArgs& a, cudaStream_t stream) {
-    int dev = 0, sms = 152;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int sms = sm_count_cached();
     // enough CTAs to cover the SMs a few times, at most 8 per row (portable cluster)
     const long rows = (long)a.B * a.N_max;
     int cs = 1;

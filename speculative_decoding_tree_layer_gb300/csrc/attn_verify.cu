@@ -669,13 +669,10 @@ RowTiling choose_tiling(const AttnVerifyArgs& a, int sm_count) {
 template <int D, int TYPE>
 cudaError_t launch_main(const AttnVerifyArgs& a, cudaStream_t stream) {
     using S = AttnSmem<D, TYPE>;
-    int dev = 0, sms = 152;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const RowTiling t = choose_tiling(a, sms);
+    const RowTiling t = choose_tiling(a, sm_count_cached());
     const size_t smem = S::total(t.RT);
     auto kern = attn_tree_verify_kernel<D, TYPE>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_smem(kern, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(t.CS, t.n_rt * a.Hkv, a.B);

@@ -185,7 +185,7 @@ cudaError_t launch_commit_rollback(const CommitArgs& a, cudaStream_t stream) {
             const size_t kv = (size_t)a.N_max * code_bytes;
             if (kv > smem) smem = kv;
         }
-        cudaError_t e = cudaFuncSetAttribute(commit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = ensure_smem(commit_kernel, smem);
         if (e != cudaSuccess) return e;
         commit_kernel<<<(unsigned)blocks, kCommitThreads, smem, stream>>>(a);
         e = cudaGetLastError();

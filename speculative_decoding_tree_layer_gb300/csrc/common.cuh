@@ -147,3 +147,54 @@ DFLV_DEVINL int popc64(uint64_t x) { return __popcll(x); }
 DFLV_DEVINL int ffs64(uint64_t x) { return __ffsll((long long)x) - 1; }
 
 }  // namespace dflv
+
+// ---------------------------------------------------------------- host-side launch helpers
+#include <atomic>
+#include <mutex>
+
+namespace dflv {
+
+// SM count of the current device, queried once per device.
+inline int sm_count_cached() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 152;
+    cache[dev].store(v, std::memory_order_relaxed);
+    return v;
+}
+
+// Raises a kernel's dynamic shared-memory limit only when a launch needs
+// more than was already granted to that kernel on this device, so
+// steady-state launches (and stream capture) make no attribute calls.
+inline cudaError_t ensure_smem_ptr(const void* kern, size_t bytes) {
+    struct Grant {
+        const void* kern;
+        int dev;
+        size_t bytes;
+    };
+    static std::mutex mu;
+    static Grant grants[256];
+    static int n_grants = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    Grant* g = nullptr;
+    for (int i = 0; i < n_grants; ++i)
+        if (grants[i].kern == kern && grants[i].dev == dev) g = &grants[i];
+    if (g && bytes <= g->bytes) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) return e;
+    if (g) g->bytes = bytes;
+    else if (n_grants < 256) grants[n_grants++] = Grant{kern, dev, bytes};
+    return cudaSuccess;
+}
+
+template <typename Kernel>
+inline cudaError_t ensure_smem(Kernel kern, size_t bytes) {
+    return ensure_smem_ptr(reinterpret_cast<const void*>(kern), bytes);
+}
+
+}  // namespace dflv

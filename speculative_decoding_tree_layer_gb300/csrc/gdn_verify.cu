@@ -14,18 +14,18 @@
 // the tree's ancestor mask.  With u_i = beta_i (v_i - alpha_i S_par(i) k_i)
 // and g_i = sum of log alpha over i's ancestors-or-self,
 //     S_i = e^{g_i} S_0 + sum_{l in anc*(i)} e^{g_i - g_l} u_l k_l^T,
-//     (I + A) U = R,   A_il = beta_i e^{g_i - g_l} (k_i . k_l)  for l a strict ancestor of i,
-//                      R_i  = beta_i v_i - beta_i e^{g_i} (S_0 k_i),
-//     o_i = e^{g_i} (S_0 q_i) + sum_{l in anc*(i)} e^{g_i - g_l} (k_l . q_i) u_l.
-// A is strictly lower triangular (parent < child), so T = (I + A)^{-1} is
-// unit lower triangular and nonzero only on ancestor pairs.  A, T and the
-// output mixing matrix MT = M T depend on k, q, beta and the decays only --
-// not on the state -- so every row of S_0 is independent: a CTA owns RB rows
-// of one head, streams them from HBM once through the bulk-copy (TMA)
-// engine, forms S_0[rows] . [K | Q] on the tensor cores (fp32 state split
-// into bf16 hi + lo, k and q exact in bf16), and finishes U and o for its
-// rows with the small ancestor-sparse T and MT.  It writes u, g and a copy
-// of k as the factors commit needs, and never writes S_0 (rollback is free).
+//     u_i + sum_{l in anc(i)} A_il u_l = R_i,
+//         A_il = beta_i e^{g_i - g_l} (k_i . k_l),   R_i = beta_i v_i - beta_i e^{g_i} (S_0 k_i),
+//     o_i = e^{g_i} (S_0 q_i) + sum_{l in anc*(i)} M_il u_l,   M_il = e^{g_i - g_l} (k_l . q_i).
+// A and M depend on k, q, beta and the decays only -- not on the state -- so
+// every row of S_0 is independent: a CTA owns RB rows of one head, streams
+// them from HBM once through the bulk-copy (TMA) engine, forms
+// S_0[rows] . [K | Q] on the tensor cores (fp32 state split into bf16 hi +
+// lo, k and q exact in bf16), then solves the unit lower-triangular system
+// for u by substitution over the tree's depth levels (all nodes of a level
+// at once, one warp per node, lanes over rows) and mixes the outputs.  It
+// writes u, g and a copy of k as the factors commit needs, and never writes
+// S_0 (rollback is free).
 #include "common.cuh"
 #include "kernels.h"
 #include "tree.cuh"
@@ -34,24 +34,46 @@ namespace dflv {
 
 namespace {
 
-constexpr int kGdnThreads = 128;
+constexpr int kGdnThreads = 256;
+constexpr int kGdnWarps = kGdnThreads / 32;
 
 struct GdnSmemLayout {
     int NP, DK, RB, KS;
-    size_t off_S, off_K, off_Q, off_A, off_M, off_T, off_MT, off_R, off_SQ, total;
+    size_t off_S, off_K, off_Q, off_A, off_M, off_R, off_SQ, total;
     __host__ __device__ GdnSmemLayout(int np, int dk, int rb) : NP(np), DK(dk), RB(rb), KS(dk + 16) {
-        off_S = 2304;  // header: mbarrier (64 B) + per-node arrays (2112 B), rounded up
+        off_S = 3200;  // header: mbarrier + per-node arrays (3136 B), rounded up to 128
         off_K = off_S + (size_t)RB * DK * 4;
         off_Q = off_K + (size_t)NP * KS * 2;
         off_A = off_Q + (size_t)NP * KS * 2;
         off_M = off_A + (size_t)NP * NP * 4;
-        off_T = off_M + (size_t)NP * NP * 4;
-        off_MT = off_T + (size_t)NP * NP * 4;
-        off_R = off_MT + (size_t)NP * NP * 4;
+        off_R = off_M + (size_t)NP * NP * 4;
         off_SQ = off_R + (size_t)NP * RB * 4;
         total = off_SQ + (size_t)NP * RB * 4;
     }
 };
+
+// sum over the set bits l of m of w[l] * x[l * stride], four terms at a time
+// so the shared-memory loads of a group are in flight together
+DFLV_DEVINL float masked_dot(uint64_t m, const float* __restrict__ w, const float* __restrict__ x, int stride) {
+    float acc = 0.f;
+    while (m) {
+        int l[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            l[k] = m ? ffs64(m) : -1;
+            m &= m - 1;
+        }
+        float wv[4], xv[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            wv[k] = l[k] >= 0 ? w[l[k]] : 0.f;
+            xv[k] = l[k] >= 0 ? x[l[k] * stride] : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc = fmaf(wv[k], xv[k], acc);
+    }
+    return acc;
+}
 
 template <int DK, int RB>
 __global__ void __launch_bounds__(kGdnThreads)
@@ -61,10 +83,13 @@ __global__ void __launch_bounds__(kGdnThreads)
     constexpr int KS = DK + 16;  // bf16 row stride: conflict-free 8-byte fragment loads
 
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+    int32_t* misc_s = reinterpret_cast<int32_t*>(smem + 16);  // [0] = deepest level
     int32_t* par_s = reinterpret_cast<int32_t*>(smem + 64);
     int32_t* depth_s = par_s + kMaxNodes;
-    uint64_t* amask_s = reinterpret_cast<uint64_t*>(smem + 64 + 512);
-    float* beta_s = reinterpret_cast<float*>(smem + 64 + 1024);
+    int32_t* order_s = depth_s + kMaxNodes;           // nodes sorted by depth
+    int32_t* lvl_s = order_s + kMaxNodes;             // first index of each level in order_s (65)
+    uint64_t* amask_s = reinterpret_cast<uint64_t*>(smem + 64 + 4 * 256 + 512);
+    float* beta_s = reinterpret_cast<float*>(smem + 64 + 4 * 256 + 512 + 512);
     float* la_s = beta_s + kMaxNodes;
     float* g_s = la_s + kMaxNodes;
     float* G_s = g_s + kMaxNodes;
@@ -73,8 +98,6 @@ __global__ void __launch_bounds__(kGdnThreads)
     uint16_t* Q_s = reinterpret_cast<uint16_t*>(smem + L.off_Q);
     float* A_s = reinterpret_cast<float*>(smem + L.off_A);
     float* M_s = reinterpret_cast<float*>(smem + L.off_M);
-    float* T_s = reinterpret_cast<float*>(smem + L.off_T);
-    float* MT_s = reinterpret_cast<float*>(smem + L.off_MT);
     float* R_s = reinterpret_cast<float*>(smem + L.off_R);
     float* SQ_s = reinterpret_cast<float*>(smem + L.off_SQ);
 
@@ -87,6 +110,7 @@ __global__ void __launch_bounds__(kGdnThreads)
     if (tid == 0) {
         mbar_init(bar, 1);
         fence_mbar_init();
+        misc_s[0] = 0;
     }
     __syncthreads();
     grid_dependency_wait();
@@ -106,18 +130,27 @@ __global__ void __launch_bounds__(kGdnThreads)
         return;
     }
 
-    // 3. Per-node scalars and the node keys / queries of q/k head hk.
+    // 3. Per-node scalars, the node keys / queries of q/k head hk, and the
+    //    nodes ordered by depth (level d = order_s[lvl_s[d] .. lvl_s[d+1])).
     for (int i = tid; i < n; i += kGdnThreads) {
-        size_t s = ((size_t)b * N + i) * a.Hv + h;
+        const size_t s = ((size_t)b * N + i) * a.Hv + h;
         beta_s[i] = __ldg(a.beta + s);
         la_s[i] = __ldg(a.log_alpha + s);
+        const int d = depth_s[i];
+        int pos = 0;
+        for (int j = 0; j < n; ++j) {
+            const int dj = depth_s[j];
+            pos += (dj < d) || (dj == d && j < i);
+        }
+        order_s[pos] = i;
+        atomicMax(misc_s, d);
     }
     constexpr int CH = DK / 8;  // 16-byte chunks per bf16 row
     for (int idx = tid; idx < NP * CH; idx += kGdnThreads) {
-        int i = idx / CH, c = idx % CH;
+        const int i = idx / CH, c = idx % CH;
         uint4 kv = make_uint4(0, 0, 0, 0), qv = make_uint4(0, 0, 0, 0);
         if (i < n) {
-            size_t off = (((size_t)b * N + i) * a.Hk + hk) * DK + c * 8;
+            const size_t off = (((size_t)b * N + i) * a.Hk + hk) * DK + c * 8;
             kv = __ldg(reinterpret_cast<const uint4*>(a.k + off));
             qv = __ldg(reinterpret_cast<const uint4*>(a.q + off));
         }
@@ -125,8 +158,13 @@ __global__ void __launch_bounds__(kGdnThreads)
         *reinterpret_cast<uint4*>(Q_s + i * KS + c * 8) = qv;
     }
     __syncthreads();
-
-    // cumulative log decay over the ancestors-or-self, root first
+    const int maxd = misc_s[0];
+    for (int d = tid; d <= maxd + 1; d += kGdnThreads) {
+        int c = 0;
+        for (int j = 0; j < n; ++j) c += depth_s[j] < d;
+        lvl_s[d] = c;
+    }
+    // cumulative log decay over the ancestors-or-self
     for (int i = tid; i < n; i += kGdnThreads) {
         float g = 0.f;
         for (uint64_t m = amask_s[i]; m; m &= m - 1) g += la_s[ffs64(m)];
@@ -140,7 +178,7 @@ __global__ void __launch_bounds__(kGdnThreads)
     //    one 8-byte load fills both halves of its fragment registers.
     {
         const int nt_count = NP / 8, tiles = (2 * NP / 16) * nt_count;
-        for (int tile = warp; tile < tiles; tile += kGdnThreads / 32) {
+        for (int tile = warp; tile < tiles; tile += kGdnWarps) {
             const int mt = tile / nt_count, nt = tile % nt_count;
             const uint16_t* Ap = (mt * 16 < NP) ? K_s + (mt * 16) * KS : Q_s + (mt * 16 - NP) * KS;
             const uint16_t* Bp = K_s + (nt * 8 + gq) * KS;
@@ -148,14 +186,14 @@ __global__ void __launch_bounds__(kGdnThreads)
 #pragma unroll
             for (int ks = 0; ks < DK / 16; ++ks) {
                 const int col = ks * 16 + tq * 4;
-                uint2 a0 = *reinterpret_cast<const uint2*>(Ap + gq * KS + col);
-                uint2 a1 = *reinterpret_cast<const uint2*>(Ap + (gq + 8) * KS + col);
-                uint2 bb = *reinterpret_cast<const uint2*>(Bp + col);
+                const uint2 a0 = *reinterpret_cast<const uint2*>(Ap + gq * KS + col);
+                const uint2 a1 = *reinterpret_cast<const uint2*>(Ap + (gq + 8) * KS + col);
+                const uint2 bb = *reinterpret_cast<const uint2*>(Bp + col);
                 const uint32_t af[4] = {a0.x, a1.x, a0.y, a1.y};
                 const uint32_t bf[2] = {bb.x, bb.y};
                 mma_bf16_16816(d, af, bf);
             }
-            int row = mt * 16 + gq, col = nt * 8 + tq * 2;
+            const int row = mt * 16 + gq, col = nt * 8 + tq * 2;
             float* dst = (row < NP) ? A_s + row * NP : M_s + (row - NP) * NP;
             dst[col] = d[0];
             dst[col + 1] = d[1];
@@ -174,49 +212,12 @@ __global__ void __launch_bounds__(kGdnThreads)
         A_s[i * NP + l] = (anc && l != i) ? beta_s[i] * dec * A_s[i * NP + l] : 0.f;
         M_s[i * NP + l] = anc ? dec * M_s[i * NP + l] : 0.f;
     }
-    __syncthreads();
 
-    // 6. T = (I + A)^{-1}, one column per thread, rows in node (topological)
-    //    order; only ancestor pairs are nonzero: T_ij = -sum_{j <= l < i, l in anc(i)} A_il T_lj.
-    for (int j = tid; j < n; j += kGdnThreads) {
-        for (int i = j; i < n; ++i) {
-            const uint64_t mi = amask_s[i];
-            float t = 0.f;
-            if ((mi >> j) & 1ull) {
-                if (i == j) {
-                    t = 1.f;
-                } else {
-                    float acc = 0.f;
-                    for (uint64_t m = mi & ~(1ull << i) & (~0ull << j); m; m &= m - 1) {
-                        const int l = ffs64(m);
-                        acc = fmaf(A_s[i * NP + l], T_s[l * NP + j], acc);
-                    }
-                    t = -acc;
-                }
-            }
-            T_s[i * NP + j] = t;
-        }
-    }
-    __syncthreads();
-
-    // 7. Output mixing MT = M T (ancestor-sparse).
-    for (int idx = tid; idx < n * n; idx += kGdnThreads) {
-        const int i = idx / n, j = idx % n;
-        const uint64_t mi = amask_s[i];
-        float acc = 0.f;
-        if ((mi >> j) & 1ull)
-            for (uint64_t m = mi & (~0ull << j); m; m &= m - 1) {
-                const int l = ffs64(m);
-                acc = fmaf(M_s[i * NP + l], T_s[l * NP + j], acc);
-            }
-        MT_s[i * NP + j] = acc;
-    }
-
-    // 8. S_0[rows] . [K | Q] on the tensor cores, fp32 state as bf16 hi + lo.
+    // 6. S_0[rows] . [K | Q] on the tensor cores, fp32 state as bf16 hi + lo.
     if (!mbar_wait_bounded(bar, 0, a.status)) return;
     {
-        constexpr int WM = RB / 16;               // m tiles (16 rows each)
-        constexpr int WN = (kGdnThreads / 32) / WM; // warps sharing one m tile
+        constexpr int WM = RB / 16;            // m tiles (16 rows each)
+        constexpr int WN = kGdnWarps / WM;     // warps sharing one m tile
         const int mt = warp % WM, wn = warp / WM;
         const int ntiles = 2 * NP / 8;
         constexpr int kMaxJ = (2 * kMaxNodes / 8 + WN - 1) / WN;
@@ -264,7 +265,7 @@ __global__ void __launch_bounds__(kGdnThreads)
     }
     __syncthreads();
 
-    // 9. R_j = beta_j (v_j - e^{g_j} S_0 k_j) for this CTA's rows.
+    // 7. R_j = beta_j (v_j - e^{g_j} S_0 k_j) for this CTA's rows.
     for (int idx = tid; idx < n * RB; idx += kGdnThreads) {
         const int j = idx / RB, r = idx % RB;
         const float vv = bf16_bits_to_float(__ldg(a.v + (((size_t)b * N + j) * a.Hv + h) * a.dv + r0 + r));
@@ -272,22 +273,28 @@ __global__ void __launch_bounds__(kGdnThreads)
     }
     __syncthreads();
 
-    // 10. u = T R and o = e^{g} SQ + MT R, rows of this CTA.
+    // 8. u_i = R_i - sum_{l in anc(i)} A_il u_l, level by level (a node's
+    //    ancestors sit on shallower levels); R_s becomes U in place.
+    for (int d = 1; d <= maxd; ++d) {
+        const int l0 = lvl_s[d], l1 = lvl_s[d + 1];
+        for (int idx = l0 * RB + tid; idx < l1 * RB; idx += kGdnThreads) {
+            const int i = order_s[idx / RB], r = idx % RB;
+            const uint64_t m = amask_s[i] & ~(1ull << i);
+            R_s[i * RB + r] -= masked_dot(m, A_s + i * NP, R_s + r, RB);
+        }
+        __syncthreads();
+    }
+
+    // 9. o_i = e^{g_i} SQ_i + sum_{l in anc*(i)} M_il u_l; u and o to global.
     for (int idx = tid; idx < n * RB; idx += kGdnThreads) {
         const int i = idx / RB, r = idx % RB;
-        float U = 0.f, O = G_s[i] * SQ_s[i * RB + r];
-        for (uint64_t m = amask_s[i]; m; m &= m - 1) {
-            const int j = ffs64(m);
-            const float rj = R_s[j * RB + r];
-            U = fmaf(T_s[i * NP + j], rj, U);
-            O = fmaf(MT_s[i * NP + j], rj, O);
-        }
+        const float O = G_s[i] * SQ_s[i * RB + r] + masked_dot(amask_s[i], M_s + i * NP, R_s + r, RB);
         const size_t off = (((size_t)b * N + i) * a.Hv + h) * a.dv + r0 + r;
-        a.u[off] = U;
+        a.u[off] = R_s[i * RB + r];
         a.out[off] = O;
     }
 
-    // 11. The remaining factors, once per (sequence, head) / (sequence, q/k head).
+    // 10. The remaining factors, once per (sequence, head) / (sequence, q/k head).
     if (blockIdx.x == 0) {
         for (int i = tid; i < n; i += kGdnThreads) a.g[((size_t)b * N + i) * a.Hv + h] = g_s[i];
         if (h % (a.Hv / a.Hk) == 0)
@@ -304,7 +311,7 @@ cudaError_t launch_dk_rb(const GdnVerifyArgs& a, cudaStream_t stream) {
     const int NP = ((a.N_max + 15) / 16) * 16;
     const GdnSmemLayout L(NP, DK, RB);
     auto kern = gdn_tree_verify_kernel<DK, RB>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
+    cudaError_t e = ensure_smem(kern, L.total);
     if (e != cudaSuccess) return e;
     dim3 grid(a.dv / RB, a.Hv, a.B);
     kern<<<grid, kGdnThreads, L.total, stream>>>(a, NP);
