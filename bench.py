@@ -312,8 +312,9 @@ class GpuStep:
         if ev is not None:
             ev[N_LAYERS][1].record()
             ev[N_LAYERS + 1][0].record()
-        chk(dflv.dflv_commit_rollback(self.gdn_desc, N_GDN, self.states, self.factors, self.attn_desc, N_ATTN,
-                                      self.caches, self.path, self.path_len, self.n_past, self.status), "commit")
+        chk(dflv.dflv_commit_rollback(self.gdn_desc, len(self.states), self.states, self.factors, self.attn_desc,
+                                      len(self.caches), self.caches, self.path, self.path_len, self.n_past,
+                                      self.status), "commit")
         if ev is not None:
             ev[N_LAYERS + 1][1].record()
 
@@ -498,6 +499,37 @@ def reduce_max(world, x):
     return float(t.item())
 
 
+# ---------------------------------------------------------------------------- profiling mode
+def profile_one(kind, launches):
+    """One kernel of the step on its own workload (the first layer of that
+    kind, or accept / commit of one step), launched back to back."""
+    import torch
+
+    import speculative_decoding_tree_layer_gb300 as dflv
+
+    dflv.load()
+    torch.cuda.set_device(0)
+    rng = np.random.default_rng(SEED)
+    host = make_host_inputs(rng, n_layers=4)
+    S = GpuStep(host, torch, dflv)
+    L = next(L for L in S.layers if L["kind"] == ("attn" if kind == "attn" else "gdn"))
+    for _ in range(launches):
+        if kind == "gdn":
+            dflv.check(dflv.dflv_tree_gdn_verify(S.gdn_desc, S.parent, S.n_nodes, L["q"], L["k"], L["v"], L["beta"],
+                                                 L["log_alpha"], L["state"], L["out"], L["fac"], S.status))
+        elif kind == "attn":
+            dflv.check(dflv.dflv_tree_attn_verify(S.attn_desc, S.parent, S.n_nodes, S.n_past, L["q"], L["k_new"],
+                                                  L["v_new"], L["kv"], L["out"], S.status))
+        elif kind == "accept":
+            dflv.check(dflv.dflv_accept_greedy(1, BUDGET, VOCAB, S.logits, S.tokens, S.parent, S.n_nodes, S.path,
+                                               S.path_len, S.next_token, S.best, S.status))
+        else:
+            S.step()
+            S.n_past.fill_(CTX)
+    torch.cuda.synchronize()
+    print(json.dumps({"kernel": kind, "launches": launches, "status": int(S.status.item())}))
+
+
 # ---------------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -506,7 +538,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", choices=["gdn", "attn", "accept", "commit"], default=None,
+                    help="profiling mode: launch one kernel of the step --launches times on its "
+                         "single-layer workload and exit (for ncu captures)")
+    ap.add_argument("--launches", type=int, default=3)
     args = ap.parse_args()
+    if args.kernel:
+        return profile_one(args.kernel, args.launches)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "ours" and args.steps + args.warmup + 1 > MAX_REPLAYS:

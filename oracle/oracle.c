@@ -250,33 +250,34 @@ int orc_gdn_commit(int B, int N, int Hk, int Hv, int dk, int dv,
 /* block quantisation: 32 values sharing one fp16 scale d                    */
 /* ------------------------------------------------------------------------ */
 
-/* q8_0: d = fp16(amax / 127), q = clamp(round_half_away(x / d), -127, 127). */
+/* q8_0: d = amax / 127 (stored as fp16), codes = clamp(round_half_away(x * (1/d)), -127, 127)
+ * with the reciprocal taken of the fp32 d: the format's usual quantiser. */
 void orc_quantize_q8_0(const float* x, int8_t* qs, uint16_t* d16) {
     float amax = 0.0f;
     for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(x[j]));
     float d = amax / 127.0f;
+    float id = (d != 0.0f) ? 1.0f / d : 0.0f;
     *d16 = orc_float_to_half_rn(d);
-    float df = orc_half_to_float(*d16);
     for (int j = 0; j < 32; ++j) {
-        float r = (df == 0.0f) ? 0.0f : roundf(x[j] / df);
+        float r = roundf(x[j] * id);
         if (r > 127.0f) r = 127.0f;
         if (r < -127.0f) r = -127.0f;
         qs[j] = (int8_t)r;
     }
 }
 
-/* q4_0: d = fp16(amax / 7), code = clamp(round_half_away(x / d), -8, 7) + 8.
+/* q4_0: d = amax / 7 (stored as fp16), code = clamp(round_half_away(x * (1/d)), -8, 7) + 8.
  * Element j < 16 sits in the low nibble of byte j, element j + 16 in its
  * high nibble. */
 void orc_quantize_q4_0(const float* x, uint8_t* nib, uint16_t* d16) {
     float amax = 0.0f;
     for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(x[j]));
     float d = amax / 7.0f;
+    float id = (d != 0.0f) ? 1.0f / d : 0.0f;
     *d16 = orc_float_to_half_rn(d);
-    float df = orc_half_to_float(*d16);
     uint8_t code[32];
     for (int j = 0; j < 32; ++j) {
-        float r = (df == 0.0f) ? 0.0f : roundf(x[j] / df);
+        float r = roundf(x[j] * id);
         if (r > 7.0f) r = 7.0f;
         if (r < -8.0f) r = -8.0f;
         code[j] = (uint8_t)((int)r + 8);

@@ -30,8 +30,9 @@
  * Precision: fp64 arithmetic for everything the method computes in floating
  * point; the committed recurrent state is stored as fp32 between steps.  The
  * block quantiser decides integer codes, so it runs in fp32 with correctly
- * rounded operations only (IEEE division, round-half-away, fp16 round to
- * nearest even): the same precision the kernels decide them in.
+ * rounded operations only (IEEE division and reciprocal, multiplication,
+ * round-half-away, fp16 round to nearest even): the same precision the
+ * kernels decide them in.
  *
  * Parity status: every function here is pinned by the "not gpu" tests in
  * tests/test_oracle_*.py (closed forms, invariants, brute force and a

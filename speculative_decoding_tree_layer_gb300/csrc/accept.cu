@@ -23,7 +23,7 @@ namespace dflv {
 
 namespace {
 
-constexpr int kArgmaxThreads = 256;
+constexpr int kArgmaxThreads = 512;
 
 DFLV_DEVINL uint32_t cluster_rank() {
     uint32_t r;
@@ -69,13 +69,13 @@ __global__ void __launch_bounds__(kArgmaxThreads) accept_argmax_kernel(AcceptArg
         const float4* r4 = reinterpret_cast<const float4*>(row);
         const int q0 = c0 >> 2, q1 = c1 >> 2;
         int q = q0 + tid;
-        // four independent 16-byte loads in flight per thread
-        for (; q + 3 * kArgmaxThreads < q1; q += 4 * kArgmaxThreads) {
-            float4 x[4];
+        // eight independent 16-byte loads in flight per thread
+        for (; q + 7 * kArgmaxThreads < q1; q += 8 * kArgmaxThreads) {
+            float4 x[8];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) x[u] = __ldcs(r4 + q + u * kArgmaxThreads);
+            for (int u = 0; u < 8; ++u) x[u] = __ldcs(r4 + q + u * kArgmaxThreads);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < 8; ++u) {
                 const int base = (q + u * kArgmaxThreads) * 4;
                 better(x[u].x, base, bv, bi);
                 better(x[u].y, base + 1, bv, bi);

@@ -90,7 +90,7 @@ dflv_status dflv_tree_gdn_verify(const dflv_gdn_desc* desc, const int32_t* paren
     if (!parent || !n_nodes || !q || !k || !v || !beta || !log_alpha || !state || !out || !factors ||
         !factors->u || !factors->g || !factors->kcopy || !status_dev)
         return DFLV_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(state) || !aligned16(factors->kcopy) ||
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(state) || !aligned16(factors->kcopy) ||
         !aligned4(parent) || !aligned4(n_nodes) || !aligned4(beta) || !aligned4(log_alpha) ||
         !aligned4(out) || !aligned4(factors->u) || !aligned4(factors->g) || !aligned4(status_dev))
         return DFLV_ERR_INVALID_ARG;

@@ -11,28 +11,30 @@
 // P + depth(i); a key at position j is visible iff j <= that position and
 // (W == 0 or j > position - W).
 //
-// How (q8_0 / q4_0):
-//   * quantise kernel: one warp per (sequence, node, KV head) writes the
-//     node's K and V rows into their slots (fp32 amax, IEEE division, fp16
-//     scale, round-half-away codes), so the tree attends exactly what a
-//     sequential decode would have stored;
-//   * main kernel: one thread-block CLUSTER per (sequence, KV head, row
-//     tile).  A row tile holds up to 128 query rows (every query head of the
-//     group x every node), so each KV byte is read once per row tile.  The
-//     cluster's CTAs split the visible key range [lo, P) plus the tree block
-//     into 64-key tiles (split-K), stream them through shared memory with
-//     16-byte cp.async double buffering, and run q.k on the tensor cores:
-//     int8 / 4-bit codes become fp16 exactly in registers and the per-block
-//     fp16 scale is applied to the fp32 accumulator of each 32-dim block, so
-//     the scores are exact up to fp32 accumulation.  V codes are staged in
-//     shared memory as exact fp16 integers and each key's block scale is
-//     folded into its softmax weight (p * d_v, rounded once to fp16) right
-//     before p.V runs on the tensor cores, with an fp32 online softmax.
-//     Rounding dequantised V to fp16 instead would add a second rounding
-//     per term and roughly triple the worst-case output error.  The per-CTA partial (max, sum,
-//     output) are merged through distributed shared memory -- no global
-//     scratch and no second launch.
-// f32 caches (small exactness checks) take a plain CUDA-core kernel.
+// How (q8_0 / q4_0): one thread-block CLUSTER per (sequence, KV head, row
+// tile).  A row tile holds up to 128 query rows (query heads of the group x
+// nodes), so each KV byte is read once per row tile.
+//   * Every CTA of the cluster first quantises its share of the tree's rows
+//     into cache slots [P, P + n) (q8_0: d = amax / 127, q4_0: d = amax / 7,
+//     stored as fp16; codes = round-half-away(x * (1/d)) from the fp32 d),
+//     then the cluster synchronises, so the tree attends exactly what a
+//     sequential decode would have stored and no extra launch is needed.
+//   * The cluster's CTAs split the visible key range [lo, P) plus the tree
+//     block into 64-key tiles (split-K) and stream them through shared
+//     memory with 16-byte cp.async double buffering.  Each tile's int8 /
+//     4-bit codes are staged once as exact fp16 integers (shared by all
+//     warps) with the block scales transposed to fp32.
+//   * q . k runs on the tensor cores (operands via ldmatrix) one 32-dim
+//     block at a time, and each block's fp32 partial is scaled by the key's
+//     block scale, so the scores are exact up to fp32 accumulation.
+//   * fp32 online softmax; each key's V block scale is folded into its
+//     softmax weight (p * d_v, rounded once to fp16) right before p . V on
+//     the tensor cores.  (Rounding dequantised V to fp16 instead adds a
+//     second rounding per term and roughly triples the worst-case error.)
+//   * The per-CTA partial (max, sum, output) are merged through distributed
+//     shared memory -- no global scratch.
+// f32 caches (small exactness checks) take a plain CUDA-core kernel after a
+// tiny kernel copies the tree's rows into the cache.
 #include <climits>
 
 #include "common.cuh"
@@ -103,76 +105,68 @@ DFLV_DEVINL void u4x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
     hi = *reinterpret_cast<uint32_t*>(&hh);
 }
 
-// ---------------------------------------------------------------- quantise tree K/V into the cache
-// q8_0: d = fp16(amax / 127), code = clamp(round_half_away(x / d), -127, 127)
-// q4_0: d = fp16(amax / 7),   code = clamp(round_half_away(x / d), -8, 7) + 8,
-//       element j < 16 in the low nibble of byte j, element j + 16 in its high nibble.
-__global__ void attn_quantize_tree_kernel(AttnVerifyArgs a) {
+// ---------------------------------------------------------------- f32 tree rows into the cache
+__global__ void attn_store_tree_f32_kernel(AttnVerifyArgs a) {
     const int i = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     grid_dependency_wait();
     const int n = __ldg(a.n_nodes + b), P = __ldg(a.n_past + b);
-    if (n < 1 || n > a.N_max) return;  // reported by the attention kernel
-    if (P < 0 || P + n > a.cap) return;
-    if (i >= n) return;
+    if (n < 1 || n > a.N_max || P < 0 || P + n > a.cap || i >= n) return;  // reported by the attention kernel
     const size_t src_row = (((size_t)b * a.N_max + i) * a.Hkv + kvh) * a.D;
     const size_t dst_row = ((size_t)b * a.Hkv + kvh) * a.cap + P + i;
-    if (a.type == DFLV_KV_F32) {
-        for (int t = threadIdx.x; t < 2 * a.D; t += blockDim.x) {
-            const int which = t / a.D, d = t % a.D;
-            const uint16_t* src = which ? a.v_new : a.k_new;
-            float* dst = reinterpret_cast<float*>(which ? a.vq : a.kq);
-            dst[dst_row * a.D + d] = bf16_bits_to_float(src[src_row + d]);
-        }
-        return;
+    for (int t = threadIdx.x; t < 2 * a.D; t += blockDim.x) {
+        const int which = t / a.D, d = t % a.D;
+        const uint16_t* src = which ? a.v_new : a.k_new;
+        float* dst = reinterpret_cast<float*>(which ? a.vq : a.kq);
+        dst[dst_row * a.D + d] = bf16_bits_to_float(src[src_row + d]);
     }
-    const int nb = a.D / 32;
-    const bool q8 = a.type == DFLV_KV_Q8_0;
-    for (int t = threadIdx.x; t < 2 * nb; t += blockDim.x) {
-        const int which = t / nb, blk = t % nb;
-        const uint16_t* src = (which ? a.v_new : a.k_new) + src_row + blk * 32;
-        float x[32];
-        float amax = 0.f;
+}
+
+// ---------------------------------------------------------------- block quantiser
+// One 32-value block of a tree row (bf16) -> codes + fp16 scale in the cache.
+template <int TYPE>
+DFLV_DEVINL void quantize_block(const uint16_t* __restrict__ src, uint8_t* __restrict__ codes,
+                                uint16_t* __restrict__ scale) {
+    float x[32];
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; j += 8) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(src + j));
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            x[j + 2 * e] = bf16_bits_to_float((uint16_t)(ww[e] & 0xffff));
+            x[j + 2 * e + 1] = bf16_bits_to_float((uint16_t)(ww[e] >> 16));
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(x[j]));
+    constexpr float qmax = (TYPE == DFLV_KV_Q8_0) ? 127.f : 7.f;
+    const float d = __fdiv_rn(amax, qmax);
+    const float id = (d != 0.f) ? __frcp_rn(d) : 0.f;
+    *scale = __half_as_ushort(__float2half_rn(d));
+    if constexpr (TYPE == DFLV_KV_Q8_0) {
+        uint32_t w[8];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-            x[j] = bf16_bits_to_float(src[j]);
-            amax = fmaxf(amax, fabsf(x[j]));
+            const float r = fminf(fmaxf(roundf(__fmul_rn(x[j], id)), -127.f), 127.f);
+            const uint32_t c = (uint32_t)(uint8_t)(int8_t)(int)r;
+            if ((j & 3) == 0) w[j >> 2] = 0;
+            w[j >> 2] |= c << (8 * (j & 3));
         }
-        const float d = __fdiv_rn(amax, q8 ? 127.f : 7.f);
-        const __half dh = __float2half_rn(d);
-        const float df = __half2float(dh);
-        uint16_t* sc = which ? a.vs : a.ks;
-        sc[dst_row * nb + blk] = __half_as_ushort(dh);
-        uint8_t* plane = reinterpret_cast<uint8_t*>(which ? a.vq : a.kq);
-        if (q8) {
-            uint32_t w[8];
+        reinterpret_cast<uint4*>(codes)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        reinterpret_cast<uint4*>(codes)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    } else {
+        uint32_t code[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                float r = (df == 0.f) ? 0.f : roundf(__fdiv_rn(x[j], df));
-                r = fminf(fmaxf(r, -127.f), 127.f);
-                const uint32_t c = (uint32_t)(uint8_t)(int8_t)(int)r;
-                if ((j & 3) == 0) w[j >> 2] = 0;
-                w[j >> 2] |= c << (8 * (j & 3));
-            }
-            uint4* dst = reinterpret_cast<uint4*>(plane + dst_row * a.D + blk * 32);
-            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        } else {
-            uint32_t code[32];
+        for (int j = 0; j < 32; ++j)
+            code[j] = (uint32_t)((int)fminf(fmaxf(roundf(__fmul_rn(x[j], id)), -8.f), 7.f) + 8);
+        uint32_t w[4];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                float r = (df == 0.f) ? 0.f : roundf(__fdiv_rn(x[j], df));
-                r = fminf(fmaxf(r, -8.f), 7.f);
-                code[j] = (uint32_t)((int)r + 8);
-            }
-            uint32_t w[4];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const uint32_t byte = code[j] | (code[j + 16] << 4);
-                if ((j & 3) == 0) w[j >> 2] = 0;
-                w[j >> 2] |= byte << (8 * (j & 3));
-            }
-            *reinterpret_cast<uint4*>(plane + dst_row * (a.D / 2) + blk * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int j = 0; j < 16; ++j) {
+            if ((j & 3) == 0) w[j >> 2] = 0;
+            w[j >> 2] |= (code[j] | (code[j + 16] << 4)) << (8 * (j & 3));
         }
+        *reinterpret_cast<uint4*>(codes) = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
@@ -181,23 +175,18 @@ template <int D, int TYPE>
 struct AttnSmem {
     static constexpr int NB = D / 32;                                  // scale blocks per row
     static constexpr int KB = (TYPE == DFLV_KV_Q8_0) ? D : D / 2;      // code bytes per row
-    static constexpr int KSB = KB + 16;                                // padded K row (bytes)
-    static constexpr int QS = D + 16;                                  // Q row stride (halves)
-    static constexpr int VS = D + 8;                                   // dequantised V row stride (halves)
+    static constexpr int HS = D + 8;                                   // fp16 row stride (halves): conflict-free ldmatrix
     static constexpr int OS = D + 4;                                   // merge row stride (floats)
     static constexpr size_t kHeader = 2048;
-    // per-buffer tile bytes
-    static constexpr size_t kK = (size_t)kTileKeys * KSB;
-    static constexpr size_t kKs = (size_t)kTileKeys * NB * 2;
-    static constexpr size_t kV = (size_t)kTileKeys * KB;
-    static constexpr size_t kVs = (size_t)kTileKeys * NB * 2;
+    static constexpr size_t kRawCodes = (size_t)kTileKeys * KB;        // one plane of one tile
+    static constexpr size_t kRawScales = (size_t)kTileKeys * NB * 2;
+    static constexpr size_t kRawTile = 2 * kRawCodes + 2 * kRawScales; // K and V, codes and scales
     static size_t __host__ __device__ off_Q() { return kHeader; }
-    static size_t __host__ __device__ off_K(int RT) { return kHeader + (size_t)RT * QS * 2; }
-    static size_t __host__ __device__ off_Ks(int RT) { return off_K(RT) + 2 * kK; }
-    static size_t __host__ __device__ off_V(int RT) { return off_Ks(RT) + 2 * kKs; }
-    static size_t __host__ __device__ off_Vs(int RT) { return off_V(RT) + 2 * kV; }
-    static size_t __host__ __device__ off_Vh(int RT) { return off_Vs(RT) + 2 * kVs; }
-    static size_t __host__ __device__ off_VsT(int RT) { return off_Vh(RT) + (size_t)kTileKeys * VS * 2; }
+    static size_t __host__ __device__ off_raw(int RT) { return kHeader + (size_t)RT * HS * 2; }
+    static size_t __host__ __device__ off_Kh(int RT) { return off_raw(RT) + 2 * kRawTile; }
+    static size_t __host__ __device__ off_Vh(int RT) { return off_Kh(RT) + (size_t)kTileKeys * HS * 2; }
+    static size_t __host__ __device__ off_KsT(int RT) { return off_Vh(RT) + (size_t)kTileKeys * HS * 2; }
+    static size_t __host__ __device__ off_VsT(int RT) { return off_KsT(RT) + (size_t)NB * kTileKeys * 4; }
     static size_t __host__ __device__ loop_total(int RT) { return off_VsT(RT) + (size_t)NB * kTileKeys * 4; }
     // merge buffers reuse the region from off_Q once the tile loop is done
     static size_t __host__ __device__ off_Om() { return kHeader; }
@@ -214,17 +203,16 @@ template <int D, int TYPE>
 __global__ void __launch_bounds__(kMaxRowTile * 2, 1)
     attn_tree_verify_kernel(AttnVerifyArgs a, int RT, int CS) {
     using S = AttnSmem<D, TYPE>;
-    constexpr int NB = S::NB, KB = S::KB, KSB = S::KSB, QS = S::QS, VS = S::VS, OS = S::OS;
+    constexpr int NB = S::NB, KB = S::KB, HS = S::HS, OS = S::OS;
     extern __shared__ __align__(128) unsigned char smem[];
     int32_t* par_s = reinterpret_cast<int32_t*>(smem);
     int32_t* depth_s = par_s + kMaxNodes;
     uint64_t* amask_s = reinterpret_cast<uint64_t*>(smem + 512);
     uint16_t* Q_s = reinterpret_cast<uint16_t*>(smem + S::off_Q());
-    uint8_t* K_s = smem + S::off_K(RT);
-    uint16_t* Ks_s = reinterpret_cast<uint16_t*>(smem + S::off_Ks(RT));
-    uint8_t* V_s = smem + S::off_V(RT);
-    uint16_t* Vs_s = reinterpret_cast<uint16_t*>(smem + S::off_Vs(RT));
+    uint8_t* raw_s = smem + S::off_raw(RT);
+    uint16_t* Kh_s = reinterpret_cast<uint16_t*>(smem + S::off_Kh(RT));
     uint16_t* Vh_s = reinterpret_cast<uint16_t*>(smem + S::off_Vh(RT));
+    float* KsT_s = reinterpret_cast<float*>(smem + S::off_KsT(RT));  // [NB][64] K block scales
     float* VsT_s = reinterpret_cast<float*>(smem + S::off_VsT(RT));  // [NB][64] V block scales
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthreads = blockDim.x;
@@ -243,13 +231,10 @@ __global__ void __launch_bounds__(kMaxRowTile * 2, 1)
     }
     const int rows_valid = G * n, row0 = rt * RT;
     if (row0 >= rows_valid) return;
-    if (!block_tree_topology(a.parent + (size_t)b * N, n, N, par_s, depth_s, amask_s,
-                             (rank == 0 && rt == 0 && kvh == 0) ? a.status : nullptr))
-        return;
 
     const size_t plane_row0 = ((size_t)b * a.Hkv + kvh) * a.cap;  // slot 0 of this (seq, kv head)
-    const uint8_t* kq = reinterpret_cast<const uint8_t*>(a.kq);
-    const uint8_t* vq = reinterpret_cast<const uint8_t*>(a.vq);
+    uint8_t* kq = reinterpret_cast<uint8_t*>(a.kq);
+    uint8_t* vq = reinterpret_cast<uint8_t*>(a.vq);
 
     // Tiles: cache keys [lo, P) in 64-key tiles, then one tree tile [P, P + n).
     const int lo = (W > 0) ? max(0, P - W + 1) : 0;
@@ -259,18 +244,17 @@ __global__ void __launch_bounds__(kMaxRowTile * 2, 1)
     auto issue_tile = [&](int t, int buf) {
         const int start = (t < n_cache_tiles) ? lo + t * kTileKeys : P;
         const int count = (t < n_cache_tiles) ? min(kTileKeys, P - start) : n;
-        uint8_t* kd = K_s + buf * S::kK;
-        uint8_t* vd = V_s + buf * S::kV;
-        uint8_t* ksd = reinterpret_cast<uint8_t*>(Ks_s) + buf * S::kKs;
-        uint8_t* vsd = reinterpret_cast<uint8_t*>(Vs_s) + buf * S::kVs;
+        uint8_t* base = raw_s + buf * S::kRawTile;
         constexpr int CPR = KB / 16;  // 16-byte chunks per code row
         for (int idx = tid; idx < count * CPR; idx += nthreads) {
             const int c = idx / CPR, ch = idx % CPR;
             const size_t g = (plane_row0 + start + c) * KB + ch * 16;
-            cp_async16(kd + c * KSB + ch * 16, kq + g);
-            cp_async16(vd + c * KB + ch * 16, vq + g);
+            cp_async16(base + c * KB + ch * 16, kq + g);
+            cp_async16(base + S::kRawCodes + c * KB + ch * 16, vq + g);
         }
         // scale rows: NB halves = 2*NB bytes each (4, 8 or 16: one cp.async per row)
+        uint8_t* ksd = base + 2 * S::kRawCodes;
+        uint8_t* vsd = ksd + S::kRawScales;
         for (int c = tid; c < count; c += nthreads) {
             const size_t g = (plane_row0 + start + c) * NB;
             if constexpr (NB * 2 == 16) {
@@ -287,12 +271,38 @@ __global__ void __launch_bounds__(kMaxRowTile * 2, 1)
         cp_async_commit();
     };
 
-    // First tile of this CTA in flight before the query rows load.
+    // First cache tile in flight before the tree rows are quantised (cache
+    // tiles never touch slots >= P).
     int t_cur = rank;
-    if (t_cur < n_tiles) issue_tile(t_cur, 0);
-    else cp_async_commit();
+    if (t_cur < n_cache_tiles) issue_tile(t_cur, 0);
 
-    // Query rows of this tile: row r <-> flat (node i, head gh) = row0 + r = i * G + gh.
+    // Quantise this CTA's share of the tree rows (rows rank, rank + CS, ...)
+    // of K and V into slots P + row; every cluster writes identical bytes.
+    {
+        const int mine = (n > rank) ? (n - rank + CS - 1) / CS : 0;
+        for (int item = tid; item < mine * 2 * NB; item += nthreads) {
+            const int j = item / (2 * NB), which = (item / NB) % 2, blk = item % NB;
+            const int row = rank + CS * j;
+            const uint16_t* src = (which ? a.v_new : a.k_new) + (((size_t)b * N + row) * a.Hkv + kvh) * D + blk * 32;
+            const size_t slot = plane_row0 + P + row;
+            uint8_t* codes = (which ? vq : kq) + slot * KB + blk * (KB / NB);
+            uint16_t* sc = (which ? a.vs : a.ks) + slot * NB + blk;
+            quantize_block<TYPE>(src, codes, sc);
+        }
+    }
+    if (!block_tree_topology(a.parent + (size_t)b * N, n, N, par_s, depth_s, amask_s,
+                             (rank == 0 && rt == 0 && kvh == 0) ? a.status : nullptr)) {
+        cp_async_wait<0>();
+        return;  // uniform over the cluster: the parent array is shared
+    }
+    __threadfence();
+    cluster_sync_all();  // tree slots written by the whole cluster are now visible
+    if (t_cur >= n_cache_tiles) {
+        if (t_cur < n_tiles) issue_tile(t_cur, 0);
+        else cp_async_commit();
+    }
+
+    // Query rows of this tile: row r <-> flat (node i, head gh) = row0 + r = i * G + gh, fp16.
     const int nwarps = nthreads / 32;
     const int RTw = nwarps * 16;  // rows covered by the warps (== RT)
     for (int idx = tid; idx < RTw * (D / 8); idx += nthreads) {
@@ -311,28 +321,33 @@ __global__ void __launch_bounds__(kMaxRowTile * 2, 1)
                                   bf16_bits_to_float((uint16_t)(w[e] >> 16)));
             outv = make_uint4(o[0], o[1], o[2], o[3]);
         }
-        *reinterpret_cast<uint4*>(Q_s + r * QS + c8 * 8) = outv;
+        *reinterpret_cast<uint4*>(Q_s + r * HS + c8 * 8) = outv;
     }
 
     // Per-thread row metadata: rows gq and gq + 8 of this warp.
-    int rnode[2], lb[2], rdepth[2];
+    int lb[2], rdepth[2];
     uint64_t ramask[2];
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
         const int rho = row0 + warp * 16 + gq + 8 * s;
         if (rho < rows_valid) {
             const int i = rho / G;
-            rnode[s] = i;
             rdepth[s] = depth_s[i];
             ramask[s] = amask_s[i];
             lb[s] = (W > 0) ? P + depth_s[i] - W + 1 : INT_MIN;
         } else {
-            rnode[s] = -1;
             rdepth[s] = 0;
             ramask[s] = 0;
             lb[s] = INT_MAX;
         }
     }
+
+    // ldmatrix lane addresses (bytes): Q as the A operand (rows x dims),
+    // K rows as the B operand (keys x dims, non-transposed), V rows as the
+    // B operand of p . V (keys x dims, transposed).
+    const uint32_t q_addr = smem_u32(Q_s + (warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * HS + (lane >> 4) * 8);
+    const uint32_t k_addr = smem_u32(Kh_s + ((lane & 7) + ((lane >> 4) & 1) * 8) * HS + ((lane >> 3) & 1) * 8);
+    const uint32_t v_addr = smem_u32(Vh_s + ((lane & 7) + ((lane >> 3) & 1) * 8) * HS + (lane >> 4) * 8);
 
     const float sl2 = a.scale * kLog2e;
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
@@ -351,81 +366,74 @@ __global__ void __launch_bounds__(kMaxRowTile * 2, 1)
         const bool tree_tile = t_cur >= n_cache_tiles;
         const int start = tree_tile ? P : lo + t_cur * kTileKeys;
         const int count = tree_tile ? n : min(kTileKeys, P - start);
-        const uint8_t* kb = K_s + buf * S::kK;
-        const uint16_t* ksb = reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(Ks_s) + buf * S::kKs);
-        const uint8_t* vb = V_s + buf * S::kV;
-        const uint16_t* vsb = reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(Vs_s) + buf * S::kVs);
+        const uint8_t* rb = raw_s + buf * S::kRawTile;
+        const uint16_t* ksb = reinterpret_cast<const uint16_t*>(rb + 2 * S::kRawCodes);
+        const uint16_t* vsb = reinterpret_cast<const uint16_t*>(rb + 2 * S::kRawCodes + S::kRawScales);
 
-        // V codes -> exact fp16 integers (rows past count are zero); block
-        // scales transposed to [block][key] in fp32 (zero past count)
-        for (int idx = tid; idx < kTileKeys * (D / 8); idx += nthreads) {
-            const int c = idx / (D / 8), d8 = idx % (D / 8);
+        // stage codes as exact fp16 integers (rows past count are zero) and
+        // the block scales transposed to [block][key] in fp32
+        for (int idx = tid; idx < 2 * kTileKeys * (D / 8); idx += nthreads) {
+            const int which = idx / (kTileKeys * (D / 8));
+            const int rem = idx % (kTileKeys * (D / 8));
+            const int c = rem / (D / 8), d8 = rem % (D / 8);
+            const uint8_t* src = rb + which * S::kRawCodes + c * KB;
             uint4 o = make_uint4(0, 0, 0, 0);
             if (c < count) {
                 if constexpr (TYPE == DFLV_KV_Q8_0) {
-                    const uint2 w = *reinterpret_cast<const uint2*>(vb + c * KB + d8 * 8);
+                    const uint2 w = *reinterpret_cast<const uint2*>(src + d8 * 8);
                     i8x4_to_f16x2(w.x, o.x, o.y);
                     i8x4_to_f16x2(w.y, o.z, o.w);
                 } else {
-                    // dims d8*8 .. d8*8+7 of 32-block blk sit in the low (first
-                    // half of the block) or high nibbles of 8 consecutive bytes
+                    // dims d8*8 .. +7 of 32-block blk: low (first half of the
+                    // block) or high nibbles of 8 consecutive bytes
                     const int blk = (d8 * 8) / 32, off = (d8 * 8) % 32;
-                    const uint2 w = *reinterpret_cast<const uint2*>(vb + c * KB + blk * 16 + (off & 15));
+                    const uint2 w = *reinterpret_cast<const uint2*>(src + blk * 16 + (off & 15));
                     const int sh = off >= 16 ? 4 : 0;
                     u4x4_to_f16x2((w.x >> sh) & 0x0f0f0f0fu, o.x, o.y);
                     u4x4_to_f16x2((w.y >> sh) & 0x0f0f0f0fu, o.z, o.w);
                 }
             }
-            *reinterpret_cast<uint4*>(Vh_s + c * VS + d8 * 8) = o;
+            *reinterpret_cast<uint4*>((which ? Vh_s : Kh_s) + c * HS + d8 * 8) = o;
         }
-        for (int idx = tid; idx < NB * kTileKeys; idx += nthreads) {
-            const int blk = idx / kTileKeys, c = idx % kTileKeys;
-            VsT_s[idx] = (c < count) ? __half2float(__ushort_as_half(vsb[c * NB + blk])) : 0.f;
+        for (int idx = tid; idx < 2 * NB * kTileKeys; idx += nthreads) {
+            const int which = idx / (NB * kTileKeys), rem = idx % (NB * kTileKeys);
+            const int blk = rem / kTileKeys, c = rem % kTileKeys;
+            const uint16_t* sb = which ? vsb : ksb;
+            (which ? VsT_s : KsT_s)[rem] = (c < count) ? __half2float(__ushort_as_half(sb[c * NB + blk])) : 0.f;
         }
+        __syncthreads();
 
-        // scores: S = sum over 32-dim blocks of scale_k * (q . codes), on tensor cores
+        // scores: S = sum over 32-dim blocks of d_k * (q . codes), on tensor cores
         float Sacc[8][4];
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) Sacc[nt][0] = Sacc[nt][1] = Sacc[nt][2] = Sacc[nt][3] = 0.f;
-        const uint16_t* q0 = Q_s + (warp * 16 + gq) * QS;
-        const uint16_t* q1 = q0 + 8 * QS;
-#pragma unroll 1
+#pragma unroll 2
         for (int blk = 0; blk < NB; ++blk) {
             uint32_t qa[2][4];
+            ldmatrix_x4(qa[0], q_addr + (2 * blk) * 32);
+            ldmatrix_x4(qa[1], q_addr + (2 * blk + 1) * 32);
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-                const int col = (2 * blk + kk) * 16 + tq * 4;
-                const uint2 r0 = *reinterpret_cast<const uint2*>(q0 + col);
-                const uint2 r1 = *reinterpret_cast<const uint2*>(q1 + col);
-                qa[kk][0] = r0.x;
-                qa[kk][1] = r1.x;
-                qa[kk][2] = r0.y;
-                qa[kk][3] = r1.y;
-            }
-#pragma unroll
-            for (int nt = 0; nt < 8; ++nt) {
-                const uint8_t* krow = kb + (nt * 8 + gq) * KSB;
-                uint32_t bfr[2][2];
-                if constexpr (TYPE == DFLV_KV_Q8_0) {
-                    const uint32_t w0 = *reinterpret_cast<const uint32_t*>(krow + (2 * blk) * 16 + tq * 4);
-                    const uint32_t w1 = *reinterpret_cast<const uint32_t*>(krow + (2 * blk + 1) * 16 + tq * 4);
-                    i8x4_to_f16x2(w0, bfr[0][0], bfr[0][1]);
-                    i8x4_to_f16x2(w1, bfr[1][0], bfr[1][1]);
-                } else {
-                    const uint32_t w = *reinterpret_cast<const uint32_t*>(krow + blk * 16 + tq * 4);
-                    u4x4_to_f16x2(w & 0x0f0f0f0fu, bfr[0][0], bfr[0][1]);
-                    u4x4_to_f16x2((w >> 4) & 0x0f0f0f0fu, bfr[1][0], bfr[1][1]);
-                }
-                float t4[4] = {0.f, 0.f, 0.f, 0.f};
-                mma_f16_16816(t4, qa[0], bfr[0]);
-                mma_f16_16816(t4, qa[1], bfr[1]);
-                const int key = nt * 8 + tq * 2;
-                const float s0 = __half2float(__ushort_as_half(ksb[key * NB + blk]));
-                const float s1 = __half2float(__ushort_as_half(ksb[(key + 1) * NB + blk]));
-                Sacc[nt][0] = fmaf(t4[0], s0, Sacc[nt][0]);
-                Sacc[nt][1] = fmaf(t4[1], s1, Sacc[nt][1]);
-                Sacc[nt][2] = fmaf(t4[2], s0, Sacc[nt][2]);
-                Sacc[nt][3] = fmaf(t4[3], s1, Sacc[nt][3]);
+            for (int np = 0; np < 4; ++np) {
+                uint32_t kb0[4], kb1[4];
+                ldmatrix_x4(kb0, k_addr + np * 16 * HS * 2 + (2 * blk) * 32);
+                ldmatrix_x4(kb1, k_addr + np * 16 * HS * 2 + (2 * blk + 1) * 32);
+                float tA[4] = {0.f, 0.f, 0.f, 0.f}, tB[4] = {0.f, 0.f, 0.f, 0.f};
+                const uint32_t bA0[2] = {kb0[0], kb0[1]}, bA1[2] = {kb1[0], kb1[1]};
+                const uint32_t bB0[2] = {kb0[2], kb0[3]}, bB1[2] = {kb1[2], kb1[3]};
+                mma_f16_16816(tA, qa[0], bA0);
+                mma_f16_16816(tA, qa[1], bA1);
+                mma_f16_16816(tB, qa[0], bB0);
+                mma_f16_16816(tB, qa[1], bB1);
+                const float2 sA = *reinterpret_cast<const float2*>(KsT_s + blk * kTileKeys + np * 16 + tq * 2);
+                const float2 sB = *reinterpret_cast<const float2*>(KsT_s + blk * kTileKeys + np * 16 + 8 + tq * 2);
+                Sacc[2 * np][0] = fmaf(tA[0], sA.x, Sacc[2 * np][0]);
+                Sacc[2 * np][1] = fmaf(tA[1], sA.y, Sacc[2 * np][1]);
+                Sacc[2 * np][2] = fmaf(tA[2], sA.x, Sacc[2 * np][2]);
+                Sacc[2 * np][3] = fmaf(tA[3], sA.y, Sacc[2 * np][3]);
+                Sacc[2 * np + 1][0] = fmaf(tB[0], sB.x, Sacc[2 * np + 1][0]);
+                Sacc[2 * np + 1][1] = fmaf(tB[1], sB.y, Sacc[2 * np + 1][1]);
+                Sacc[2 * np + 1][2] = fmaf(tB[2], sB.x, Sacc[2 * np + 1][2]);
+                Sacc[2 * np + 1][3] = fmaf(tB[3], sB.y, Sacc[2 * np + 1][3]);
             }
         }
 
@@ -448,17 +456,23 @@ __global__ void __launch_bounds__(kMaxRowTile * 2, 1)
                 Sacc[nt][c] = v;
                 mt[s] = fmaxf(mt[s], v);
             }
+        // The running max only moves when a row's tile max exceeds it by more
+        // than 2^8 (log2 domain): weights stay <= 256, exact after the final
+        // normalisation, and O is rescaled only on those (rare) tiles.
         float alpha[2];
+        bool rescale = false;
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
             mt[s] = fmaxf(mt[s], __shfl_xor_sync(0xffffffffu, mt[s], 1));
             mt[s] = fmaxf(mt[s], __shfl_xor_sync(0xffffffffu, mt[s], 2));
-            const float m_new = fmaxf(m_run[s], mt[s]);
-            const float base = (m_new == -INFINITY) ? 0.f : m_new;
-            alpha[s] = exp2f(m_run[s] - base);
-            m_run[s] = m_new;
-            mt[s] = base;
-            l_run[s] *= alpha[s];
+            alpha[s] = 1.f;
+            if (mt[s] > m_run[s] + 8.f) {
+                alpha[s] = (m_run[s] == -INFINITY) ? 0.f : exp2f(m_run[s] - mt[s]);
+                m_run[s] = mt[s];
+                l_run[s] *= alpha[s];
+                rescale = true;
+            }
+            mt[s] = (m_run[s] == -INFINITY) ? 0.f : m_run[s];
         }
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
@@ -469,20 +483,19 @@ __global__ void __launch_bounds__(kMaxRowTile * 2, 1)
                 Sacc[nt][c] = p;
                 l_run[s] += p;
             }
+        if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-        for (int j = 0; j < D / 8; ++j) {
-            O[j][0] *= alpha[0];
-            O[j][1] *= alpha[0];
-            O[j][2] *= alpha[1];
-            O[j][3] *= alpha[1];
+            for (int j = 0; j < D / 8; ++j) {
+                O[j][0] *= alpha[0];
+                O[j][1] *= alpha[0];
+                O[j][2] *= alpha[1];
+                O[j][3] *= alpha[1];
+            }
         }
-        __syncthreads();  // V codes and scales staged
 
         // O += (P * d_v) V_codes on tensor cores, one 32-dim V block at a time
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-            const int key = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-            const uint32_t base = smem_u32(Vh_s + key * VS + (lane >> 4) * 8);
             const int k01 = kk * 16 + tq * 2;
 #pragma unroll
             for (int blk = 0; blk < NB; ++blk) {
@@ -497,14 +510,14 @@ __global__ void __launch_bounds__(kMaxRowTile * 2, 1)
                 for (int half = 0; half < 2; ++half) {
                     const int dn = 2 * blk + half;
                     uint32_t r[4];
-                    ldmatrix_x4_trans(r, base + dn * 16 * 2);
+                    ldmatrix_x4_trans(r, v_addr + kk * 16 * HS * 2 + dn * 32);
                     const uint32_t b0[2] = {r[0], r[1]}, b1[2] = {r[2], r[3]};
                     mma_f16_16816(O[2 * dn], pa, b0);
                     mma_f16_16816(O[2 * dn + 1], pa, b1);
                 }
             }
         }
-        __syncthreads();  // buffers free for the next prefetch
+        __syncthreads();  // staged tile consumed: the next one may overwrite it
     }
     cp_async_wait<0>();
 
@@ -647,46 +660,77 @@ __global__ void attn_tree_verify_f32_kernel(AttnVerifyArgs a) {
 
 // ---------------------------------------------------------------- launch
 struct RowTiling {
-    int RT, n_rt, CS;
+    int RT, n_rt;
 };
 
-RowTiling choose_tiling(const AttnVerifyArgs& a, int sm_count) {
-    const int G = a.Hq / a.Hkv;
-    const int rows = G * a.N_max;
+RowTiling choose_rows(const AttnVerifyArgs& a) {
+    const int rows = (a.Hq / a.Hkv) * a.N_max;
     RowTiling t;
     t.n_rt = (rows + kMaxRowTile - 1) / kMaxRowTile;
     const int per = (rows + t.n_rt - 1) / t.n_rt;
     t.RT = ((per + 15) / 16) * 16;
+    return t;
+}
+
+// Largest cluster (power of two, <= 16) that the SMs can hold at one CTA per
+// SM alongside the others and that the key range can feed; 16 uses the
+// non-portable cluster size when the device can schedule it.
+template <typename Kernel>
+int choose_cluster(Kernel kern, const AttnVerifyArgs& a, const RowTiling& t, size_t smem, int sms) {
     const long range = (a.window > 0) ? (long)a.window - 1 : (long)a.cap;
     const long tiles = (range + kTileKeys - 1) / kTileKeys + 1;
     const long clusters = (long)t.n_rt * a.Hkv * a.B;
     int cs = 1;
-    while (cs < 8 && clusters * cs * 2 <= sm_count && cs * 2 <= tiles) cs *= 2;
-    t.CS = cs;
-    return t;
+    while (cs < 8 && clusters * cs * 2 <= sms && cs * 2 <= tiles) cs *= 2;
+    if (cs == 16) {
+        static int ok16 = -1;  // probed once per process
+        if (ok16 < 0) {
+            ok16 = 0;
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+                cudaLaunchConfig_t cfg = {};
+                cfg.gridDim = dim3(16, 1, 1);
+                cfg.blockDim = dim3(t.RT * 2, 1, 1);
+                cfg.dynamicSmemBytes = smem;
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeClusterDimension;
+                attr[0].val.clusterDim.x = 16;
+                attr[0].val.clusterDim.y = 1;
+                attr[0].val.clusterDim.z = 1;
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+                int n_clusters = 0;
+                if (cudaOccupancyMaxActiveClusters(&n_clusters, kern, &cfg) == cudaSuccess && n_clusters >= 1)
+                    ok16 = 1;
+            }
+            cudaGetLastError();
+        }
+        if (!ok16) cs = 8;
+    }
+    return cs;
 }
 
 template <int D, int TYPE>
 cudaError_t launch_main(const AttnVerifyArgs& a, cudaStream_t stream) {
     using S = AttnSmem<D, TYPE>;
-    const RowTiling t = choose_tiling(a, sm_count_cached());
+    const RowTiling t = choose_rows(a);
     const size_t smem = S::total(t.RT);
     auto kern = attn_tree_verify_kernel<D, TYPE>;
     cudaError_t e = ensure_smem(kern, smem);
     if (e != cudaSuccess) return e;
+    const int cs = choose_cluster(kern, a, t, smem, sm_count_cached());
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(t.CS, t.n_rt * a.Hkv, a.B);
+    cfg.gridDim = dim3(cs, t.n_rt * a.Hkv, a.B);
     cfg.blockDim = dim3(t.RT * 2, 1, 1);  // RT / 16 warps
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = t.CS;
+    attr[0].val.clusterDim.x = cs;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a, t.RT, t.CS);
+    return cudaLaunchKernelEx(&cfg, kern, a, t.RT, cs);
 }
 
 }  // namespace
@@ -703,10 +747,10 @@ size_t attn_verify_smem_bytes(int D, int type, int RT) {
 }
 
 cudaError_t launch_attn_tree_verify(const AttnVerifyArgs& a, cudaStream_t stream) {
-    attn_quantize_tree_kernel<<<dim3(a.N_max, a.Hkv, a.B), 32, 0, stream>>>(a);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
     if (a.type == DFLV_KV_F32) {
+        attn_store_tree_f32_kernel<<<dim3(a.N_max, a.Hkv, a.B), 64, 0, stream>>>(a);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
         attn_tree_verify_f32_kernel<<<dim3((a.N_max + 7) / 8, a.Hq, a.B), 256, 0, stream>>>(a);
         return cudaGetLastError();
     }

@@ -38,48 +38,60 @@ DFLV_DEVINL bool path_ok(const CommitArgs& a, int b, int& L) {
 
 __device__ void commit_gdn_head(const CommitArgs& a, int layer, int b, int h, unsigned char* smem) {
     const int tid = threadIdx.x;
-    int L;
-    if (!path_ok(a, b, L)) {
-        if (tid == 0 && layer == 0 && h == 0) raise_status(a.status, DFLV_DEV_PATH);
-        return;
-    }
     const CommitGdnLayer ly = a.gdn[layer];
     const int dk = a.dk, dv = a.dv, N = a.N_max;
-    const int hk = h / (a.Hv / a.Hk);
-    float* wu_s = reinterpret_cast<float*>(smem);   // [L][dv]  e^{g_e-g_p} u_p
-    float* kf_s = wu_s + (size_t)N * dv;            // [L][dk]  k_p
-    __shared__ float w_s[64];
-    __shared__ float Ge_s;
-    const int e = __ldg(a.path + (size_t)b * N + L - 1);
-    const float ge = __ldg(ly.g + ((size_t)b * N + e) * a.Hv + h);
-    for (int m = tid; m < L; m += kCommitThreads) {
-        const int p = __ldg(a.path + (size_t)b * N + m);
-        w_s[m] = expf(ge - __ldg(ly.g + ((size_t)b * N + p) * a.Hv + h));
-    }
-    if (tid == 0) Ge_s = expf(ge);
-    __syncthreads();
-    for (int idx = tid; idx < L * dv; idx += kCommitThreads) {
-        const int m = idx / dv, r = idx % dv;
-        const int p = __ldg(a.path + (size_t)b * N + m);
-        wu_s[idx] = w_s[m] * __ldg(ly.u + (((size_t)b * N + p) * a.Hv + h) * dv + r);
-    }
-    for (int idx = tid; idx < L * dk; idx += kCommitThreads) {
-        const int m = idx / dk, c = idx % dk;
-        const int p = __ldg(a.path + (size_t)b * N + m);
-        kf_s[idx] = bf16_bits_to_float(__ldg(ly.kcopy + (((size_t)b * N + p) * a.Hk + hk) * dk + c));
-    }
-    __syncthreads();
-
-    const float Ge = Ge_s;
     float4* S = reinterpret_cast<float4*>(ly.state + ((size_t)b * a.Hv + h) * dv * dk);
     const int E4 = dv * dk / 4;
     constexpr int U = 8;  // float4 per thread in flight
-    for (int base = 0; base < E4; base += U * kCommitThreads) {
-        float4 x[U];
+    // The first batch of state loads goes out before the (dependent) factor
+    // loads, so their latencies overlap.
+    float4 x[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int e4 = base + u * kCommitThreads + tid;
-            if (e4 < E4) x[u] = __ldcs(S + e4);
+    for (int u = 0; u < U; ++u) {
+        const int e4 = u * kCommitThreads + tid;
+        if (e4 < E4) x[u] = __ldcs(S + e4);
+    }
+    // Prologue in two rounds of independent loads: (1) path length and the
+    // whole path row, (2) everything indexed by the path.
+    __shared__ int32_t path_s[64];
+    __shared__ float gp_s[64];
+    const int L = __ldg(a.path_len + b);
+    const bool L_ok = L >= 1 && L <= N;
+    int bad = L_ok ? 0 : 1;
+    for (int m = tid; m < N; m += kCommitThreads) {
+        const int p = __ldg(a.path + (size_t)b * N + m);
+        path_s[m] = p;
+        if (L_ok && m < L && (p < 0 || p >= N)) bad = 1;
+    }
+    if (__syncthreads_or(bad)) {
+        if (tid == 0 && layer == 0 && h == 0) raise_status(a.status, DFLV_DEV_PATH);
+        return;
+    }
+    const int hk = h / (a.Hv / a.Hk);
+    float* wu_s = reinterpret_cast<float*>(smem);   // [L][dv]  e^{g_e-g_p} u_p
+    float* kf_s = wu_s + (size_t)N * dv;            // [L][dk]  k_p
+    for (int m = tid; m < L; m += kCommitThreads) gp_s[m] = __ldg(ly.g + ((size_t)b * N + path_s[m]) * a.Hv + h);
+    for (int idx = tid; idx < L * dv; idx += kCommitThreads) {
+        const int m = idx / dv, r = idx % dv;
+        wu_s[idx] = __ldg(ly.u + (((size_t)b * N + path_s[m]) * a.Hv + h) * dv + r);
+    }
+    for (int idx = tid; idx < L * dk; idx += kCommitThreads) {
+        const int m = idx / dk, c = idx % dk;
+        kf_s[idx] = bf16_bits_to_float(__ldg(ly.kcopy + (((size_t)b * N + path_s[m]) * a.Hk + hk) * dk + c));
+    }
+    __syncthreads();
+    const float ge = gp_s[L - 1];  // the path's end node
+    for (int idx = tid; idx < L * dv; idx += kCommitThreads) wu_s[idx] *= expf(ge - gp_s[idx / dv]);
+    __syncthreads();
+
+    const float Ge = expf(ge);
+    for (int base = 0; base < E4; base += U * kCommitThreads) {
+        if (base > 0) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int e4 = base + u * kCommitThreads + tid;
+                if (e4 < E4) x[u] = __ldcs(S + e4);
+            }
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {

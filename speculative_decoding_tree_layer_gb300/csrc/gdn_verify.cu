@@ -39,10 +39,11 @@ constexpr int kGdnWarps = kGdnThreads / 32;
 
 struct GdnSmemLayout {
     int NP, DK, RB, KS;
-    size_t off_S, off_K, off_Q, off_A, off_M, off_R, off_SQ, total;
+    size_t off_S, off_V, off_K, off_Q, off_A, off_M, off_R, off_SQ, total;
     __host__ __device__ GdnSmemLayout(int np, int dk, int rb) : NP(np), DK(dk), RB(rb), KS(dk + 16) {
         off_S = 3200;  // header: mbarrier + per-node arrays (3136 B), rounded up to 128
-        off_K = off_S + (size_t)RB * DK * 4;
+        off_V = off_S + (size_t)RB * DK * 4;     // bf16 v of this CTA's rows, [node][RB]
+        off_K = off_V + (size_t)NP * RB * 2;
         off_Q = off_K + (size_t)NP * KS * 2;
         off_A = off_Q + (size_t)NP * KS * 2;
         off_M = off_A + (size_t)NP * NP * 4;
@@ -94,6 +95,7 @@ __global__ void __launch_bounds__(kGdnThreads)
     float* g_s = la_s + kMaxNodes;
     float* G_s = g_s + kMaxNodes;
     float* S_s = reinterpret_cast<float*>(smem + L.off_S);
+    uint16_t* V_s = reinterpret_cast<uint16_t*>(smem + L.off_V);
     uint16_t* K_s = reinterpret_cast<uint16_t*>(smem + L.off_K);
     uint16_t* Q_s = reinterpret_cast<uint16_t*>(smem + L.off_Q);
     float* A_s = reinterpret_cast<float*>(smem + L.off_A);
@@ -115,27 +117,53 @@ __global__ void __launch_bounds__(kGdnThreads)
     __syncthreads();
     grid_dependency_wait();
 
-    // 1. Stream this CTA's RB rows of S_0 (contiguous) through the bulk-copy
-    //    engine while the tree-only work below proceeds.
+    // 1. Every input of this CTA is requested at once: its RB rows of S_0
+    //    (contiguous) through the bulk-copy engine, and the parent array, the
+    //    node scalars, keys, queries and v block with 16- / 4-byte cp.async.
+    //    All N_max node rows are fetched (rows past n are never read back
+    //    into a result), so nothing waits for n.
     if (tid == 0) {
         const float* src = a.state + (((size_t)b * a.Hv + h) * a.dv + r0) * DK;
         mbar_arrive_expect_tx(bar, RB * DK * 4);
         bulk_g2s(S_s, src, RB * DK * 4, bar);
     }
-
-    // 2. Tree topology.
+    constexpr int CH = DK / 8;  // 16-byte chunks per bf16 row
+    for (int idx = tid; idx < N * CH; idx += kGdnThreads) {
+        const int i = idx / CH, c = idx % CH;
+        const size_t off = (((size_t)b * N + i) * a.Hk + hk) * DK + c * 8;
+        cp_async16(K_s + i * KS + c * 8, a.k + off);
+        cp_async16(Q_s + i * KS + c * 8, a.q + off);
+    }
+    constexpr int VCH = RB / 8;  // 16-byte chunks of this CTA's v rows
+    for (int idx = tid; idx < N * VCH; idx += kGdnThreads) {
+        const int i = idx / VCH, c = idx % VCH;
+        cp_async16(V_s + i * RB + c * 8, a.v + (((size_t)b * N + i) * a.Hv + h) * a.dv + r0 + c * 8);
+    }
+    for (int i = tid; i < N; i += kGdnThreads) {
+        const size_t sidx = ((size_t)b * N + i) * a.Hv + h;
+        cp_async4(beta_s + i, a.beta + sidx);
+        cp_async4(la_s + i, a.log_alpha + sidx);
+        cp_async4(par_s + i, a.parent + (size_t)b * N + i);
+    }
+    cp_async_commit();
+    // rows [N, NP) of K and Q take part in the tensor-core tiles: zero them
+    for (int idx = tid; idx < (NP - N) * CH; idx += kGdnThreads) {
+        const int i = N + idx / CH, c = idx % CH;
+        *reinterpret_cast<uint4*>(K_s + i * KS + c * 8) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(Q_s + i * KS + c * 8) = make_uint4(0, 0, 0, 0);
+    }
     const int n = __ldg(a.n_nodes + b);
-    if (!block_tree_topology(a.parent + (size_t)b * N, n, N, par_s, depth_s, amask_s, a.status)) {
+    cp_async_wait<0>();
+    __syncthreads();
+
+    // 2. Tree topology (from the staged parent array).
+    if (!block_tree_topology_smem(n, N, par_s, depth_s, amask_s, a.status)) {
         if (tid == 0) mbar_wait_bounded(bar, 0, a.status);  // let the copy land before leaving
         return;
     }
 
-    // 3. Per-node scalars, the node keys / queries of q/k head hk, and the
-    //    nodes ordered by depth (level d = order_s[lvl_s[d] .. lvl_s[d+1])).
+    // 3. Nodes ordered by depth (level d = order_s[lvl_s[d] .. lvl_s[d+1])).
     for (int i = tid; i < n; i += kGdnThreads) {
-        const size_t s = ((size_t)b * N + i) * a.Hv + h;
-        beta_s[i] = __ldg(a.beta + s);
-        la_s[i] = __ldg(a.log_alpha + s);
         const int d = depth_s[i];
         int pos = 0;
         for (int j = 0; j < n; ++j) {
@@ -144,18 +172,6 @@ __global__ void __launch_bounds__(kGdnThreads)
         }
         order_s[pos] = i;
         atomicMax(misc_s, d);
-    }
-    constexpr int CH = DK / 8;  // 16-byte chunks per bf16 row
-    for (int idx = tid; idx < NP * CH; idx += kGdnThreads) {
-        const int i = idx / CH, c = idx % CH;
-        uint4 kv = make_uint4(0, 0, 0, 0), qv = make_uint4(0, 0, 0, 0);
-        if (i < n) {
-            const size_t off = (((size_t)b * N + i) * a.Hk + hk) * DK + c * 8;
-            kv = __ldg(reinterpret_cast<const uint4*>(a.k + off));
-            qv = __ldg(reinterpret_cast<const uint4*>(a.q + off));
-        }
-        *reinterpret_cast<uint4*>(K_s + i * KS + c * 8) = kv;
-        *reinterpret_cast<uint4*>(Q_s + i * KS + c * 8) = qv;
     }
     __syncthreads();
     const int maxd = misc_s[0];
@@ -268,7 +284,7 @@ __global__ void __launch_bounds__(kGdnThreads)
     // 7. R_j = beta_j (v_j - e^{g_j} S_0 k_j) for this CTA's rows.
     for (int idx = tid; idx < n * RB; idx += kGdnThreads) {
         const int j = idx / RB, r = idx % RB;
-        const float vv = bf16_bits_to_float(__ldg(a.v + (((size_t)b * N + j) * a.Hv + h) * a.dv + r0 + r));
+        const float vv = bf16_bits_to_float(V_s[j * RB + r]);
         R_s[j * RB + r] = beta_s[j] * (vv - G_s[j] * R_s[j * RB + r]);
     }
     __syncthreads();

@@ -54,4 +54,34 @@ DFLV_DEVINL bool block_tree_topology(const int32_t* __restrict__ parent_b, int n
     return true;
 }
 
+// Same as block_tree_topology, with the parent array already in par_s.
+DFLV_DEVINL bool block_tree_topology_smem(int n, int N_max, const int32_t* par_s, int32_t* depth_s,
+                                          uint64_t* amask_s, int32_t* status_dev) {
+    const int tid = threadIdx.x;
+    const bool n_ok = (n >= 1 && n <= N_max && n <= kMaxNodes);
+    int bad = n_ok ? 0 : 1;
+    if (n_ok)
+        for (int i = tid; i < n; i += blockDim.x) {
+            const int p = par_s[i];
+            if (i == 0 ? (p != -1) : (p < 0 || p >= i)) bad = 1;
+        }
+    bad = __syncthreads_or(bad);
+    if (bad) {
+        if (tid == 0) raise_status(status_dev, DFLV_DEV_TOPOLOGY);
+        return false;
+    }
+    for (int i = tid; i < n; i += blockDim.x) {
+        uint64_t m = 1ull << i;
+        int d = 0;
+        for (int c = par_s[i]; c >= 0; c = par_s[c]) {
+            m |= 1ull << c;
+            ++d;
+        }
+        depth_s[i] = d;
+        amask_s[i] = m;
+    }
+    __syncthreads();
+    return true;
+}
+
 }  // namespace dflv

@@ -90,8 +90,8 @@ def test_fp16_conversion_matches_numpy(orc):
 
 @pytest.mark.parametrize("kind", ["q8_0", "q4_0"])
 def test_round_trip_error_bound(orc, kind):
-    # |x - dequant(quant(x))| <= d16/2 plus what clamping can add when d16
-    # rounded below amax/qmax.
+    # Codes come from the fp32 scale d = amax/qmax, reconstruction uses the
+    # stored fp16 d16: |x - d16 c| <= |x - d c| + |c| |d - d16| <= d/2 + qmax |d - d16|.
     rng = np.random.default_rng(2)
     qmax = 127.0 if kind == "q8_0" else 7.0
     for _ in range(300):
@@ -104,7 +104,7 @@ def test_round_trip_error_bound(orc, kind):
             y = orc.dequantize_q4_0(nib, d16)
         d = float(np.abs(x).max()) / qmax
         dh = orc.half_to_float(d16)
-        bound = dh / 2 + qmax * max(0.0, d - dh) + 1e-12
+        bound = d * (0.5 + qmax * 2.0 ** -22) + qmax * abs(d - dh) + 1e-12  # + rounding of x * (1/d)
         assert np.abs(x.astype(np.float64) - y).max() <= bound
 
 
