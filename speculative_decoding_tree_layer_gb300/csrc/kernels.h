@@ -46,6 +46,7 @@ struct AttnVerifyArgs {
 };
 
 cudaError_t launch_attn_tree_verify(const AttnVerifyArgs& a, cudaStream_t stream);
+cudaError_t launch_attn_tree_verify_tc(const AttnVerifyArgs& a, cudaStream_t stream);
 
 struct AcceptArgs {
     int B, N_max, vocab;
