@@ -260,9 +260,15 @@ class GpuStep:
         self.next_token = t.zeros(1, dtype=t.int32, device=dev)
         self.best = t.zeros((1, N), dtype=t.int32, device=dev)
         self.h_out = t.empty(N + 2, dtype=t.int32, pin_memory=True)
+        # every layer but the first follows a kernel that writes neither its
+        # committed state / cache prefix nor the tree: those may be read early
+        early = dflv.DFLV_FLAG_EARLY_PREFETCH
         self.gdn_desc = dflv.gdn_desc(1, N, GDN["Hk"], GDN["Hv"], GDN["dk"], GDN["dv"])
+        self.gdn_desc_next = dflv.gdn_desc(1, N, GDN["Hk"], GDN["Hv"], GDN["dk"], GDN["dv"], early)
         self.attn_desc = dflv.attn_desc(1, N, ATT["Hq"], ATT["Hkv"], ATT["D"], cap, WINDOW, dflv.DFLV_KV_Q8_0,
                                         1.0 / np.sqrt(ATT["D"]))
+        self.attn_desc_next = dflv.attn_desc(1, N, ATT["Hq"], ATT["Hkv"], ATT["D"], cap, WINDOW, dflv.DFLV_KV_Q8_0,
+                                             1.0 / np.sqrt(ATT["D"]), early)
         self.layers = []
         self.states, self.factors, self.caches = [], [], []
         self.state0 = []
@@ -296,11 +302,11 @@ class GpuStep:
             if ev is not None:
                 ev[li][0].record()
             if L["kind"] == "gdn":
-                chk(dflv.dflv_tree_gdn_verify(self.gdn_desc, self.parent, self.n_nodes, L["q"], L["k"], L["v"],
+                chk(dflv.dflv_tree_gdn_verify(self.gdn_desc if li == 0 else self.gdn_desc_next, self.parent, self.n_nodes, L["q"], L["k"], L["v"],
                                               L["beta"], L["log_alpha"], L["state"], L["out"], L["fac"],
                                               self.status), "gdn verify")
             else:
-                chk(dflv.dflv_tree_attn_verify(self.attn_desc, self.parent, self.n_nodes, self.n_past, L["q"],
+                chk(dflv.dflv_tree_attn_verify(self.attn_desc_next, self.parent, self.n_nodes, self.n_past, L["q"],
                                                L["k_new"], L["v_new"], L["kv"], L["out"], self.status),
                     "attn verify")
             if ev is not None:

@@ -85,6 +85,20 @@ typedef enum {
     DFLV_KV_F32 = 2   /* plain fp32 cache (small exactness checks) */
 } dflv_kv_type;
 
+/* Launch overlap.  Every kernel of this library is launched with
+ * programmatic dependent launch: it may be scheduled while the preceding
+ * kernel on the stream finishes, and it waits for that kernel's completion
+ * (and memory) before it reads anything.  With DFLV_FLAG_EARLY_PREFETCH in a
+ * verify call's descriptor, the kernel starts reading the inputs that the
+ * step itself never produces before that wait: for gated-DeltaNet the
+ * committed state and the tree (parent, n_nodes), for attention the tree,
+ * n_past and the cached slots below P.  Set the flag only when the kernel
+ * that immediately precedes the call on the stream writes none of these
+ * buffers -- in a verify step, every layer after the first.  (Each kernel
+ * of the library releases its successor only after its own wait, so the
+ * overlap never reaches past the immediate predecessor.) */
+enum { DFLV_FLAG_EARLY_PREFETCH = 1 };
+
 /* ------------------------------------------------------------------------ */
 /* Gated-DeltaNet layer                                                      */
 /* ------------------------------------------------------------------------ */
@@ -94,6 +108,7 @@ typedef enum {
  * dk in {16, 32, 64, 128}, dv a multiple of 16 (<= 512). */
 typedef struct {
     int32_t B, N_max, Hk, Hv, dk, dv;
+    uint32_t flags; /* 0 or DFLV_FLAG_EARLY_PREFETCH */
 } dflv_gdn_desc;
 
 /* Per-node factors captured by verify for commit ([PR606]: factor capture
@@ -145,6 +160,7 @@ typedef struct {
     int32_t B, N_max, Hq, Hkv, D, cap, window;
     dflv_kv_type type;
     float scale;
+    uint32_t flags; /* 0 or DFLV_FLAG_EARLY_PREFETCH */
 } dflv_attn_desc;
 
 /* One attention layer's cache, structure-of-arrays planes:

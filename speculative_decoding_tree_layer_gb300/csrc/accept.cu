@@ -55,6 +55,7 @@ __global__ void __launch_bounds__(kArgmaxThreads) accept_argmax_kernel(AcceptArg
     const int i = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     grid_dependency_wait();
+    grid_launch_dependents();
     const int n = __ldg(a.n_nodes + b);
     if (n < 1 || n > a.N_max || i >= n) return;  // uniform over the cluster
 
@@ -127,6 +128,7 @@ __global__ void __launch_bounds__(kArgmaxThreads) accept_argmax_kernel(AcceptArg
 __global__ void accept_walk_kernel(AcceptArgs a) {
     const int b = blockIdx.x, lane = threadIdx.x;
     grid_dependency_wait();
+    grid_launch_dependents();
     const int n = __ldg(a.n_nodes + b), N = a.N_max;
     if (n < 1 || n > N) {
         if (lane == 0) {
@@ -180,21 +182,9 @@ cudaError_t launch_accept_greedy(const AcceptArgs& a, cudaStream_t stream) {
     const long rows = (long)a.B * a.N_max;
     int cs = 1;
     while (cs < 8 && rows * cs < 2L * sms && (long)cs * 2 * kArgmaxThreads * 16 <= a.vocab) cs *= 2;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(cs, a.N_max, a.B);
-    cfg.blockDim = dim3(kArgmaxThreads, 1, 1);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cs;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, accept_argmax_kernel, a, cs);
+    cudaError_t e = launch_pdl(accept_argmax_kernel, dim3(cs, a.N_max, a.B), dim3(kArgmaxThreads), 0, stream, cs, a, cs);
     if (e != cudaSuccess) return e;
-    accept_walk_kernel<<<a.B, 32, 0, stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(accept_walk_kernel, dim3(a.B), dim3(32), 0, stream, 1, a);
 }
 
 }  // namespace dflv

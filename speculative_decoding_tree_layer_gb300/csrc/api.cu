@@ -18,6 +18,7 @@ dflv_status check_gdn_desc(const dflv_gdn_desc* d) {
     if (d->B < 1 || d->N_max < 1 || d->Hk < 1 || d->Hv < 1 || d->dk < 1 || d->dv < 1)
         return DFLV_ERR_INVALID_ARG;
     if (d->Hv % d->Hk != 0) return DFLV_ERR_INVALID_ARG;
+    if (d->flags & ~(uint32_t)DFLV_FLAG_EARLY_PREFETCH) return DFLV_ERR_INVALID_ARG;
     if (d->N_max > 64) return DFLV_ERR_UNSUPPORTED;
     if (d->dk != 16 && d->dk != 32 && d->dk != 64 && d->dk != 128) return DFLV_ERR_UNSUPPORTED;
     if (d->dv % 16 != 0 || d->dv > 512) return DFLV_ERR_UNSUPPORTED;
@@ -29,6 +30,7 @@ dflv_status check_attn_desc(const dflv_attn_desc* d) {
     if (d->B < 1 || d->N_max < 1 || d->Hq < 1 || d->Hkv < 1 || d->D < 1 || d->cap < 1 || d->window < 0)
         return DFLV_ERR_INVALID_ARG;
     if (d->Hq % d->Hkv != 0) return DFLV_ERR_INVALID_ARG;
+    if (d->flags & ~(uint32_t)DFLV_FLAG_EARLY_PREFETCH) return DFLV_ERR_INVALID_ARG;
     if (d->N_max > 64) return DFLV_ERR_UNSUPPORTED;
     if (d->cap < d->N_max) return DFLV_ERR_CAPACITY;
     if (!(d->scale == d->scale)) return DFLV_ERR_INVALID_ARG;
@@ -101,6 +103,7 @@ dflv_status dflv_tree_gdn_verify(const dflv_gdn_desc* desc, const int32_t* paren
     a.Hv = desc->Hv;
     a.dk = desc->dk;
     a.dv = desc->dv;
+    a.flags = desc->flags;
     a.parent = parent;
     a.n_nodes = n_nodes;
     a.q = q;
@@ -144,6 +147,7 @@ dflv_status dflv_tree_attn_verify(const dflv_attn_desc* desc, const int32_t* par
     a.window = desc->window;
     a.type = desc->type;
     a.scale = desc->scale;
+    a.flags = desc->flags;
     a.parent = parent;
     a.n_nodes = n_nodes;
     a.n_past = n_past;

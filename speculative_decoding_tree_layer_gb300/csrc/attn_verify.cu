@@ -55,6 +55,7 @@ using namespace attn;
 __global__ void attn_store_tree_f32_kernel(AttnVerifyArgs a) {
     const int i = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     grid_dependency_wait();
+    grid_launch_dependents();
     const int n = __ldg(a.n_nodes + b), P = __ldg(a.n_past + b);
     if (n < 1 || n > a.N_max || P < 0 || P + n > a.cap || i >= n) return;  // reported by the attention kernel
     const size_t src_row = (((size_t)b * a.N_max + i) * a.Hkv + kvh) * a.D;
@@ -119,6 +120,7 @@ __global__ void __launch_bounds__(kMaxRowTile * 2, 1)
     const int G = a.Hq / a.Hkv, N = a.N_max, W = a.window;
 
     grid_dependency_wait();
+    grid_launch_dependents();
     const int n = __ldg(a.n_nodes + b), P = __ldg(a.n_past + b);
     // Uniform over the cluster: every CTA leaves before any cluster barrier.
     if (P < 0 || P + n > a.cap || n < 1 || n > N) {
@@ -489,6 +491,7 @@ __global__ void attn_tree_verify_f32_kernel(AttnVerifyArgs a) {
     const int i = blockIdx.x * 8 + warp;
     const int N = a.N_max, D = a.D, W = a.window, G = a.Hq / a.Hkv, kvh = h / G;
     grid_dependency_wait();
+    grid_launch_dependents();
     const int n = __ldg(a.n_nodes + b), P = __ldg(a.n_past + b);
     if (P < 0 || P + n > a.cap || n < 1 || n > N) {
         if (threadIdx.x == 0 && blockIdx.x == 0 && h == 0)
@@ -615,30 +618,16 @@ cudaError_t launch_main(const AttnVerifyArgs& a, cudaStream_t stream) {
     cudaError_t e = ensure_smem(kern, smem);
     if (e != cudaSuccess) return e;
     const int cs = choose_cluster(kern, a, t, smem, sm_count_cached());
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(cs, t.n_rt * a.Hkv, a.B);
-    cfg.blockDim = dim3(t.RT * 2, 1, 1);  // RT / 16 warps
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cs;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a, t.RT, cs);
+    return launch_pdl(kern, dim3(cs, t.n_rt * a.Hkv, a.B), dim3(t.RT * 2), smem, stream, cs, a, t.RT, cs);
 }
 
 }  // namespace
 
 cudaError_t launch_attn_tree_verify(const AttnVerifyArgs& a, cudaStream_t stream) {
     if (a.type == DFLV_KV_F32) {
-        attn_store_tree_f32_kernel<<<dim3(a.N_max, a.Hkv, a.B), 64, 0, stream>>>(a);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_pdl(attn_store_tree_f32_kernel, dim3(a.N_max, a.Hkv, a.B), dim3(64), 0, stream, 1, a);
         if (e != cudaSuccess) return e;
-        attn_tree_verify_f32_kernel<<<dim3((a.N_max + 7) / 8, a.Hq, a.B), 256, 0, stream>>>(a);
-        return cudaGetLastError();
+        return launch_pdl(attn_tree_verify_f32_kernel, dim3((a.N_max + 7) / 8, a.Hq, a.B), dim3(256), 0, stream, 1, a);
     }
     // head sizes 128 / 256: the tensor-memory kernel (attn_verify_tc.cu);
     // 64: the warp-MMA kernel below

@@ -157,6 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
     const int G = a.Hq / a.Hkv, N = a.N_max, W = a.window;
 
     grid_dependency_wait();
+    grid_launch_dependents();
     const int n = __ldg(a.n_nodes + b), P = __ldg(a.n_past + b);
     // Uniform over the cluster: every CTA leaves before any cluster barrier.
     if (P < 0 || P + n > a.cap || n < 1 || n > N) {
@@ -561,19 +562,7 @@ cudaError_t launch_tc(const AttnVerifyArgs& a, cudaStream_t stream) {
     while (cs < 16 && clusters * cs * 2 <= sms && cs * 2 <= tiles &&
            active_clusters(kern, S::total, cs * 2) >= clusters)
         cs *= 2;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(cs, n_rt * a.Hkv, a.B);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = S::total;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cs;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a, RT, cs);
+    return launch_pdl(kern, dim3(cs, n_rt * a.Hkv, a.B), dim3(kThreads), S::total, stream, cs, a, RT, cs);
 }
 
 }  // namespace

@@ -199,13 +199,14 @@ cudaError_t launch_commit_rollback(const CommitArgs& a, cudaStream_t stream) {
         }
         cudaError_t e = ensure_smem(commit_kernel, smem);
         if (e != cudaSuccess) return e;
-        commit_kernel<<<(unsigned)blocks, kCommitThreads, smem, stream>>>(a);
-        e = cudaGetLastError();
+        // (commit releases no dependent early: the next kernel may read the
+        // states it writes)
+        e = launch_pdl(commit_kernel, dim3((unsigned)blocks), dim3(kCommitThreads), smem, stream, 1, a);
         if (e != cudaSuccess) return e;
     }
     if (a.n_past != nullptr) {
-        commit_advance_kernel<<<(a.B + 255) / 256, 256, 0, stream>>>(a.path_len, a.n_past, a.B, a.N_max);
-        return cudaGetLastError();
+        return launch_pdl(commit_advance_kernel, dim3((a.B + 255) / 256), dim3(256), 0, stream, 1, a.path_len,
+                          a.n_past, a.B, a.N_max);
     }
     return cudaSuccess;
 }

@@ -150,6 +150,11 @@ DFLV_DEVINL void cp_async_wait() {
 // Waits until the grids this one depends on (programmatic dependent launch)
 // have completed and their memory is visible.  A no-op without PDL.
 DFLV_DEVINL void grid_dependency_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+// Lets the next kernel on the stream (if launched with PDL) be scheduled
+// now.  Every kernel of this library calls it only after its own
+// grid_dependency_wait, so at most one predecessor of a kernel can still be
+// running while that kernel executes the part before its own wait.
+DFLV_DEVINL void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
 
 // ---------------------------------------------------------------- misc
 DFLV_DEVINL int popc64(uint64_t x) { return __popcll(x); }
@@ -160,6 +165,7 @@ DFLV_DEVINL int ffs64(uint64_t x) { return __ffsll((long long)x) - 1; }
 // ---------------------------------------------------------------- host-side launch helpers
 #include <atomic>
 #include <mutex>
+#include <utility>
 
 namespace dflv {
 
@@ -204,6 +210,36 @@ inline cudaError_t ensure_smem_ptr(const void* kern, size_t bytes) {
 template <typename Kernel>
 inline cudaError_t ensure_smem(Kernel kern, size_t bytes) {
     return ensure_smem_ptr(reinterpret_cast<const void*>(kern), bytes);
+}
+
+// Launches kern<<<grid, block, smem, stream>>>(args...) with programmatic
+// dependent launch allowed (the kernel may be scheduled while the preceding
+// kernel on the stream finishes; it calls grid_dependency_wait before it
+// touches anything that kernel may write) and, if cluster_x > 1, as
+// clusters of cluster_x CTAs along x.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              int cluster_x, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (cluster_x > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = cluster_x;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 }  // namespace dflv

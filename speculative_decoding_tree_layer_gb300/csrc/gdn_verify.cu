@@ -18,14 +18,20 @@
 //         A_il = beta_i e^{g_i - g_l} (k_i . k_l),   R_i = beta_i v_i - beta_i e^{g_i} (S_0 k_i),
 //     o_i = e^{g_i} (S_0 q_i) + sum_{l in anc*(i)} M_il u_l,   M_il = e^{g_i - g_l} (k_l . q_i).
 // A and M depend on k, q, beta and the decays only -- not on the state -- so
-// every row of S_0 is independent: a CTA owns RB rows of one head, streams
-// them from HBM once through the bulk-copy (TMA) engine, forms
-// S_0[rows] . [K | Q] on the tensor cores (fp32 state split into bf16 hi +
-// lo, k and q exact in bf16), then solves the unit lower-triangular system
-// for u by substitution over the tree's depth levels (all nodes of a level
-// at once, one warp per node, lanes over rows) and mixes the outputs.  It
-// writes u, g and a copy of k as the factors commit needs, and never writes
-// S_0 (rollback is free).
+// every row of S_0 is independent: a CTA owns RB rows of one head and
+// streams them from HBM once through the bulk-copy (TMA) engine.  Half of
+// its warps form K K^T and Q K^T on the tensor cores (lower-triangular tiles
+// only) and apply the decays and the ancestor mask, giving dense
+// lower-triangular A and M; the other half form S_0[rows] . [K | Q] on the
+// tensor cores (fp32 state split into bf16 hi + lo, k and q exact in bf16).
+// Then one lane per row solves the unit lower-triangular system for u with
+// the node values in registers (nodes in index order: parent[i] < i), and
+// all warps mix the outputs.  The node count is padded to a compile-time
+// NPT (32 or 64) so every loop has a fixed trip count and the tensor-core
+// fragments of a step are loaded together.  With early prefetch the state
+// rows and the tree are fetched before the kernel waits for its predecessor.
+// It writes u, g and a copy of k as the factors commit needs, and never
+// writes S_0 (rollback is free).
 #include "common.cuh"
 #include "kernels.h"
 #include "tree.cuh"
@@ -36,6 +42,7 @@ namespace {
 
 constexpr int kGdnThreads = 256;
 constexpr int kGdnWarps = kGdnThreads / 32;
+constexpr int kHalfWarps = kGdnWarps / 2;
 
 struct GdnSmemLayout {
     int NP, DK, RB, KS;
@@ -45,50 +52,161 @@ struct GdnSmemLayout {
         off_V = off_S + (size_t)RB * DK * 4;     // bf16 v of this CTA's rows, [node][RB]
         off_K = off_V + (size_t)NP * RB * 2;
         off_Q = off_K + (size_t)NP * KS * 2;
-        off_A = off_Q + (size_t)NP * KS * 2;
-        off_M = off_A + (size_t)NP * NP * 4;
-        off_R = off_M + (size_t)NP * NP * 4;
-        off_SQ = off_R + (size_t)NP * RB * 4;
+        off_A = off_Q + (size_t)NP * KS * 2;     // dense [NP][NP], zero off the strict ancestors
+        off_M = off_A + (size_t)NP * NP * 4;     // dense [NP][NP], zero off the ancestors-or-self
+        off_R = off_M + (size_t)NP * NP * 4;     // [node][RB]: S_0 k, then u
+        off_SQ = off_R + (size_t)NP * RB * 4;    // [node][RB]: S_0 q
         total = off_SQ + (size_t)NP * RB * 4;
     }
 };
 
-// sum over the set bits l of m of w[l] * x[l * stride], four terms at a time
-// so the shared-memory loads of a group are in flight together
-DFLV_DEVINL float masked_dot(uint64_t m, const float* __restrict__ w, const float* __restrict__ x, int stride) {
-    float acc = 0.f;
-    while (m) {
-        int l[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            l[k] = m ? ffs64(m) : -1;
-            m &= m - 1;
-        }
-        float wv[4], xv[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            wv[k] = l[k] >= 0 ? w[l[k]] : 0.f;
-            xv[k] = l[k] >= 0 ? x[l[k] * stride] : 0.f;
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) acc = fmaf(wv[k], xv[k], acc);
-    }
-    return acc;
+// barrier over the first `count` threads of the block (whole warps), id != 0
+DFLV_DEVINL void named_barrier_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-template <int DK, int RB>
-__global__ void __launch_bounds__(kGdnThreads)
-    gdn_tree_verify_kernel(GdnVerifyArgs a, int NP) {
+// 4. [K ; Q] K^T on the tensor cores by the kHalfWarps warps of the first
+//    half: K K^T into A_s, Q K^T into M_s.  Only the 16 x 8 tiles that reach
+//    the diagonal or below are formed (ancestors have smaller indices); a
+//    warp keeps all of its tiles in flight at once.  The MMA's k index is
+//    permuted consistently on both operands: thread tq of a quad holds
+//    columns 4tq .. 4tq+3 of each 16-wide k step, so one 8-byte load fills
+//    both halves of its fragment registers.
+template <int DK, int NPT>
+DFLV_DEVINL void gdn_gram_tiles(const uint16_t* K_s, const uint16_t* Q_s, float* A_s, float* M_s, int warp,
+                                int gq, int tq) {
+    constexpr int KS = DK + 16;
+    constexpr int MT = NPT / 16;                 // 16-row tiles per half
+    constexpr int PER = MT * (MT + 1);           // lower tiles per half: 2m + 2 in tile row m
+    constexpr int TPW = 2 * PER / kHalfWarps;    // tiles per warp
+    static_assert((2 * PER) % kHalfWarps == 0, "tiles must split evenly over the warps");
+    const uint16_t* Ap[TPW];
+    const uint16_t* Bp[TPW];
+    float* dst[TPW];
+#pragma unroll
+    for (int t = 0; t < TPW; ++t) {
+        const int tile = warp + kHalfWarps * t;
+        const int half = tile / PER;             // 0: K rows (A), 1: Q rows (M)
+        int q = tile % PER, m = 0;
+        while (q >= 2 * m + 2) {
+            q -= 2 * m + 2;
+            ++m;
+        }
+        const int nt = q;
+        Ap[t] = (half ? Q_s : K_s) + (m * 16 + gq) * KS;
+        Bp[t] = K_s + (nt * 8 + gq) * KS;
+        dst[t] = (half ? M_s : A_s) + (m * 16 + gq) * NPT + nt * 8 + tq * 2;
+    }
+    float d[TPW][4];
+#pragma unroll
+    for (int t = 0; t < TPW; ++t) d[t][0] = d[t][1] = d[t][2] = d[t][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < DK / 16; ++ks) {
+        const int col = ks * 16 + tq * 4;
+        uint2 a0[TPW], a1[TPW], bb[TPW];
+#pragma unroll
+        for (int t = 0; t < TPW; ++t) {
+            a0[t] = *reinterpret_cast<const uint2*>(Ap[t] + col);
+            a1[t] = *reinterpret_cast<const uint2*>(Ap[t] + 8 * KS + col);
+            bb[t] = *reinterpret_cast<const uint2*>(Bp[t] + col);
+        }
+#pragma unroll
+        for (int t = 0; t < TPW; ++t) {
+            const uint32_t af[4] = {a0[t].x, a1[t].x, a0[t].y, a1[t].y};
+            const uint32_t bf[2] = {bb[t].x, bb[t].y};
+            mma_bf16_16816(d[t], af, bf);
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < TPW; ++t) {
+        dst[t][0] = d[t][0];
+        dst[t][1] = d[t][1];
+        dst[t][8 * NPT] = d[t][2];
+        dst[t][8 * NPT + 1] = d[t][3];
+    }
+}
+
+// 6. S_0[rows] . [K | Q] by the kHalfWarps warps wq of the second half: the
+//    fp32 state as bf16 hi + lo against exact bf16 k and q.  SK goes to
+//    R_s[node][row], SQ to SQ_s[node][row].  A warp owns one 16-row tile and
+//    J column tiles; hi and lo accumulate separately while that keeps the
+//    register count low, so no two consecutive MMAs depend on each other.
+template <int DK, int RB, int NPT>
+DFLV_DEVINL void gdn_state_products(const float* S_s, const uint16_t* K_s, const uint16_t* Q_s, float* R_s,
+                                    float* SQ_s, int wq, int gq, int tq) {
+    constexpr int KS = DK + 16;
+    constexpr int WM = RB / 16;              // m tiles (16 rows each)
+    constexpr int WN = kHalfWarps / WM;      // warps sharing one m tile
+    static_assert(WM * WN == kHalfWarps, "row block must split over the warps");
+    constexpr int J = 2 * NPT / 8 / WN;      // column tiles per warp
+    constexpr bool SPLIT = J <= 4;           // separate lo accumulators
+    const int mt = wq % WM, wn = wq / WM;
+    const uint16_t* Bp[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const int nt = wn + WN * j;
+        Bp[j] = (nt * 8 < NPT) ? K_s + (nt * 8 + gq) * KS : Q_s + (nt * 8 - NPT + gq) * KS;
+    }
+    float acc[J][4], acl[SPLIT ? J : 1][4];
+#pragma unroll
+    for (int j = 0; j < J; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+#pragma unroll
+    for (int j = 0; j < (SPLIT ? J : 1); ++j) acl[j][0] = acl[j][1] = acl[j][2] = acl[j][3] = 0.f;
+    const float* S0 = S_s + (mt * 16 + gq) * DK;
+    const float* S8 = S0 + 8 * DK;
+#pragma unroll 2
+    for (int ks = 0; ks < DK / 16; ++ks) {
+        const int col = ks * 16 + tq * 4;
+        const float4 s0 = *reinterpret_cast<const float4*>(S0 + col);
+        const float4 s1 = *reinterpret_cast<const float4*>(S8 + col);
+        uint2 bb[J];
+#pragma unroll
+        for (int j = 0; j < J; ++j) bb[j] = *reinterpret_cast<const uint2*>(Bp[j] + col);
+        uint32_t ahi[4], alo[4];
+        split_bf16x2(s0.x, s0.y, ahi[0], alo[0]);
+        split_bf16x2(s1.x, s1.y, ahi[1], alo[1]);
+        split_bf16x2(s0.z, s0.w, ahi[2], alo[2]);
+        split_bf16x2(s1.z, s1.w, ahi[3], alo[3]);
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            const uint32_t bf[2] = {bb[j].x, bb[j].y};
+            mma_bf16_16816(acc[j], ahi, bf);
+        }
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            const uint32_t bf[2] = {bb[j].x, bb[j].y};
+            if constexpr (SPLIT) mma_bf16_16816(acl[j], alo, bf);
+            else mma_bf16_16816(acc[j], alo, bf);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const int nt = wn + WN * j;
+        const int c = nt * 8 + tq * 2, row = mt * 16 + gq;
+        float* dst = (c < NPT) ? R_s + c * RB : SQ_s + (c - NPT) * RB;
+        float v[4] = {acc[j][0], acc[j][1], acc[j][2], acc[j][3]};
+        if constexpr (SPLIT) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[e] += acl[j][e];
+        }
+        dst[row] = v[0];
+        dst[RB + row] = v[1];
+        dst[row + 8] = v[2];
+        dst[RB + row + 8] = v[3];
+    }
+}
+
+template <int DK, int RB, int NPT>
+__global__ void __launch_bounds__(kGdnThreads, 2)
+    gdn_tree_verify_kernel(GdnVerifyArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
-    const GdnSmemLayout L(NP, DK, RB);
+    const GdnSmemLayout L(NPT, DK, RB);
     constexpr int KS = DK + 16;  // bf16 row stride: conflict-free 8-byte fragment loads
 
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
-    int32_t* misc_s = reinterpret_cast<int32_t*>(smem + 16);  // [0] = deepest level
+    int32_t* misc_s = reinterpret_cast<int32_t*>(smem + 16);  // [1]: the state copy timed out
     int32_t* par_s = reinterpret_cast<int32_t*>(smem + 64);
     int32_t* depth_s = par_s + kMaxNodes;
-    int32_t* order_s = depth_s + kMaxNodes;           // nodes sorted by depth
-    int32_t* lvl_s = order_s + kMaxNodes;             // first index of each level in order_s (65)
     uint64_t* amask_s = reinterpret_cast<uint64_t*>(smem + 64 + 4 * 256 + 512);
     float* beta_s = reinterpret_cast<float*>(smem + 64 + 4 * 256 + 512 + 512);
     float* la_s = beta_s + kMaxNodes;
@@ -109,205 +227,167 @@ __global__ void __launch_bounds__(kGdnThreads)
     const int N = a.N_max;
     const int hk = h / (a.Hv / a.Hk);
 
+    // With early prefetch, everything up to the dependency wait reads only
+    // the committed state and the tree, which the preceding kernel does not
+    // write; the rest waits for it.
+    const bool early = (a.flags & DFLV_FLAG_EARLY_PREFETCH) != 0;
+    if (!early) grid_dependency_wait();
     if (tid == 0) {
         mbar_init(bar, 1);
         fence_mbar_init();
-        misc_s[0] = 0;
+        misc_s[1] = 0;
     }
     __syncthreads();
-    grid_dependency_wait();
 
-    // 1. Every input of this CTA is requested at once: its RB rows of S_0
-    //    (contiguous) through the bulk-copy engine, and the parent array, the
-    //    node scalars, keys, queries and v block with 16- / 4-byte cp.async.
-    //    All N_max node rows are fetched (rows past n are never read back
-    //    into a result), so nothing waits for n.
+    // 1. This CTA's RB rows of S_0 (contiguous) through the bulk-copy engine,
+    //    and the parent array; then, once the inputs of this layer may be
+    //    read, the keys, queries, v block and node scalars with 16- / 4-byte
+    //    cp.async.  All N_max node rows are fetched (rows past n are never
+    //    read back into a result), so nothing waits for n.
     if (tid == 0) {
         const float* src = a.state + (((size_t)b * a.Hv + h) * a.dv + r0) * DK;
         mbar_arrive_expect_tx(bar, RB * DK * 4);
         bulk_g2s(S_s, src, RB * DK * 4, bar);
     }
-    constexpr int CH = DK / 8;  // 16-byte chunks per bf16 row
-    for (int idx = tid; idx < N * CH; idx += kGdnThreads) {
-        const int i = idx / CH, c = idx % CH;
-        const size_t off = (((size_t)b * N + i) * a.Hk + hk) * DK + c * 8;
-        cp_async16(K_s + i * KS + c * 8, a.k + off);
-        cp_async16(Q_s + i * KS + c * 8, a.q + off);
-    }
-    constexpr int VCH = RB / 8;  // 16-byte chunks of this CTA's v rows
-    for (int idx = tid; idx < N * VCH; idx += kGdnThreads) {
-        const int i = idx / VCH, c = idx % VCH;
-        cp_async16(V_s + i * RB + c * 8, a.v + (((size_t)b * N + i) * a.Hv + h) * a.dv + r0 + c * 8);
-    }
-    for (int i = tid; i < N; i += kGdnThreads) {
-        const size_t sidx = ((size_t)b * N + i) * a.Hv + h;
-        cp_async4(beta_s + i, a.beta + sidx);
-        cp_async4(la_s + i, a.log_alpha + sidx);
-        cp_async4(par_s + i, a.parent + (size_t)b * N + i);
-    }
+    for (int i = tid; i < N; i += kGdnThreads) cp_async4(par_s + i, a.parent + (size_t)b * N + i);
     cp_async_commit();
-    // rows [N, NP) of K and Q take part in the tensor-core tiles: zero them
-    for (int idx = tid; idx < (NP - N) * CH; idx += kGdnThreads) {
+    constexpr int CH = DK / 8;  // 16-byte chunks per bf16 row
+    auto issue_layer_inputs = [&]() {
+        for (int idx = tid; idx < N * CH; idx += kGdnThreads) {
+            const int i = idx / CH, c = idx % CH;
+            const size_t off = (((size_t)b * N + i) * a.Hk + hk) * DK + c * 8;
+            cp_async16(K_s + i * KS + c * 8, a.k + off);
+            cp_async16(Q_s + i * KS + c * 8, a.q + off);
+        }
+        constexpr int VCH = RB / 8;  // 16-byte chunks of this CTA's v rows
+        for (int idx = tid; idx < N * VCH; idx += kGdnThreads) {
+            const int i = idx / VCH, c = idx % VCH;
+            cp_async16(V_s + i * RB + c * 8, a.v + (((size_t)b * N + i) * a.Hv + h) * a.dv + r0 + c * 8);
+        }
+        for (int i = tid; i < N; i += kGdnThreads) {
+            const size_t sidx = ((size_t)b * N + i) * a.Hv + h;
+            cp_async4(beta_s + i, a.beta + sidx);
+            cp_async4(la_s + i, a.log_alpha + sidx);
+        }
+        cp_async_commit();
+    };
+    if (!early) {
+        grid_launch_dependents();
+        issue_layer_inputs();
+    }
+    // rows [N, NPT) of K and Q take part in the tensor-core tiles: zero them
+    for (int idx = tid; idx < (NPT - N) * CH; idx += kGdnThreads) {
         const int i = N + idx / CH, c = idx % CH;
         *reinterpret_cast<uint4*>(K_s + i * KS + c * 8) = make_uint4(0, 0, 0, 0);
         *reinterpret_cast<uint4*>(Q_s + i * KS + c * 8) = make_uint4(0, 0, 0, 0);
     }
     const int n = __ldg(a.n_nodes + b);
-    cp_async_wait<0>();
+    if (early) cp_async_wait<0>();
+    else cp_async_wait<1>();
     __syncthreads();
 
     // 2. Tree topology (from the staged parent array).
-    if (!block_tree_topology_smem(n, N, par_s, depth_s, amask_s, a.status)) {
-        if (tid == 0) mbar_wait_bounded(bar, 0, a.status);  // let the copy land before leaving
+    if (!block_tree_topology_smem(n, N, par_s, depth_s, amask_s, nullptr)) {
+        if (early) grid_dependency_wait();
+        cp_async_wait<0>();
+        if (tid == 0) {
+            raise_status(a.status, DFLV_DEV_TOPOLOGY);
+            mbar_wait_bounded(bar, 0, a.status);  // let the copy land before leaving
+        }
         return;
     }
-
-    // 3. Nodes ordered by depth (level d = order_s[lvl_s[d] .. lvl_s[d+1])).
-    for (int i = tid; i < n; i += kGdnThreads) {
-        const int d = depth_s[i];
-        int pos = 0;
-        for (int j = 0; j < n; ++j) {
-            const int dj = depth_s[j];
-            pos += (dj < d) || (dj == d && j < i);
-        }
-        order_s[pos] = i;
-        atomicMax(misc_s, d);
+    if (early) {
+        grid_dependency_wait();
+        grid_launch_dependents();
+        issue_layer_inputs();
     }
+    cp_async_wait<0>();
     __syncthreads();
-    const int maxd = misc_s[0];
-    for (int d = tid; d <= maxd + 1; d += kGdnThreads) {
-        int c = 0;
-        for (int j = 0; j < n; ++j) c += depth_s[j] < d;
-        lvl_s[d] = c;
-    }
-    // cumulative log decay over the ancestors-or-self
-    for (int i = tid; i < n; i += kGdnThreads) {
-        float g = 0.f;
-        for (uint64_t m = amask_s[i]; m; m &= m - 1) g += la_s[ffs64(m)];
-        g_s[i] = g;
-        G_s[i] = expf(g);
-    }
 
-    // 4. [K ; Q] K^T on the tensor cores: KK (rows < NP) and KQ (rows >= NP).
-    //    The MMA's k index is permuted consistently on both operands: thread
-    //    tq of a quad holds columns 4tq .. 4tq+3 of each 16-wide k step, so
-    //    one 8-byte load fills both halves of its fragment registers.
-    {
-        const int nt_count = NP / 8, tiles = (2 * NP / 16) * nt_count;
-        for (int tile = warp; tile < tiles; tile += kGdnWarps) {
-            const int mt = tile / nt_count, nt = tile % nt_count;
-            const uint16_t* Ap = (mt * 16 < NP) ? K_s + (mt * 16) * KS : Q_s + (mt * 16 - NP) * KS;
-            const uint16_t* Bp = K_s + (nt * 8 + gq) * KS;
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int ks = 0; ks < DK / 16; ++ks) {
-                const int col = ks * 16 + tq * 4;
-                const uint2 a0 = *reinterpret_cast<const uint2*>(Ap + gq * KS + col);
-                const uint2 a1 = *reinterpret_cast<const uint2*>(Ap + (gq + 8) * KS + col);
-                const uint2 bb = *reinterpret_cast<const uint2*>(Bp + col);
-                const uint32_t af[4] = {a0.x, a1.x, a0.y, a1.y};
-                const uint32_t bf[2] = {bb.x, bb.y};
-                mma_bf16_16816(d, af, bf);
+    if (warp < kHalfWarps) {
+        // 3. cumulative log decay over the ancestors-or-self
+        for (int i = tid; i < n; i += kGdnThreads / 2) {
+            float g = 0.f;
+            for (uint64_t m = amask_s[i]; m; m &= m - 1) g += la_s[ffs64(m)];
+            g_s[i] = g;
+            G_s[i] = expf(g);
+        }
+        gdn_gram_tiles<DK, NPT>(K_s, Q_s, A_s, M_s, warp, gq, tq);
+        named_barrier_sync(1, kGdnThreads / 2);
+        // 5. Decays and the ancestor mask, in place over the whole [NPT][NPT]:
+        //    A_il = beta_i e^{g_i-g_l} k_i.k_l for strict ancestors l of i,
+        //    M_il = e^{g_i-g_l} q_i.k_l for l in anc*(i), zero elsewhere
+        //    (including every row or column of a node >= n).
+        for (int idx = tid; idx < NPT * NPT; idx += kGdnThreads / 2) {
+            const int i = idx / NPT, l = idx % NPT;
+            float av = 0.f, mv = 0.f;
+            if (i < n && l <= i && ((amask_s[i] >> l) & 1ull)) {
+                const float dec = expf(g_s[i] - g_s[l]);
+                mv = dec * M_s[idx];
+                if (l != i) av = beta_s[i] * dec * A_s[idx];
             }
-            const int row = mt * 16 + gq, col = nt * 8 + tq * 2;
-            float* dst = (row < NP) ? A_s + row * NP : M_s + (row - NP) * NP;
-            dst[col] = d[0];
-            dst[col + 1] = d[1];
-            dst[8 * NP + col] = d[2];
-            dst[8 * NP + col + 1] = d[3];
+            A_s[idx] = av;
+            M_s[idx] = mv;
         }
+    } else {
+        // 6. S_0[rows] . [K | Q]
+        if (mbar_wait_bounded(bar, 0, a.status))
+            gdn_state_products<DK, RB, NPT>(S_s, K_s, Q_s, R_s, SQ_s, warp - kHalfWarps, gq, tq);
+        else if (lane == 0)
+            atomicOr(misc_s + 1, 1);
     }
     __syncthreads();
+    if (misc_s[1]) return;  // the state copy never landed (status already raised)
 
-    // 5. Decays and the ancestor mask:
-    //    A_il = beta_i e^{g_i-g_l} k_i.k_l (l strict ancestor), M_il = e^{g_i-g_l} q_i.k_l (l in anc*(i)).
-    for (int idx = tid; idx < n * n; idx += kGdnThreads) {
-        const int i = idx / n, l = idx % n;
-        const bool anc = (amask_s[i] >> l) & 1ull;
-        const float dec = anc ? expf(g_s[i] - g_s[l]) : 0.f;
-        A_s[i * NP + l] = (anc && l != i) ? beta_s[i] * dec * A_s[i * NP + l] : 0.f;
-        M_s[i * NP + l] = anc ? dec * M_s[i * NP + l] : 0.f;
-    }
-
-    // 6. S_0[rows] . [K | Q] on the tensor cores, fp32 state as bf16 hi + lo.
-    if (!mbar_wait_bounded(bar, 0, a.status)) return;
-    {
-        constexpr int WM = RB / 16;            // m tiles (16 rows each)
-        constexpr int WN = kGdnWarps / WM;     // warps sharing one m tile
-        const int mt = warp % WM, wn = warp / WM;
-        const int ntiles = 2 * NP / 8;
-        constexpr int kMaxJ = (2 * kMaxNodes / 8 + WN - 1) / WN;
-        float acc[kMaxJ][4];
+    // 7-8. Rows are independent: lane r of the first RB threads solves
+    //    u_i = R_i - sum_{l < i} A_il u_l,  R_i = beta_i (v_i - e^{g_i} S_0 k_i),
+    //    for all nodes in index order (a node's ancestors precede it) with
+    //    u in registers.  A is dense and zero off the ancestors, so every
+    //    trip count is fixed; the rows of A are read by all lanes at once.
+    if (tid < RB) {
+        const int r = tid;
+        float u[NPT];
 #pragma unroll
-        for (int j = 0; j < kMaxJ; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-        const float* S0 = S_s + (mt * 16 + gq) * DK;
-        const float* S8 = S0 + 8 * DK;
-#pragma unroll 2
-        for (int ks = 0; ks < DK / 16; ++ks) {
-            const int col = ks * 16 + tq * 4;
-            const float4 s0 = *reinterpret_cast<const float4*>(S0 + col);
-            const float4 s1 = *reinterpret_cast<const float4*>(S8 + col);
-            uint32_t ahi[4], alo[4];
-            split_bf16x2(s0.x, s0.y, ahi[0], alo[0]);
-            split_bf16x2(s1.x, s1.y, ahi[1], alo[1]);
-            split_bf16x2(s0.z, s0.w, ahi[2], alo[2]);
-            split_bf16x2(s1.z, s1.w, ahi[3], alo[3]);
+        for (int i = 0; i < NPT; ++i) u[i] = 0.f;
 #pragma unroll
-            for (int j = 0; j < kMaxJ; ++j) {
-                const int nt = wn + WN * j;
-                if (nt < ntiles) {
-                    const uint16_t* Bp = (nt * 8 < NP) ? K_s + (nt * 8 + gq) * KS
-                                                       : Q_s + (nt * 8 - NP + gq) * KS;
-                    const uint2 bb = *reinterpret_cast<const uint2*>(Bp + col);
-                    const uint32_t bf[2] = {bb.x, bb.y};
-                    mma_bf16_16816(acc[j], ahi, bf);
-                    mma_bf16_16816(acc[j], alo, bf);
+        for (int i = 0; i < NPT; ++i) {
+            if (i < n) {
+                float acc[4] = {beta_s[i] * (bf16_bits_to_float(V_s[i * RB + r]) - G_s[i] * R_s[i * RB + r]),
+                                0.f, 0.f, 0.f};
+                const float4* Ar = reinterpret_cast<const float4*>(A_s + i * NPT);
+#pragma unroll
+                for (int l4 = 0; l4 < (i + 3) / 4; ++l4) {
+                    const float4 w = Ar[l4];
+                    acc[0] = fmaf(-w.x, u[4 * l4], acc[0]);
+                    acc[1] = fmaf(-w.y, u[4 * l4 + 1], acc[1]);
+                    acc[2] = fmaf(-w.z, u[4 * l4 + 2], acc[2]);
+                    acc[3] = fmaf(-w.w, u[4 * l4 + 3], acc[3]);
                 }
+                u[i] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
             }
         }
-        // SK -> R_s[node][row], SQ -> SQ_s[node][row]
 #pragma unroll
-        for (int j = 0; j < kMaxJ; ++j) {
-            const int nt = wn + WN * j;
-            if (nt < ntiles) {
-                const int c = nt * 8 + tq * 2, row = mt * 16 + gq;
-                float* dst = (c < NP) ? R_s + c * RB : SQ_s + (c - NP) * RB;
-                dst[row] = acc[j][0];
-                dst[RB + row] = acc[j][1];
-                dst[row + 8] = acc[j][2];
-                dst[RB + row + 8] = acc[j][3];
-            }
-        }
+        for (int i = 0; i < NPT; ++i)
+            if (i < n) R_s[i * RB + r] = u[i];
     }
     __syncthreads();
 
-    // 7. R_j = beta_j (v_j - e^{g_j} S_0 k_j) for this CTA's rows.
-    for (int idx = tid; idx < n * RB; idx += kGdnThreads) {
-        const int j = idx / RB, r = idx % RB;
-        const float vv = bf16_bits_to_float(V_s[j * RB + r]);
-        R_s[j * RB + r] = beta_s[j] * (vv - G_s[j] * R_s[j * RB + r]);
-    }
-    __syncthreads();
-
-    // 8. u_i = R_i - sum_{l in anc(i)} A_il u_l, level by level (a node's
-    //    ancestors sit on shallower levels); R_s becomes U in place.
-    for (int d = 1; d <= maxd; ++d) {
-        const int l0 = lvl_s[d], l1 = lvl_s[d + 1];
-        for (int idx = l0 * RB + tid; idx < l1 * RB; idx += kGdnThreads) {
-            const int i = order_s[idx / RB], r = idx % RB;
-            const uint64_t m = amask_s[i] & ~(1ull << i);
-            R_s[i * RB + r] -= masked_dot(m, A_s + i * NP, R_s + r, RB);
-        }
-        __syncthreads();
-    }
-
-    // 9. o_i = e^{g_i} SQ_i + sum_{l in anc*(i)} M_il u_l; u and o to global.
+    // 9. o_i = e^{g_i} SQ_i + sum_{l <= i} M_il u_l; u and o to global.
     for (int idx = tid; idx < n * RB; idx += kGdnThreads) {
         const int i = idx / RB, r = idx % RB;
-        const float O = G_s[i] * SQ_s[i * RB + r] + masked_dot(amask_s[i], M_s + i * NP, R_s + r, RB);
+        const float4* Mr = reinterpret_cast<const float4*>(M_s + i * NPT);
+        float acc0 = G_s[i] * SQ_s[i * RB + r], acc1 = 0.f;
+        for (int l4 = 0; l4 <= i / 4; ++l4) {
+            const float4 w = Mr[l4];
+            const int l = 4 * l4;
+            acc0 = fmaf(w.x, R_s[l * RB + r], acc0);
+            acc1 = fmaf(w.y, R_s[(l + 1) * RB + r], acc1);
+            acc0 = fmaf(w.z, R_s[(l + 2) * RB + r], acc0);
+            acc1 = fmaf(w.w, R_s[(l + 3) * RB + r], acc1);
+        }
         const size_t off = (((size_t)b * N + i) * a.Hv + h) * a.dv + r0 + r;
         a.u[off] = R_s[i * RB + r];
-        a.out[off] = O;
+        a.out[off] = acc0 + acc1;
     }
 
     // 10. The remaining factors, once per (sequence, head) / (sequence, q/k head).
@@ -322,29 +402,28 @@ __global__ void __launch_bounds__(kGdnThreads)
     }
 }
 
-template <int DK, int RB>
+template <int DK, int RB, int NPT>
 cudaError_t launch_dk_rb(const GdnVerifyArgs& a, cudaStream_t stream) {
-    const int NP = ((a.N_max + 15) / 16) * 16;
-    const GdnSmemLayout L(NP, DK, RB);
-    auto kern = gdn_tree_verify_kernel<DK, RB>;
+    const GdnSmemLayout L(NPT, DK, RB);
+    auto kern = gdn_tree_verify_kernel<DK, RB, NPT>;
     cudaError_t e = ensure_smem(kern, L.total);
     if (e != cudaSuccess) return e;
     dim3 grid(a.dv / RB, a.Hv, a.B);
-    kern<<<grid, kGdnThreads, L.total, stream>>>(a, NP);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, dim3(kGdnThreads), L.total, stream, 1, a);
 }
 
 template <int DK>
 cudaError_t launch_dk(const GdnVerifyArgs& a, cudaStream_t stream) {
-    if (a.dv % 32 == 0) return launch_dk_rb<DK, 32>(a, stream);
-    return launch_dk_rb<DK, 16>(a, stream);
+    const bool small = a.N_max <= 32;
+    if (a.dv % 32 == 0)
+        return small ? launch_dk_rb<DK, 32, 32>(a, stream) : launch_dk_rb<DK, 32, 64>(a, stream);
+    return small ? launch_dk_rb<DK, 16, 32>(a, stream) : launch_dk_rb<DK, 16, 64>(a, stream);
 }
 
 }  // namespace
 
 size_t gdn_verify_smem_bytes(int N_max, int dk, int dv) {
-    const int NP = ((N_max + 15) / 16) * 16;
-    return GdnSmemLayout(NP, dk, dv % 32 == 0 ? 32 : 16).total;
+    return GdnSmemLayout(N_max <= 32 ? 32 : 64, dk, dv % 32 == 0 ? 32 : 16).total;
 }
 
 cudaError_t launch_gdn_tree_verify(const GdnVerifyArgs& a, cudaStream_t stream) {

@@ -10,6 +10,7 @@ namespace dflv {
 
 struct GdnVerifyArgs {
     int B, N_max, Hk, Hv, dk, dv;
+    unsigned flags;  // DFLV_FLAG_*
     const int32_t* parent;
     const int32_t* n_nodes;
     const uint16_t* q;
@@ -31,6 +32,7 @@ size_t gdn_verify_smem_bytes(int N_max, int dk, int dv);
 struct AttnVerifyArgs {
     int B, N_max, Hq, Hkv, D, cap, window, type;
     float scale;
+    unsigned flags;  // DFLV_FLAG_*
     const int32_t* parent;
     const int32_t* n_nodes;
     const int32_t* n_past;

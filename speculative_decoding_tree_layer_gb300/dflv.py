@@ -21,6 +21,7 @@ HEADER = os.path.join(os.path.dirname(_HERE), "include", "dflv.h")
 DFLV_OK, DFLV_ERR_INVALID_ARG, DFLV_ERR_TOPOLOGY, DFLV_ERR_UNSUPPORTED, DFLV_ERR_CAPACITY, DFLV_ERR_CUDA = range(6)
 DFLV_DEV_TOPOLOGY, DFLV_DEV_CAPACITY, DFLV_DEV_PATH, DFLV_DEV_TIMEOUT = 1, 2, 4, 8
 DFLV_KV_Q8_0, DFLV_KV_Q4_0, DFLV_KV_F32 = 0, 1, 2
+DFLV_FLAG_EARLY_PREFETCH = 1
 DFLV_MAX_COMMIT_GDN_LAYERS, DFLV_MAX_COMMIT_ATTN_LAYERS = 128, 64
 
 _c_i32 = ctypes.c_int32
@@ -28,7 +29,8 @@ _vp = ctypes.c_void_p
 
 
 class dflv_gdn_desc(ctypes.Structure):
-    _fields_ = [("B", _c_i32), ("N_max", _c_i32), ("Hk", _c_i32), ("Hv", _c_i32), ("dk", _c_i32), ("dv", _c_i32)]
+    _fields_ = [("B", _c_i32), ("N_max", _c_i32), ("Hk", _c_i32), ("Hv", _c_i32), ("dk", _c_i32), ("dv", _c_i32),
+                ("flags", ctypes.c_uint32)]
 
 
 class dflv_gdn_factors(ctypes.Structure):
@@ -37,7 +39,8 @@ class dflv_gdn_factors(ctypes.Structure):
 
 class dflv_attn_desc(ctypes.Structure):
     _fields_ = [("B", _c_i32), ("N_max", _c_i32), ("Hq", _c_i32), ("Hkv", _c_i32), ("D", _c_i32),
-                ("cap", _c_i32), ("window", _c_i32), ("type", ctypes.c_int), ("scale", ctypes.c_float)]
+                ("cap", _c_i32), ("window", _c_i32), ("type", ctypes.c_int), ("scale", ctypes.c_float),
+                ("flags", ctypes.c_uint32)]
 
 
 class dflv_kv_layer(ctypes.Structure):
@@ -119,16 +122,16 @@ def check(code: int, where: str = "dflv"):
 
 
 # ---------------------------------------------------------------- structs from tensors
-def gdn_desc(B, N_max, Hk, Hv, dk, dv):
-    return dflv_gdn_desc(B, N_max, Hk, Hv, dk, dv)
+def gdn_desc(B, N_max, Hk, Hv, dk, dv, flags=0):
+    return dflv_gdn_desc(B, N_max, Hk, Hv, dk, dv, flags)
 
 
 def gdn_factors(u, g, kcopy):
     return dflv_gdn_factors(_ptr(u), _ptr(g), _ptr(kcopy))
 
 
-def attn_desc(B, N_max, Hq, Hkv, D, cap, window, kv_type, scale):
-    return dflv_attn_desc(B, N_max, Hq, Hkv, D, cap, window, kv_type, scale)
+def attn_desc(B, N_max, Hq, Hkv, D, cap, window, kv_type, scale, flags=0):
+    return dflv_attn_desc(B, N_max, Hq, Hkv, D, cap, window, kv_type, scale, flags)
 
 
 def kv_layer(kq, vq, ks=None, vs=None):

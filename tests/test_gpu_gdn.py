@@ -24,7 +24,7 @@ def dflv():
     return pkg
 
 
-def gpu_gdn(dflv, parent, n_nodes, inp, Hk, Hv, dk, dv, expect_status=0):
+def gpu_gdn(dflv, parent, n_nodes, inp, Hk, Hv, dk, dv, expect_status=0, flags=0):
     B, N = parent.shape
     keep = {k: dev(v) for k, v in inp.items()}
     keep["parent"], keep["n_nodes"] = dev(parent), dev(n_nodes)
@@ -33,7 +33,7 @@ def gpu_gdn(dflv, parent, n_nodes, inp, Hk, Hv, dk, dv, expect_status=0):
     g = torch.full((B, N, Hv), float("nan"), dtype=torch.float32, device="cuda")
     kc = torch.zeros((B, N, Hk, dk), dtype=torch.int16, device="cuda")
     st = zeros_status()
-    rc = dflv.dflv_tree_gdn_verify(dflv.gdn_desc(B, N, Hk, Hv, dk, dv), keep["parent"], keep["n_nodes"],
+    rc = dflv.dflv_tree_gdn_verify(dflv.gdn_desc(B, N, Hk, Hv, dk, dv, flags), keep["parent"], keep["n_nodes"],
                                    keep["q"], keep["k"], keep["v"], keep["beta"], keep["log_alpha"],
                                    keep["state"], out, dflv.gdn_factors(u, g, kc), st)
     dflv.check(rc, "dflv_tree_gdn_verify")
@@ -141,6 +141,48 @@ def test_gdn_bad_topology_sets_status(dflv):
     n_bad = np.array([0, 5], np.int32)
     gpu_gdn(dflv, synth.batch_trees([synth.chain_tree(4)] * 2, 4)[0], n_bad, inp, 1, 2, 16, 16,
             expect_status=dflv.DFLV_DEV_TOPOLOGY)
+    # the same with the tree read before the dependency wait
+    gpu_gdn(dflv, parent, n_nodes, inp, 1, 2, 16, 16, expect_status=dflv.DFLV_DEV_TOPOLOGY,
+            flags=dflv.DFLV_FLAG_EARLY_PREFETCH)
+
+
+def test_gdn_layers_back_to_back_with_early_prefetch(dflv, orc):
+    # four layers launched back to back on one stream, every layer after the
+    # first with the state and tree read before the dependency wait; each
+    # layer's inputs are written by an elementwise kernel queued just before
+    # it, so a kernel that read them before its dependency wait could still
+    # see the zeros they held
+    rng = np.random.default_rng(1240)
+    par, _ = synth.ddtree(rng, 22, 151936)
+    parent, n_nodes = synth.batch_trees([par], 22)
+    dp, dn = dev(parent), dev(n_nodes)
+    G = synth.GDN_27B
+    st = zeros_status()
+    layers = []
+    for li in range(4):
+        inp = synth.gdn_inputs(rng, 1, 22, **G)
+        src = {k: dev(v) for k, v in inp.items()}
+        dst = {k: torch.zeros_like(v) for k, v in src.items()}
+        out = torch.full((1, 22, G["Hv"], G["dv"]), float("nan"), device="cuda")
+        u = torch.empty_like(out)
+        g = torch.empty((1, 22, G["Hv"]), device="cuda")
+        kc = torch.empty((1, 22, G["Hk"], G["dk"]), dtype=torch.int16, device="cuda")
+        layers.append((inp, src, dst, out, u, g, kc))
+    for inp, src, dst, out, u, g, kc in layers:
+        dst["state"].copy_(src["state"])   # the committed state: not produced inside the step
+    torch.cuda.synchronize()
+    for li, (inp, src, dst, out, u, g, kc) in enumerate(layers):
+        for k in ("q", "k", "v", "beta", "log_alpha"):
+            torch.mul(src[k], 1, out=dst[k])   # an elementwise kernel produces this layer's inputs
+        flags = 0 if li == 0 else dflv.DFLV_FLAG_EARLY_PREFETCH
+        dflv.check(dflv.dflv_tree_gdn_verify(dflv.gdn_desc(1, 22, G["Hk"], G["Hv"], G["dk"], G["dv"], flags), dp, dn,
+                                             dst["q"], dst["k"], dst["v"], dst["beta"], dst["log_alpha"],
+                                             dst["state"], out, dflv.gdn_factors(u, g, kc), st))
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for inp, src, dst, out, u, g, kc in layers:
+        ref = oracle_gdn(orc, parent, n_nodes, inp)
+        compare_valid(host(out), ref, n_nodes, "o")
 
 
 def test_gdn_state_is_read_only(dflv):
