@@ -45,7 +45,8 @@
  *     DFLV_DEV_* bits; the outputs of the affected sequence are then
  *     unspecified.  status_dev points to one int32 in device memory that the
  *     caller zeroes and reads back when it wants to check.
- *   - Pointers to bf16/f32/int8/u8 arrays must be 16-byte aligned.
+ *   - Pointers to bf16/f32/int8/u8 arrays and to the fp16 scale planes of a
+ *     KV cache must be 16-byte aligned.
  *   - No global state: calls are re-entrant on distinct buffers.
  *   - Padded nodes (i >= n_nodes[b]) are ignored; their outputs are
  *     unspecified.

@@ -51,11 +51,9 @@ dflv_status check_attn_desc(const dflv_attn_desc* d) {
 dflv_status check_kv_layer(const dflv_attn_desc* d, const dflv_kv_layer* c) {
     if (!c || !c->kq || !c->vq || !aligned16(c->kq) || !aligned16(c->vq)) return DFLV_ERR_INVALID_ARG;
     if (d->type != DFLV_KV_F32) {
-        if (!c->ks || !c->vs) return DFLV_ERR_INVALID_ARG;
-        // one scale row is D/32 halves = 4, 8 or 16 bytes and is copied whole
-        const int row = d->D / 32 * 2;
-        if ((reinterpret_cast<uintptr_t>(c->ks) % row) || (reinterpret_cast<uintptr_t>(c->vs) % row))
-            return DFLV_ERR_INVALID_ARG;
+        // the scale planes are read by the bulk-copy engine from 16-byte
+        // aligned addresses
+        if (!c->ks || !c->vs || !aligned16(c->ks) || !aligned16(c->vs)) return DFLV_ERR_INVALID_ARG;
     }
     return DFLV_OK;
 }

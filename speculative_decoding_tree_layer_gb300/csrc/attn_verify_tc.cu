@@ -9,25 +9,29 @@
 // cached positions inside its window and to its ancestors-or-self.
 //
 // How: one thread-block cluster per (sequence, KV head, row tile of <= 128
-// query rows); the cluster's CTAs split the visible keys (and the tree
-// block) into 32-key tiles.  Per CTA and tile:
-//   * the int8 / 4-bit codes arrive by 16-byte cp.async (double-buffered)
-//     and are staged as a pair of fp16 tiles hi + lo with the block scale
-//     folded in (d * code is exact in fp32; hi = fp16(x), lo = fp16(x - hi)),
-//     so the products below are exact to ~2^-22;
-//   * one thread issues tcgen05.mma: [S_hi | S_lo] = Q [K_hi ; K_lo]^T into
-//     tensor memory (M = 128 rows, N = 64 = the two 32-key halves stored
-//     back to back, K = head size); S = S_hi + S_lo;
-//   * eight warps read S (TMEM lane = query row; warps w and w + 4 share a
-//     lane range and take 16 keys each), apply the tree / window mask, run an
-//     fp32 online softmax with a lazily updated running max (rescaling O in
-//     tensor memory only when a row's max grows by more than 2^8), and write
-//     P as fp16 hi + lo;
-//   * one thread issues O += P_hi V_hi + P_hi V_lo + P_lo V_hi (M = 128,
-//     N = head size, K = 32) with O resident in tensor memory across tiles;
-//   * partial (max, sum, O) are merged across the cluster through
-//     distributed shared memory.
-// Operands use the no-swizzle core-matrix layout described in tcgen05.cuh.
+// query rows); the cluster's CTAs split the visible cache keys evenly into
+// 32-key tiles (tile starts aligned to 32 keys), and the tree block is one
+// or two extra tiles.  Inside a CTA the tiles flow through a pipeline of
+// three warp roles that hand over through mbarriers (every wait bounded):
+//   * stage warps (4): raw codes and scales arrive by bulk copies (TMA
+//     engine, double-buffered, requested for the first tiles before the
+//     kernel waits for its predecessor when early prefetch is on); they are
+//     expanded into fp16 hi + lo tiles with the block scale folded in
+//     (d * code is exact in fp32; hi = fp16(x), lo = fp16(x - hi)).  K tiles
+//     are double-buffered.  A tree tile is quantised from the new keys and
+//     values in place (and written to the cache);
+//   * the MMA warp (1) issues tcgen05.mma: [S_hi | S_lo] = Q [K_hi ; K_lo]^T
+//     into one of two S buffers in tensor memory (M = 128, N = 64, K = head
+//     size), so the next tile's scores are formed while the softmax works on
+//     this one, and O += P_hi V_hi + P_hi V_lo + P_lo V_hi with O resident in
+//     tensor memory;
+//   * softmax warps (4): one thread per query row (its TMEM lane) reads the
+//     32 scores, applies the tree / window mask and an fp32 online softmax
+//     with a lazily updated running max (O is rescaled in tensor memory only
+//     when a row's max grows by more than 2^8), and writes P as fp16 hi + lo.
+// Partial (max, sum, O) are merged across the cluster through distributed
+// shared memory.  Operands use the no-swizzle core-matrix layout described
+// in tcgen05.cuh.
 #include <climits>
 
 #include "attn_common.cuh"
@@ -42,75 +46,121 @@ namespace {
 
 using namespace attn;
 
-constexpr int kTK = 32;        // keys per tile
-constexpr int kRows = 128;     // MMA M: query rows per CTA
-constexpr int kThreads = 256;  // all warps stage; softmax: two threads per row (16 keys each)
+constexpr int kTK = 32;          // keys per tile
+constexpr int kRows = 128;       // MMA M: query rows per CTA
+constexpr int kSoftWarps = 4;    // warps 0-3
+constexpr int kStageWarps = 4;   // warps 4-7
+constexpr int kMmaWarp = kSoftWarps + kStageWarps;  // warp 8
+constexpr int kLoadWarp = kMmaWarp + 1;              // warp 9: raw tile copies
+constexpr int kThreads = (kLoadWarp + 1) * 32;
+constexpr int kStage0 = kSoftWarps * 32;             // first stage thread
+constexpr int kStageThreads = kStageWarps * 32;
+constexpr int kStageBarrier = 2;                     // named barrier of the stage warps
 
 template <int D, int TYPE>
-struct TcSmem {
+struct TcLayout {
     static constexpr int NB = D / 32;
     static constexpr int KB = (TYPE == DFLV_KV_Q8_0) ? D : D / 2;  // code bytes per key row
     static constexpr int RSK = KB + 16;                               // padded raw row stride
     static constexpr int OS = D + 4;                                  // merge row stride (floats)
-    static constexpr size_t kHeader = 3072;  // tree arrays, barriers, [2][128] exchange floats at 2048
+    static constexpr size_t kHeader = 2048;   // tree arrays, barriers, flags
     static constexpr size_t kQ = (size_t)kRows * D * 2;
-    static constexpr size_t kKV = (size_t)kTK * D * 2;   // one of K_hi, K_lo, V_hi, V_lo
-    static constexpr size_t kP = (size_t)kRows * kTK * 2;
+    static constexpr size_t kK = (size_t)2 * kTK * D * 2;    // K_hi rows 0-31, K_lo rows 32-63
+    static constexpr size_t kV = (size_t)kTK * D * 2;        // one of V_hi, V_lo
+    static constexpr size_t kP = (size_t)kRows * kTK * 2;    // one of P_hi, P_lo
     static constexpr size_t kRawCodes = (size_t)kTK * RSK;
-    static constexpr size_t kRawScales = (size_t)kTK * NB * 2;
-    static constexpr size_t kRaw = 2 * kRawCodes + 2 * kRawScales;
+    static constexpr size_t kRawScales = (size_t)kTK * NB * 2 + 16;  // + room for a misaligned start
+    static constexpr size_t kRaw = kRawCodes + kRawScales;           // one plane (K or V) of one tile
     static constexpr size_t off_Q = kHeader;
-    static constexpr size_t off_Khi = off_Q + kQ;
-    static constexpr size_t off_Klo = off_Khi + kKV;
-    static constexpr size_t off_Vhi = off_Klo + kKV;
-    static constexpr size_t off_Vlo = off_Vhi + kKV;
-    static constexpr size_t off_Phi = off_Vlo + kKV;
+    static constexpr size_t off_K = off_Q + kQ;              // two buffers
+    static constexpr size_t off_Vhi = off_K + 2 * kK;
+    static constexpr size_t off_Vlo = off_Vhi + kV;
+    static constexpr size_t off_Phi = off_Vlo + kV;
     static constexpr size_t off_Plo = off_Phi + kP;
-    static constexpr size_t off_raw = off_Plo + kP;
-    static constexpr size_t loop_total = off_raw + 2 * kRaw;
+    static constexpr size_t off_rawK = off_Plo + kP;         // two buffers
+    static constexpr size_t off_rawV = off_rawK + 2 * kRaw;  // two buffers
+    static constexpr size_t loop_total = off_rawV + 2 * kRaw;
     static constexpr size_t off_Om = kHeader;
     static constexpr size_t off_Mm = off_Om + (size_t)kRows * OS * 4;
     static constexpr size_t off_Lm = off_Mm + (size_t)kRows * 4;
     static constexpr size_t merge_total = off_Lm + (size_t)kRows * 4;
     static constexpr size_t total = loop_total > merge_total ? loop_total : merge_total;
-    static constexpr uint32_t kTmemCols = (D + 2 * kTK <= 256) ? 256 : 512;  // O at column 0, S after it
+    static constexpr uint32_t kTmemCols = (D + 4 * kTK <= 256) ? 256 : 512;  // O, then two S buffers
+    static_assert(kRawCodes % 16 == 0 && kRaw % 16 == 0, "bulk-copy destinations stay 16-byte aligned");
 };
 
-// Stage one 32-key tile of K or V codes as fp16 hi + lo with the block scale
-// folded in; rows past count are zero.  Items are ordered key % 8 fastest so
-// that 8 consecutive threads fill one 128-byte run of a core matrix.
+// header offsets
+constexpr int kHdrDepth = 256, kHdrMask = 512, kHdrBar = 1024, kHdrSlot = 1152, kHdrFail = 1156;
+enum Bar { kRawK0, kRawK1, kRawV0, kRawV1, kKFree0, kKFree1, kVFree0, kVFree1, kKReady0, kKReady1, kVReady,
+           kSFull0, kSFull1, kPReady, kODone, kMmaFin, kNumBars };
+static_assert(kHdrBar + kNumBars * 8 <= kHdrSlot, "barriers fit below the TMEM slot");
+
+DFLV_DEVINL bool wait_phase(uint64_t* bar, uint32_t parity) {
+    for (uint32_t it = 0; it < kWaitLimit; ++it)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+// Expand one raw tile (codes + scales of `count` keys) into fp16 hi + lo with
+// the block scale d folded in; rows past count are zero.  Codes become exact
+// fp16 values by byte permutation; hi = d * code rounded once (HMUL2) and
+// lo = d * code - hi rounded once (HFMA2: the fused product is exact), the
+// same bits as rounding the exact fp32 product and its remainder.  The 128
+// stage threads take items key % 8 fastest, so 8 consecutive threads fill
+// one 128-byte core-matrix run.
 template <int D, int TYPE>
 DFLV_DEVINL void stage_hilo(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scales, int count,
-                            uint8_t* __restrict__ hi, uint8_t* __restrict__ lo, int tid) {
-    using S = TcSmem<D, TYPE>;
+                            uint8_t* __restrict__ hi, uint8_t* __restrict__ lo, int st) {
+    using L = TcLayout<D, TYPE>;
     constexpr int C8 = D / 8;
-    for (int idx = tid; idx < kTK * C8; idx += kThreads) {
+    constexpr int PER = kTK * C8 / kStageThreads;  // items per thread
+    static_assert(PER * kStageThreads == kTK * C8, "items split evenly over the stage threads");
+    uint2 wv[PER];
+    uint16_t sbv[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {  // every load first
+        const int idx = st + j * kStageThreads;
+        const int c = (idx & 7) + (idx / (8 * C8)) * 8, d8 = (idx >> 3) % C8;
+        wv[j] = make_uint2(0, 0);
+        sbv[j] = 0;
+        if (c < count) {
+            sbv[j] = scales[c * L::NB + (d8 * 8) / 32];
+            if constexpr (TYPE == DFLV_KV_Q8_0) {
+                wv[j] = *reinterpret_cast<const uint2*>(codes + c * L::RSK + d8 * 8);
+            } else {
+                const int blk = (d8 * 8) / 32, off = (d8 * 8) % 32;
+                wv[j] = *reinterpret_cast<const uint2*>(codes + c * L::RSK + blk * 16 + (off & 15));
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const int idx = st + j * kStageThreads;
         const int c = (idx & 7) + (idx / (8 * C8)) * 8;  // key
         const int d8 = (idx >> 3) % C8;                    // 8-dim chunk
         uint4 h = make_uint4(0, 0, 0, 0), l = make_uint4(0, 0, 0, 0);
         if (c < count) {
-            const float sc = __half2float(__ushort_as_half(scales[c * S::NB + (d8 * 8) / 32]));
-            float x[8];
+            const __half2 d2 = __halves2half2(__ushort_as_half(sbv[j]), __ushort_as_half(sbv[j]));
+            uint32_t cv[4];  // 8 codes as 4 half2
+            const uint2 w = wv[j];
             if constexpr (TYPE == DFLV_KV_Q8_0) {
-                const uint2 w = *reinterpret_cast<const uint2*>(codes + c * S::RSK + d8 * 8);
-                const uint32_t ww[2] = {w.x, w.y};
-#pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = sc * (float)(int8_t)((ww[e >> 2] >> (8 * (e & 3))) & 0xff);
+                i8x4_to_f16x2(w.x, cv[0], cv[1]);
+                i8x4_to_f16x2(w.y, cv[2], cv[3]);
             } else {
-                const int blk = (d8 * 8) / 32, off = (d8 * 8) % 32;
-                const uint2 w = *reinterpret_cast<const uint2*>(codes + c * S::RSK + blk * 16 + (off & 15));
-                const uint32_t ww[2] = {w.x, w.y};
-                const int sh = off >= 16 ? 4 : 0;
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    x[e] = sc * (float)((int)((ww[e >> 2] >> (8 * (e & 3) + sh)) & 15) - 8);
+                // element j < 16 of a 32-block in the low nibble of byte j,
+                // element j + 16 in its high nibble
+                const int off = (d8 * 8) % 32;
+                const uint32_t m0 = off >= 16 ? (w.x >> 4) & 0x0f0f0f0fu : w.x & 0x0f0f0f0fu;
+                const uint32_t m1 = off >= 16 ? (w.y >> 4) & 0x0f0f0f0fu : w.y & 0x0f0f0f0fu;
+                u4x4_to_f16x2(m0, cv[0], cv[1]);
+                u4x4_to_f16x2(m1, cv[2], cv[3]);
             }
             uint32_t hv[4], lv[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const __half2 h2 = __floats2half2_rn(x[2 * e], x[2 * e + 1]);
-                const float2 hf = __half22float2(h2);
-                const __half2 l2 = __floats2half2_rn(x[2 * e] - hf.x, x[2 * e + 1] - hf.y);
+                const __half2 x = *reinterpret_cast<const __half2*>(&cv[e]);
+                const __half2 h2 = __hmul2(x, d2);
+                const __half2 l2 = __hfma2(x, d2, __hneg2(h2));
                 hv[e] = *reinterpret_cast<const uint32_t*>(&h2);
                 lv[e] = *reinterpret_cast<const uint32_t*>(&l2);
             }
@@ -123,41 +173,76 @@ DFLV_DEVINL void stage_hilo(const uint8_t* __restrict__ codes, const uint16_t* _
     }
 }
 
-DFLV_DEVINL bool wait_phase(uint64_t* bar, uint32_t parity) {
-    for (uint32_t it = 0; it < kWaitLimit; ++it)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
+// Request one raw plane (codes + scales) of a cache tile with 16-byte
+// cp.async copies spread over the 32 lanes of the load warp; each lane then
+// arrives on bar (initialised for 32 arrivals) once its own copies have
+// landed.  The
+// scales are copied from the 16-byte boundary at or below the first one
+// (their byte offset in the buffer is returned by scale_shift).
+template <int D, int TYPE>
+DFLV_DEVINL int scale_shift(const uint16_t* plane_scales, size_t row0, int start) {
+    using L = TcLayout<D, TYPE>;
+    return (int)(reinterpret_cast<uintptr_t>(plane_scales + (row0 + start) * L::NB) & 15);
 }
 
 template <int D, int TYPE>
+DFLV_DEVINL void issue_raw(const uint8_t* plane_codes, const uint16_t* plane_scales, size_t row0, int start,
+                           int count, uint8_t* raw, uint64_t* bar, int st) {
+    using L = TcLayout<D, TYPE>;
+    constexpr int CPR = L::KB / 16;  // 16-byte chunks per key row
+    for (int idx = st; idx < count * CPR; idx += 32) {
+        const int c = idx / CPR, ch = idx % CPR;
+        cp_async16(raw + c * L::RSK + ch * 16, plane_codes + (row0 + start + c) * L::KB + ch * 16);
+    }
+    const uintptr_t sa = reinterpret_cast<uintptr_t>(plane_scales + (row0 + start) * L::NB);
+    const int shift = (int)(sa & 15);
+    const int schunks = (shift + count * L::NB * 2 + 15) >> 4;
+    for (int idx = st; idx < schunks; idx += 32)
+        cp_async16(raw + L::kRawCodes + idx * 16, reinterpret_cast<const void*>(sa - shift + idx * 16));
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// barrier over `count` threads (whole warps) under id; returns the OR of
+// pred over them, the same value in every participating thread
+DFLV_DEVINL bool named_barrier_or(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+struct TileInfo {
+    int start, count;
+    bool tree;
+};
+
+template <int D, int TYPE>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, int RT, int CS) {
-    using S = TcSmem<D, TYPE>;
-    constexpr int NB = S::NB, KB = S::KB, RSK = S::RSK, OS = S::OS;
+    using L = TcLayout<D, TYPE>;
+    constexpr int NB = L::NB, OS = L::OS;
     extern __shared__ __align__(1024) unsigned char smem[];
     int32_t* par_s = reinterpret_cast<int32_t*>(smem);
-    int32_t* depth_s = par_s + kMaxNodes;
-    uint64_t* amask_s = reinterpret_cast<uint64_t*>(smem + 512);
-    uint64_t* bar_s = reinterpret_cast<uint64_t*>(smem + 1024);   // QK done
-    uint64_t* bar_o = bar_s + 1;                                   // PV done
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 1040);
-    int32_t* fail_s = reinterpret_cast<int32_t*>(smem + 1044);
-    float* xch_s = reinterpret_cast<float*>(smem + 2048);  // [2][128] per-half tile max / row sum
-    unsigned char* Q_s = smem + S::off_Q;
-    unsigned char* Khi_s = smem + S::off_Khi;
-    unsigned char* Klo_s = smem + S::off_Klo;
-    unsigned char* Vhi_s = smem + S::off_Vhi;
-    unsigned char* Vlo_s = smem + S::off_Vlo;
-    unsigned char* Phi_s = smem + S::off_Phi;
-    unsigned char* Plo_s = smem + S::off_Plo;
-    unsigned char* raw_s = smem + S::off_raw;
+    int32_t* depth_s = reinterpret_cast<int32_t*>(smem + kHdrDepth);
+    uint64_t* amask_s = reinterpret_cast<uint64_t*>(smem + kHdrMask);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kHdrBar);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kHdrSlot);
+    int32_t* fail_s = reinterpret_cast<int32_t*>(smem + kHdrFail);
+    auto failed = [&]() { return *reinterpret_cast<volatile int32_t*>(fail_s) != 0; };
+    unsigned char* Q_s = smem + L::off_Q;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rank = (int)cluster_ctarank();
     const int kvh = blockIdx.y % a.Hkv, rt = blockIdx.y / a.Hkv, b = blockIdx.z;
     const int G = a.Hq / a.Hkv, N = a.N_max, W = a.window;
+    const bool early = (a.flags & DFLV_FLAG_EARLY_PREFETCH) != 0;
 
-    grid_dependency_wait();
-    grid_launch_dependents();
+    // Before the dependency wait (early prefetch) only the tree, n_past and
+    // the cached slots below P are read; none of them is written by the
+    // kernel this one may overlap.
+    if (!early) grid_dependency_wait();
     const int n = __ldg(a.n_nodes + b), P = __ldg(a.n_past + b);
     // Uniform over the cluster: every CTA leaves before any cluster barrier.
     if (P < 0 || P + n > a.cap || n < 1 || n > N) {
@@ -167,107 +252,91 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
     }
     const int rows_valid = G * n, row0 = rt * RT;
     if (row0 >= rows_valid) return;
+    if (!block_tree_topology(a.parent + (size_t)b * N, n, N, par_s, depth_s, amask_s,
+                             (rank == 0 && rt == 0 && kvh == 0) ? a.status : nullptr))
+        return;  // uniform over the cluster: the parent array is shared
 
     const size_t plane_row0 = ((size_t)b * a.Hkv + kvh) * a.cap;
     uint8_t* kq = reinterpret_cast<uint8_t*>(a.kq);
     uint8_t* vq = reinterpret_cast<uint8_t*>(a.vq);
 
-    // tiles: cache keys [lo, P) then the tree slots [P, P + n), 32 keys each
+    // tiles: visible cache keys [lo, P) in 32-key tiles starting at a
+    // multiple of 32, then the tree slots [P, P + n); the whole list is split
+    // evenly over the cluster, so the tree tiles go to the last ranks
     const int lo = (W > 0) ? max(0, P - W + 1) : 0;
-    const int n_cache_tiles = (P - lo + kTK - 1) / kTK;
-    const int n_tiles = n_cache_tiles + (n + kTK - 1) / kTK;
-    auto tile_start = [&](int t) { return t < n_cache_tiles ? lo + t * kTK : P + (t - n_cache_tiles) * kTK; };
-    auto tile_count = [&](int t) {
-        return t < n_cache_tiles ? min(kTK, P - (lo + t * kTK)) : min(kTK, n - (t - n_cache_tiles) * kTK);
-    };
-    auto issue_tile = [&](int t, int buf) {
-        const int start = tile_start(t), count = tile_count(t);
-        uint8_t* base = raw_s + buf * S::kRaw;
-        constexpr int CPR = KB / 16;
-        for (int idx = tid; idx < count * CPR; idx += kThreads) {
-            const int c = idx / CPR, ch = idx % CPR;
-            const size_t g = (plane_row0 + start + c) * KB + ch * 16;
-            cp_async16(base + c * RSK + ch * 16, kq + g);
-            cp_async16(base + S::kRawCodes + c * RSK + ch * 16, vq + g);
-        }
-        uint8_t* ksd = base + 2 * S::kRawCodes;
-        uint8_t* vsd = ksd + S::kRawScales;
-        for (int c = tid; c < count; c += kThreads) {
-            const size_t g = (plane_row0 + start + c) * NB;
-            if constexpr (NB * 2 == 16) {
-                cp_async16(ksd + c * 16, a.ks + g);
-                cp_async16(vsd + c * 16, a.vs + g);
-            } else {
-                asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(smem_u32(ksd + c * 8)), "l"(a.ks + g) : "memory");
-                asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(smem_u32(vsd + c * 8)), "l"(a.vs + g) : "memory");
-            }
-        }
-        cp_async_commit();
+    const int c0 = (lo / kTK) * kTK;
+    const int n_cache_tiles = (P > lo) ? (P - c0 + kTK - 1) / kTK : 0;
+    const int n_all = n_cache_tiles + (n + kTK - 1) / kTK;
+    const int g0 = (int)((long)n_all * rank / CS), T = (int)((long)n_all * (rank + 1) / CS) - g0;
+    auto tile = [&](int u) {
+        const int g = g0 + u;
+        TileInfo ti;
+        ti.tree = g >= n_cache_tiles;
+        ti.start = ti.tree ? P + (g - n_cache_tiles) * kTK : c0 + g * kTK;
+        ti.count = ti.tree ? min(kTK, P + n - ti.start) : min(kTK, P - ti.start);
+        return ti;
     };
 
-    // ---- set-up: TMEM, barriers, first tile, tree quantisation, topology
-    if (warp == 0) tc::alloc(tmem_slot, S::kTmemCols);
     if (tid == 0) {
-        mbar_init(bar_s, 1);
-        mbar_init(bar_o, 1);
+        for (int i = 0; i < kNumBars; ++i) {
+            const bool by_stagers = (i >= kKFree0 && i <= kVFree1) || i == kKReady0 || i == kKReady1 || i == kVReady;
+            const int count = i <= kRawV1 ? 32 : by_stagers ? kStageThreads : (i == kPReady ? kSoftWarps * 32 : 1);
+            mbar_init(bars + i, count);
+        }
         fence_mbar_init();
         *fail_s = 0;
     }
-    int t_cur = rank;
-    if (t_cur < n_cache_tiles) issue_tile(t_cur, 0);
-    {
-        const int mine = (n > rank) ? (n - rank + CS - 1) / CS : 0;
-        for (int item = tid; item < mine * 2 * NB; item += kThreads) {
-            const int j = item / (2 * NB), which = (item / NB) % 2, blk = item % NB;
-            const int row = rank + CS * j;
-            const uint16_t* src = (which ? a.v_new : a.k_new) + (((size_t)b * N + row) * a.Hkv + kvh) * D + blk * 32;
-            const size_t slot = plane_row0 + P + row;
-            quantize_block<TYPE>(src, (which ? vq : kq) + slot * KB + blk * (KB / NB),
-                                 (which ? a.vs : a.ks) + slot * NB + blk);
-        }
-    }
-    const bool topo_ok = block_tree_topology(a.parent + (size_t)b * N, n, N, par_s, depth_s, amask_s,
-                                             (rank == 0 && rt == 0 && kvh == 0) ? a.status : nullptr);
-    if (!topo_ok) {  // uniform over the cluster: the parent array is shared
-        cp_async_wait<0>();
-        tc::fence_before_sync();
-        __syncthreads();
-        if (warp == 0) tc::dealloc(*tmem_slot, S::kTmemCols);
-        return;
-    }
-    __threadfence();
-    cluster_sync_all();  // tree slots written by the whole cluster are visible
-    if (t_cur >= n_cache_tiles) {
-        if (t_cur < n_tiles) issue_tile(t_cur, 0);
-        else cp_async_commit();
-    }
+    if (warp == kMmaWarp) tc::alloc(tmem_slot, L::kTmemCols);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
 
-    // ---- Q rows -> fp16, core-matrix layout (rows past the tile are zero)
+    const int st = tid - kStage0;  // stage thread index (valid for warps 4-7)
+    uint8_t* rawK = smem + L::off_rawK;
+    uint8_t* rawV = smem + L::off_rawV;
+    auto issue_tile_raw = [&](int u, bool k_plane, bool v_plane) {
+        const TileInfo ti = tile(u);
+        if (k_plane)
+            issue_raw<D, TYPE>(kq, a.ks, plane_row0, ti.start, ti.count, rawK + (u & 1) * L::kRaw,
+                               bars + kRawK0 + (u & 1), lane);
+        if (v_plane)
+            issue_raw<D, TYPE>(vq, a.vs, plane_row0, ti.start, ti.count, rawV + (u & 1) * L::kRaw,
+                               bars + kRawV0 + (u & 1), lane);
+    };
+    // the first two tiles' raw planes are requested at once
+    if (warp == kLoadWarp)
+        for (int u = 0; u < min(T, 2); ++u)
+            if (!tile(u).tree) issue_tile_raw(u, true, true);
+
+    if (early) grid_dependency_wait();
+
+    // ---- Q rows -> fp16, core-matrix layout (rows past the tile are zero);
+    //      every load of a thread is issued before the first is used
     {
-        // all of this thread's loads first (kRows * D / 8 / kThreads of them),
-        // then the conversions and stores
         constexpr int C8 = D / 8;
-        constexpr int PER = kRows * C8 / kThreads;
-        uint4 inv[PER];
+        constexpr int PER = (kRows * C8 + kThreads - 1) / kThreads;
+        uint4 inq[PER];
 #pragma unroll
         for (int j = 0; j < PER; ++j) {
             const int idx = tid + j * kThreads;
             const int r = (idx & 7) + (idx / (8 * C8)) * 8;
             const int d8 = (idx >> 3) % C8;
             const int rho = row0 + r;
-            inv[j] = make_uint4(0, 0, 0, 0);
-            if (r < RT && rho < rows_valid) {
+            inq[j] = make_uint4(0, 0, 0, 0);
+            if (idx < kRows * C8 && r < RT && rho < rows_valid) {
                 const int i = rho / G, gh = rho % G;
-                inv[j] = __ldg(reinterpret_cast<const uint4*>(
-                    a.q + (((size_t)b * N + i) * a.Hq + kvh * G + gh) * D + d8 * 8));
+                inq[j] = __ldg(reinterpret_cast<const uint4*>(a.q + (((size_t)b * N + i) * a.Hq + kvh * G + gh) * D +
+                                                             d8 * 8));
             }
         }
 #pragma unroll
         for (int j = 0; j < PER; ++j) {
             const int idx = tid + j * kThreads;
+            if (idx >= kRows * C8) break;
             const int r = (idx & 7) + (idx / (8 * C8)) * 8;
             const int d8 = (idx >> 3) % C8;
-            const uint32_t w[4] = {inv[j].x, inv[j].y, inv[j].z, inv[j].w};
+            const uint32_t w[4] = {inq[j].x, inq[j].y, inq[j].z, inq[j].w};
             uint32_t o[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e)
@@ -276,194 +345,298 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
             *reinterpret_cast<uint4*>(Q_s + tc::cm_offset(r, d8 * 8, D)) = make_uint4(o[0], o[1], o[2], o[3]);
         }
     }
-
-    // ---- per-row state: thread tid owns row tid % 128, key half tid / 128
-    const int srow = tid & (kRows - 1), half = tid >> 7;
-    int lb = INT_MAX, rdepth = 0;
-    uint64_t ramask = 0;
+    // ---- the tree's own keys and values: the CTA that attends to a tree
+    //      tile quantises that tile's rows into the cache itself (every row
+    //      tile's CTA writes the same bytes) and copies them back like a
+    //      cached tile once this block's writes are visible
     {
-        const int rho = row0 + srow;
-        if (srow < RT && rho < rows_valid) {
-            const int i = rho / G;
-            rdepth = depth_s[i];
-            ramask = amask_s[i];
-            lb = (W > 0) ? P + depth_s[i] - W + 1 : INT_MIN;
+        const int r_lo = max(0, g0 - n_cache_tiles) * kTK;
+        const int r_hi = min(n, (g0 + T - n_cache_tiles) * kTK);
+        const int nblk = (r_hi > r_lo) ? (r_hi - r_lo) * NB : 0;
+        for (int k = tid; k < 2 * nblk; k += kThreads) {
+            const bool vplane = k >= nblk;
+            const int kk = vplane ? k - nblk : k, row = r_lo + kk / NB, blk = kk % NB;
+            const uint16_t* src = (vplane ? a.v_new : a.k_new) + (((size_t)b * N + row) * a.Hkv + kvh) * D + blk * 32;
+            const size_t slot = plane_row0 + P + row;
+            quantize_block<TYPE>(src, (vplane ? vq : kq) + slot * L::KB + blk * (L::KB / NB),
+                                 (vplane ? a.vs : a.ks) + slot * NB + blk);
         }
+        __threadfence();
     }
-    const float sl2 = a.scale * kLog2e;
+    fence_proxy_async_smem();
+    __syncthreads();
+
+    const uint32_t tmem_O = tmem;  // columns [0, D); S buffers at D and D + 64
     float m_run = -INFINITY, l_run = 0.f;
 
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t tmem_O = tmem;          // columns [0, D)
-    const uint32_t tmem_S = tmem + D;      // columns [D, D + 64): Q.K_hi then Q.K_lo
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;  // warps w and w+4 share lanes
-
-    constexpr uint32_t idesc_qk = tc::idesc_f16(kRows, 2 * kTK, false);  // K_lo follows K_hi in smem
-    constexpr uint32_t idesc_pv = tc::idesc_f16(kRows, D, true);
-    uint32_t phase = 0;
-    bool o_valid = false;
-    int buf = 0;
-    for (; t_cur < n_tiles; t_cur += CS, buf ^= 1) {
-        const int t_next = t_cur + CS;
-        if (t_next < n_tiles) issue_tile(t_next, buf ^ 1);
-        else cp_async_commit();
-        cp_async_wait<1>();
-        __syncthreads();
-
-        const bool tree_tile = t_cur >= n_cache_tiles;
-        const int start = tile_start(t_cur), count = tile_count(t_cur);
-        const uint8_t* rb = raw_s + buf * S::kRaw;
-        const uint16_t* ksb = reinterpret_cast<const uint16_t*>(rb + 2 * S::kRawCodes);
-        const uint16_t* vsb = reinterpret_cast<const uint16_t*>(rb + 2 * S::kRawCodes + S::kRawScales);
-        stage_hilo<D, TYPE>(rb, ksb, count, Khi_s, Klo_s, tid);
-        stage_hilo<D, TYPE>(rb + S::kRawCodes, vsb, count, Vhi_s, Vlo_s, tid);
-        fence_proxy_async_smem();
-        __syncthreads();
-
-        // [S_hi | S_lo] = Q [K_hi ; K_lo]^T
-        if (tid == 0 && !*fail_s) {
-            tc::fence_after_sync();
-            const uint32_t qa = smem_u32(Q_s), kh = smem_u32(Khi_s);
-            constexpr uint32_t SBO = (D / 8) * 128;
-#pragma unroll 4
-            for (int ks = 0; ks < D / 16; ++ks)
-                tc::mma_f16(tmem_S, tc::smem_desc(qa + ks * 256, 128, SBO), tc::smem_desc(kh + ks * 256, 128, SBO),
-                            idesc_qk, ks > 0);
-            tc::commit(bar_s);
-        }
-
+    if (warp < kSoftWarps) {
+        // ================================================ softmax: thread = query row
+        const int srow = tid;
+        int lb = INT_MAX, rdepth = 0;
+        uint64_t ramask = 0;
         {
-            // warp-uniform: the tcgen05 loads below are .sync.aligned
-            const bool ok = __all_sync(0xffffffffu, *fail_s == 0 && wait_phase(bar_s, phase));
-            if (!ok && lane == 0) atomicOr(fail_s, 1);
-            tc::fence_after_sync();
-            constexpr int HK = kTK / 2;  // keys per thread
-            float s[HK];
-            if (ok) {
-                float sh[32], sl[32];
-                tc::ld32(tmem_S + lane_off, sh);
-                tc::ld32(tmem_S + lane_off + kTK, sl);
-#pragma unroll
-                for (int c = 0; c < HK; ++c) s[c] = half ? sh[HK + c] + sl[HK + c] : sh[c] + sl[c];
+            const int rho = row0 + srow;
+            if (srow < RT && rho < rows_valid) {
+                const int i = rho / G;
+                rdepth = depth_s[i];
+                ramask = amask_s[i];
+                lb = (W > 0) ? P + depth_s[i] - W + 1 : INT_MIN;
             }
-            float mt = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < HK; ++j) {
-                const int c = half * HK + j;
-                bool vis;
-                if (tree_tile) {
-                    const int l = start - P + c;
-                    vis = c < count && ((ramask >> l) & 1ull) && (W == 0 || depth_s[l] > rdepth - W);
-                } else {
-                    vis = c < count && start + c >= lb;
+        }
+        const float sl2 = a.scale * kLog2e;
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        unsigned char* Phi = smem + L::off_Phi;
+        unsigned char* Plo = smem + L::off_Plo;
+        // a warp whose rows are all padding only keeps the barrier phases
+        // in step (its P rows and O rows are never read back)
+        const bool warp_active = 32 * warp < min(RT, rows_valid - row0);
+        for (int t = 0; t < T && !warp_active; ++t) {
+            if (t > 0) {
+                const bool ok = __all_sync(0xffffffffu, wait_phase(bars + kODone, (t - 1) & 1));
+                if (!ok) {
+                    if (lane == 0) atomicOr(fail_s, 1);
+                    break;
                 }
-                s[j] = (vis && ok) ? s[j] * sl2 : -INFINITY;
-                mt = fmaxf(mt, s[j]);
             }
-            xch_s[half * kRows + srow] = mt;
-            __syncthreads();
-            mt = fmaxf(mt, xch_s[(half ^ 1) * kRows + srow]);
+            mbar_arrive(bars + kPReady);
+        }
+        for (int t = 0; t < T && warp_active; ++t) {
+            const TileInfo ti = tile(t);
+            bool ok = wait_phase(bars + kSFull0 + (t & 1), (t >> 1) & 1);
+            ok = __all_sync(0xffffffffu, ok && !failed());
+            if (!ok) {
+                if (lane == 0) atomicOr(fail_s, 1);
+                break;
+            }
+            tc::fence_after_sync();
+            float s[kTK];
+            {
+                float sh[32], sl[32];
+                const uint32_t ts = tmem + D + (uint32_t)((t & 1) * 2 * kTK);
+                tc::ld32(ts + lane_off, sh);
+                tc::ld32(ts + lane_off + kTK, sl);
+#pragma unroll
+                for (int c = 0; c < kTK; ++c) s[c] = sh[c] + sl[c];
+            }
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            if (ti.tree) {
+#pragma unroll
+                for (int c = 0; c < kTK; ++c) {
+                    const int l = ti.start - P + c;
+                    const bool vis = c < ti.count && ((ramask >> l) & 1ull) && (W == 0 || depth_s[l] > rdepth - W);
+                    s[c] = vis ? s[c] * sl2 : -INFINITY;
+                    mx[c & 3] = fmaxf(mx[c & 3], s[c]);
+                }
+            } else {
+                // visible: first <= c < lim (lb is INT_MIN without a window, INT_MAX for padding rows)
+                const int lim = min(ti.count, kTK), first = (lb == INT_MIN) ? 0 : lb - ti.start;
+#pragma unroll
+                for (int c = 0; c < kTK; ++c) {
+                    s[c] = (c < lim && c >= first) ? s[c] * sl2 : -INFINITY;
+                    mx[c & 3] = fmaxf(mx[c & 3], s[c]);
+                }
+            }
+            const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
             float alpha = 1.f;
             bool rescale = false;
             if (mt > m_run + 8.f) {
                 alpha = (m_run == -INFINITY) ? 0.f : exp2f(m_run - mt);
                 m_run = mt;
                 l_run *= alpha;
-                rescale = o_valid;
+                rescale = t > 0;
+            }
+            // P and O are free once the previous tile's PV has completed
+            if (t > 0) {
+                bool ok2 = wait_phase(bars + kODone, (t - 1) & 1);
+                ok2 = __all_sync(0xffffffffu, ok2);
+                if (!ok2) {
+                    if (lane == 0) atomicOr(fail_s, 1);
+                    break;
+                }
+                tc::fence_after_sync();
+            }
+            if (__any_sync(0xffffffffu, rescale)) {
+                const float al = rescale ? alpha : 1.f;
+#pragma unroll 1
+                for (int c0o = 0; c0o < D; c0o += 32) {
+                    float o[32];
+                    tc::ld32(tmem_O + lane_off + c0o, o);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] *= al;
+                    tc::st32(tmem_O + lane_off + c0o, o);
+                }
             }
             const float base = (m_run == -INFINITY) ? 0.f : m_run;
-            uint32_t ph[HK / 2], pl[HK / 2];
+            uint32_t ph[kTK / 2], pl[kTK / 2];
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int j = 0; j < HK; j += 2) {
+            for (int j = 0; j < kTK; j += 2) {
                 const float p0 = exp2f(s[j] - base), p1 = exp2f(s[j + 1] - base);
-                l_run += p0 + p1;
+                ls[(j >> 1) & 3] += p0 + p1;
                 const __half2 h2 = __floats2half2_rn(p0, p1);
                 const float2 hf = __half22float2(h2);
                 const __half2 l2 = __floats2half2_rn(p0 - hf.x, p1 - hf.y);
                 ph[j / 2] = *reinterpret_cast<const uint32_t*>(&h2);
                 pl[j / 2] = *reinterpret_cast<const uint32_t*>(&l2);
             }
+            l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
 #pragma unroll
-            for (int k8 = 0; k8 < HK / 8; ++k8) {
-                const uint32_t off = tc::cm_offset(srow, half * HK + k8 * 8, kTK);
-                *reinterpret_cast<uint4*>(Phi_s + off) = make_uint4(ph[4 * k8], ph[4 * k8 + 1], ph[4 * k8 + 2], ph[4 * k8 + 3]);
-                *reinterpret_cast<uint4*>(Plo_s + off) = make_uint4(pl[4 * k8], pl[4 * k8 + 1], pl[4 * k8 + 2], pl[4 * k8 + 3]);
-            }
-            // O *= alpha for this row (tensor memory) when its max moved; the
-            // two threads of a row take half of the columns each
-            if (__any_sync(0xffffffffu, rescale) && ok) {
-                const float al = rescale ? alpha : 1.f;
-#pragma unroll 1
-                for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
-                    float o[32];
-                    tc::ld32(tmem_O + lane_off + c0, o);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] *= al;
-                    tc::st32(tmem_O + lane_off + c0, o);
-                }
+            for (int k8 = 0; k8 < kTK / 8; ++k8) {
+                const uint32_t off = tc::cm_offset(srow, k8 * 8, kTK);
+                *reinterpret_cast<uint4*>(Phi + off) = make_uint4(ph[4 * k8], ph[4 * k8 + 1], ph[4 * k8 + 2], ph[4 * k8 + 3]);
+                *reinterpret_cast<uint4*>(Plo + off) = make_uint4(pl[4 * k8], pl[4 * k8 + 1], pl[4 * k8 + 2], pl[4 * k8 + 3]);
             }
             fence_proxy_async_smem();
+            tc::fence_before_sync();
+            mbar_arrive(bars + kPReady);
         }
-        tc::fence_before_sync();
-        __syncthreads();
-
-        // O += P_hi V_hi + P_hi V_lo + P_lo V_hi
-        if (tid == 0 && !*fail_s) {
+        // the last PV
+        if (__all_sync(0xffffffffu, T > 0 && !failed())) {
+            bool ok = __all_sync(0xffffffffu, wait_phase(bars + kODone, (T - 1) & 1));
+            if (!ok && lane == 0) atomicOr(fail_s, 1);
             tc::fence_after_sync();
-            const uint32_t ph = smem_u32(Phi_s), pl = smem_u32(Plo_s), vh = smem_u32(Vhi_s), vl = smem_u32(Vlo_s);
-            constexpr uint32_t P_SBO = (kTK / 8) * 128, V_LBO = (D / 8) * 128;
+        }
+    } else if (warp < kMmaWarp) {
+        // ================================================ stage warps
+        for (int t = 0; t <= T; ++t) {
+            bool ok = true;
+            if (t < T) {
+                const TileInfo ti = tile(t);
+                uint8_t* rk = rawK + (t & 1) * L::kRaw;
+                ok = ok && wait_phase(bars + kRawK0 + (t & 1), (t >> 1) & 1);
+                const int shift = scale_shift<D, TYPE>(a.ks, plane_row0, ti.start);
+                if (t >= 2) ok = ok && wait_phase(bars + kSFull0 + (t & 1), ((t - 2) >> 1) & 1);
+                if (ok)
+                    stage_hilo<D, TYPE>(rk, reinterpret_cast<const uint16_t*>(rk + L::kRawCodes + shift), ti.count,
+                                        smem + L::off_K + (t & 1) * L::kK,
+                                        smem + L::off_K + (t & 1) * L::kK + L::kK / 2, st);
+                mbar_arrive(bars + kKFree0 + (t & 1));  // raw K buffer of this parity released
+                fence_proxy_async_smem();
+                mbar_arrive(bars + kKReady0 + (t & 1));
+            }
+            if (t >= 1 && ok) {
+                const int u = t - 1;
+                const TileInfo tu = tile(u);
+                uint8_t* rv = rawV + (u & 1) * L::kRaw;
+                ok = ok && wait_phase(bars + kRawV0 + (u & 1), (u >> 1) & 1);
+                const int shift = scale_shift<D, TYPE>(a.vs, plane_row0, tu.start);
+                if (u >= 1) ok = ok && wait_phase(bars + kODone, (u - 1) & 1);
+                if (ok)
+                    stage_hilo<D, TYPE>(rv, reinterpret_cast<const uint16_t*>(rv + L::kRawCodes + shift), tu.count,
+                                        smem + L::off_Vhi, smem + L::off_Vlo, st);
+                mbar_arrive(bars + kVFree0 + (u & 1));  // raw V buffer of this parity released
+                fence_proxy_async_smem();
+                mbar_arrive(bars + kVReady);
+            }
+            // a failure is seen by every stage thread at the same iteration
+            const bool bad = named_barrier_or(kStageBarrier, kStageThreads, !ok || failed());
+            if (bad) {
+                if (st == 0) atomicOr(fail_s, 1);
+                break;
+            }
+        }
+    } else if (warp == kLoadWarp) {
+        // ================================================ raw tile copies: tile u
+        // goes into buffer u & 1 once the stage warps have released tile u - 2
+        bool ok = true;
+        for (int u = 0; u < T && ok; ++u) {
+            if (u < 2 && !tile(u).tree) continue;  // requested before the loop
+            if (u >= 2) ok = wait_phase(bars + kKFree0 + (u & 1), ((u - 2) >> 1) & 1);
+            if (ok) issue_tile_raw(u, true, false);
+            if (u >= 2) ok = ok && wait_phase(bars + kVFree0 + (u & 1), ((u - 2) >> 1) & 1);
+            if (ok) issue_tile_raw(u, false, true);
+        }
+        if (!__all_sync(0xffffffffu, ok) && lane == 0) atomicOr(fail_s, 1);
+        cp_async_wait<0>();  // this lane's copies have landed before the CTA moves on
+    } else if (lane == 0) {
+        // ================================================ MMA issue (one thread)
+        const uint32_t qa = smem_u32(Q_s);
+        constexpr uint32_t SBO = (D / 8) * 128;
+        constexpr uint32_t idesc_qk = tc::idesc_f16(kRows, 2 * kTK, false);  // K_lo follows K_hi
+        constexpr uint32_t idesc_pv = tc::idesc_f16(kRows, D, true);
+        constexpr uint32_t P_SBO = (kTK / 8) * 128, V_LBO = (D / 8) * 128;
+        auto issue_qk = [&](int t) {
+            const uint32_t kb = smem_u32(smem + L::off_K + (t & 1) * L::kK);
+            const uint32_t ts = tmem + D + (uint32_t)((t & 1) * 2 * kTK);
+#pragma unroll 4
+            for (int ks = 0; ks < D / 16; ++ks)
+                tc::mma_f16(ts, tc::smem_desc(qa + ks * 256, 128, SBO), tc::smem_desc(kb + ks * 256, 128, SBO),
+                            idesc_qk, ks > 0);
+            tc::commit(bars + kSFull0 + (t & 1));
+        };
+        bool ok = true;
+        if (T > 0) {
+            ok = wait_phase(bars + kKReady0, 0);
+            if (ok) {
+                tc::fence_after_sync();
+                issue_qk(0);
+            }
+        }
+        for (int t = 0; t < T && ok; ++t) {
+            if (t + 1 < T) {
+                ok = wait_phase(bars + kKReady0 + ((t + 1) & 1), ((t + 1) >> 1) & 1);
+                if (!ok) break;
+                tc::fence_after_sync();
+                issue_qk(t + 1);
+            }
+            ok = wait_phase(bars + kPReady, t & 1) && wait_phase(bars + kVReady, t & 1);
+            if (!ok) break;
+            tc::fence_after_sync();
+            const uint32_t ph = smem_u32(smem + L::off_Phi), pl = smem_u32(smem + L::off_Plo);
+            const uint32_t vh = smem_u32(smem + L::off_Vhi), vl = smem_u32(smem + L::off_Vlo);
 #pragma unroll
             for (int ks = 0; ks < kTK / 16; ++ks) {
                 const uint64_t ah = tc::smem_desc(ph + ks * 256, 128, P_SBO);
                 const uint64_t al = tc::smem_desc(pl + ks * 256, 128, P_SBO);
                 const uint64_t bh = tc::smem_desc(vh + ks * 2 * V_LBO, V_LBO, 128);
                 const uint64_t bl = tc::smem_desc(vl + ks * 2 * V_LBO, V_LBO, 128);
-                tc::mma_f16(tmem_O, ah, bh, idesc_pv, o_valid || ks > 0);
+                tc::mma_f16(tmem_O, ah, bh, idesc_pv, t > 0 || ks > 0);
                 tc::mma_f16(tmem_O, ah, bl, idesc_pv, true);
                 tc::mma_f16(tmem_O, al, bh, idesc_pv, true);
             }
-            tc::commit(bar_o);
+            tc::commit(bars + kODone);
         }
-        // every thread waits: the tile buffers and O are reused next
-        if (!*fail_s && !wait_phase(bar_o, phase)) atomicOr(fail_s, 1);
-        tc::fence_after_sync();
-        o_valid = true;
-        phase ^= 1;
+        if (!ok) atomicOr(fail_s, 1);
+        // every MMA issued above has completed before TMEM or smem is reused
+        tc::commit(bars + kMmaFin);
+        wait_phase(bars + kMmaFin, 0);
     }
-    cp_async_wait<0>();
     __syncthreads();
-    if (*fail_s && tid == 0) raise_status(a.status, DFLV_DEV_TIMEOUT);
+    const bool any_fail = failed();  // settled: every role has left its loop
+    if (any_fail && tid == 0) raise_status(a.status, DFLV_DEV_TIMEOUT);
+    // the next kernel may be scheduled while the partials are merged
+    grid_launch_dependents();
 
     // ---- partial results -> shared memory (reusing the tile region)
-    float* Om = reinterpret_cast<float*>(smem + S::off_Om);
-    float* Mm = reinterpret_cast<float*>(smem + S::off_Mm);
-    float* Lm = reinterpret_cast<float*>(smem + S::off_Lm);
-    xch_s[half * kRows + srow] = l_run;
-    __syncthreads();
-    {
+    float* Om = reinterpret_cast<float*>(smem + L::off_Om);
+    float* Mm = reinterpret_cast<float*>(smem + L::off_Mm);
+    float* Lm = reinterpret_cast<float*>(smem + L::off_Lm);
+    if (warp < kSoftWarps) {
+        const int srow = tid;
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const bool have_o = T > 0 && !any_fail;
 #pragma unroll 1
-        for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
+        for (int c0o = 0; c0o < D; c0o += 32) {
             float o[32];
-            if (o_valid && !*fail_s) tc::ld32(tmem_O + lane_off + c0, o);
-            else {
+            if (have_o) {
+                tc::ld32(tmem_O + lane_off + c0o, o);
+            } else {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) o[e] = 0.f;
             }
 #pragma unroll
             for (int e = 0; e < 32; e += 4)
-                *reinterpret_cast<float4*>(Om + srow * OS + c0 + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+                *reinterpret_cast<float4*>(Om + srow * OS + c0o + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
         }
-        if (half == 0) {
-            Mm[srow] = m_run;
-            Lm[srow] = l_run + xch_s[kRows + srow];
-        }
+        Mm[srow] = have_o ? m_run : -INFINITY;
+        Lm[srow] = have_o ? l_run : 0.f;
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::dealloc(tmem, S::kTmemCols);
+    if (warp == kMmaWarp) {
+        tc::fence_after_sync();
+        tc::dealloc(tmem, L::kTmemCols);
+    }
     cluster_sync_all();
 
     // ---- merge: rank r finalises rows r, r + CS, ... (one warp per row); a
@@ -474,8 +647,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
     for (int r = rank + CS * warp; r < RT; r += CS * nwarps) {
         const int rho = row0 + r;
         if (rho >= rows_valid) continue;
+        // every peer's running max and sum, requested together (CS <= 16)
+        float mq16[16], lq16[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            mq16[q] = q < CS ? ld_dsmem_f32(map_to_rank(mm_base + r * 4, q)) : -INFINITY;
+            lq16[q] = q < CS ? ld_dsmem_f32(map_to_rank(lm_base + r * 4, q)) : 0.f;
+        }
         float M = -INFINITY;
-        for (int q = 0; q < CS; ++q) M = fmaxf(M, ld_dsmem_f32(map_to_rank(mm_base + r * 4, q)));
+#pragma unroll
+        for (int q = 0; q < 16; ++q) M = fmaxf(M, mq16[q]);
         const float bse = (M == -INFINITY) ? 0.f : M;
         float Lt = 0.f, acc[PL];
 #pragma unroll
@@ -485,8 +666,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 const bool on = q0 + q < CS;
-                mq[q] = on ? ld_dsmem_f32(map_to_rank(mm_base + r * 4, q0 + q)) : -INFINITY;
-                lq[q] = on ? ld_dsmem_f32(map_to_rank(lm_base + r * 4, q0 + q)) : 0.f;
+                mq[q] = q0 == 0 ? mq16[q] : mq16[8 + q];
+                lq[q] = q0 == 0 ? lq16[q] : lq16[8 + q];
 #pragma unroll
                 for (int e = 0; e < PL; e += 4) {
                     float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -545,24 +726,24 @@ int active_clusters(Kernel kern, size_t smem, int cs) {
 
 template <int D, int TYPE>
 cudaError_t launch_tc(const AttnVerifyArgs& a, cudaStream_t stream) {
-    using S = TcSmem<D, TYPE>;
+    using L = TcLayout<D, TYPE>;
     auto kern = attn_tc_kernel<D, TYPE>;
-    cudaError_t e = ensure_smem(kern, S::total);
+    cudaError_t e = ensure_smem(kern, L::total);
     if (e != cudaSuccess) return e;
     const int rows = (a.Hq / a.Hkv) * a.N_max;
     const int n_rt = (rows + kRows - 1) / kRows;
     const int RT = (rows + n_rt - 1) / n_rt;
     const long range = (a.window > 0) ? (long)a.window - 1 : (long)a.cap;
-    const long tiles = (range + kTK - 1) / kTK + 2;
+    const long tiles = (range + kTK - 1) / kTK + 3;
     const long clusters = (long)n_rt * a.Hkv * a.B;
     const int sms = sm_count_cached();
     // the largest cluster (<= 16) that still lets every cluster be resident
     // at once and that the key range can feed
     int cs = 1;
     while (cs < 16 && clusters * cs * 2 <= sms && cs * 2 <= tiles &&
-           active_clusters(kern, S::total, cs * 2) >= clusters)
+           active_clusters(kern, L::total, cs * 2) >= clusters)
         cs *= 2;
-    return launch_pdl(kern, dim3(cs, n_rt * a.Hkv, a.B), dim3(kThreads), S::total, stream, cs, a, RT, cs);
+    return launch_pdl(kern, dim3(cs, n_rt * a.Hkv, a.B), dim3(kThreads), L::total, stream, cs, a, RT, cs);
 }
 
 }  // namespace

@@ -157,3 +157,45 @@ def test_attn_errors_set_status(dflv):
     parent[0, 3] = 4
     out, planes = gpu_attn(dflv, parent, n_nodes, n_past, inp, cache, 0, synth.KV_Q8_0, 2, 1, 64,
                            expect_status=dflv.DFLV_DEV_TOPOLOGY)
+
+
+def test_attn_layers_back_to_back_with_early_prefetch(dflv, orc):
+    # three attention layers launched back to back on one stream, every
+    # layer after the first reading its tree and cache prefix before the
+    # dependency wait; q, k_new and v_new of each layer are written by an
+    # elementwise kernel queued just before it, so a kernel that read them
+    # before its wait could still see the zeros they held
+    rng = np.random.default_rng(1250)
+    Hq, Hkv, D, P, W = 24, 4, 256, 3000, 2048
+    par, _ = synth.ddtree(rng, 22, 151936)
+    parent, n_nodes = synth.batch_trees([par], 22)
+    n_past = np.array([P], np.int32)
+    dp, dn, dP = dev(parent), dev(n_nodes), dev(n_past)
+    st = zeros_status()
+    layers = []
+    for li in range(3):
+        inp = synth.attn_inputs(rng, 1, 22, Hq, Hkv, D)
+        cache = synth.kv_cache(rng, 1, Hkv, P + 64, D, synth.KV_Q8_0)
+        src = {k: dev(v) for k, v in inp.items()}
+        dst = {k: torch.zeros_like(v) for k, v in src.items()}
+        dc = {k: dev(v) for k, v in cache.items()}
+        out = torch.full((1, 22, Hq, D), float("nan"), device="cuda")
+        layers.append((inp, cache, src, dst, dc, out))
+    torch.cuda.synchronize()
+    for li, (inp, cache, src, dst, dc, out) in enumerate(layers):
+        for k in ("q", "k_new", "v_new"):
+            torch.mul(src[k], 1, out=dst[k])
+        flags = 0 if li == 0 else dflv.DFLV_FLAG_EARLY_PREFETCH
+        desc = dflv.attn_desc(1, 22, Hq, Hkv, D, P + 64, W, synth.KV_Q8_0, 1.0 / np.sqrt(D), flags)
+        dflv.check(dflv.dflv_tree_attn_verify(desc, dp, dn, dP, dst["q"], dst["k_new"], dst["v_new"],
+                                              dflv.kv_layer(dc["kq"], dc["vq"], dc["ks"], dc["vs"]), out, st))
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for inp, cache, src, dst, dc, out in layers:
+        ref_cache = synth.copy_cache(cache)
+        ref = orc.tree_attn_verify(parent, n_nodes, n_past, inp["q"], inp["k_new"], inp["v_new"], ref_cache, W,
+                                   synth.KV_Q8_0)
+        assert_close(host(out)[0, :22], ref[0, :22], what="o")
+        for key in ("kq", "vq", "ks", "vs"):
+            got = host(dc[key], _plane_np_dtype(key, synth.KV_Q8_0))
+            assert np.array_equal(got, ref_cache[key]), key
