@@ -182,9 +182,10 @@ def hbm_peak():
 
 
 def kernel_source_hash(kind):
-    files = {"gdn": "gdn_verify.cu", "attn": "attn_verify.cu", "accept": "accept.cu", "commit": "commit.cu"}
+    files = {"gdn": ["gdn_verify.cu"], "attn": ["attn_verify.cu", "attn_verify_tc.cu", "attn_common.cuh", "tcgen05.cuh"],
+             "accept": ["accept.cu"], "commit": ["commit.cu"]}
     h = hashlib.sha256()
-    for f in (files[kind], "common.cuh", "tree.cuh"):
+    for f in files[kind] + ["common.cuh", "tree.cuh"]:
         with open(os.path.join(ROOT, "speculative_decoding_tree_layer_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -293,36 +294,25 @@ class GpuStep:
                          kv=dflv.kv_layer(dc["kq"], dc["vq"], dc["ks"], dc["vs"]))
                 self.caches.append(L["kv"])
             self.layers.append(L)
-        self.launches_per_step = N_GDN * 1 + N_ATTN * 2 + 2 + 2
+        self.launches_per_step = N_GDN + N_ATTN + 2 + 2  # accept and commit: two kernels each
 
-    # one launch sequence; events (optional) bracket each kernel group
-    def step(self, ev=None):
+    # one pass of the hot path: every layer's verify, acceptance, commit
+    def step(self):
         dflv, chk = self.dflv, self.dflv.check
         for li, L in enumerate(self.layers):
-            if ev is not None:
-                ev[li][0].record()
             if L["kind"] == "gdn":
-                chk(dflv.dflv_tree_gdn_verify(self.gdn_desc if li == 0 else self.gdn_desc_next, self.parent, self.n_nodes, L["q"], L["k"], L["v"],
-                                              L["beta"], L["log_alpha"], L["state"], L["out"], L["fac"],
-                                              self.status), "gdn verify")
+                chk(dflv.dflv_tree_gdn_verify(self.gdn_desc if li == 0 else self.gdn_desc_next, self.parent,
+                                              self.n_nodes, L["q"], L["k"], L["v"], L["beta"], L["log_alpha"],
+                                              L["state"], L["out"], L["fac"], self.status), "gdn verify")
             else:
                 chk(dflv.dflv_tree_attn_verify(self.attn_desc_next, self.parent, self.n_nodes, self.n_past, L["q"],
                                                L["k_new"], L["v_new"], L["kv"], L["out"], self.status),
                     "attn verify")
-            if ev is not None:
-                ev[li][1].record()
-        if ev is not None:
-            ev[N_LAYERS][0].record()
         chk(dflv.dflv_accept_greedy(1, BUDGET, VOCAB, self.logits, self.tokens, self.parent, self.n_nodes,
                                     self.path, self.path_len, self.next_token, self.best, self.status), "accept")
-        if ev is not None:
-            ev[N_LAYERS][1].record()
-            ev[N_LAYERS + 1][0].record()
         chk(dflv.dflv_commit_rollback(self.gdn_desc, len(self.states), self.states, self.factors, self.attn_desc,
                                       len(self.caches), self.caches, self.path, self.path_len, self.n_past,
                                       self.status), "commit")
-        if ev is not None:
-            ev[N_LAYERS + 1][1].record()
 
     def reset(self):
         """Committed state back to its initial value (between passes)."""
@@ -331,12 +321,52 @@ class GpuStep:
         self.n_past.fill_(CTX)
 
 
-def make_events(torch, n):
-    try:
-        return [(torch.cuda.Event(enable_timing=True, external=True),
-                 torch.cuda.Event(enable_timing=True, external=True)) for _ in range(n)]
-    except TypeError:
-        return None
+def kernel_chain_ms(S, torch, stream, steps, warmup):
+    """Average launch duration of each kernel kind inside its own chain."""
+    dflv, chk = S.dflv, S.dflv.check
+
+    def gdn_chain():
+        for li, L in enumerate(S.layers):
+            if L["kind"] == "gdn":
+                chk(dflv.dflv_tree_gdn_verify(S.gdn_desc if li == 0 else S.gdn_desc_next, S.parent, S.n_nodes,
+                                              L["q"], L["k"], L["v"], L["beta"], L["log_alpha"], L["state"],
+                                              L["out"], L["fac"], S.status), "gdn verify")
+
+    def attn_chain():
+        for L in S.layers:
+            if L["kind"] == "attn":
+                chk(dflv.dflv_tree_attn_verify(S.attn_desc_next, S.parent, S.n_nodes, S.n_past, L["q"],
+                                               L["k_new"], L["v_new"], L["kv"], L["out"], S.status), "attn verify")
+
+    def accept():
+        chk(dflv.dflv_accept_greedy(1, BUDGET, VOCAB, S.logits, S.tokens, S.parent, S.n_nodes, S.path,
+                                    S.path_len, S.next_token, S.best, S.status), "accept")
+
+    def commit():
+        chk(dflv.dflv_commit_rollback(S.gdn_desc, len(S.states), S.states, S.factors, S.attn_desc,
+                                      len(S.caches), S.caches, S.path, S.path_len, S.n_past, S.status), "commit")
+
+    out = {}
+    for name, fn, n in (("gdn", gdn_chain, N_GDN), ("attn", attn_chain, N_ATTN), ("accept", accept, 1),
+                        ("commit", commit, 1)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        S.reset()
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record()
+            for _ in range(steps):
+                g.replay()
+            e1.record()
+        torch.cuda.synchronize()
+        out[name] = e0.elapsed_time(e1) / (steps * n)
+        S.reset()
+        torch.cuda.synchronize()
+    return out
 
 
 def run_gpu(args, rank, world):
@@ -389,31 +419,11 @@ def run_gpu(args, rank, world):
     assert status == 0, f"device status {status}"
     ms_max = reduce_max(world, ms)
 
-    # ---- per-kernel durations: the same step with event nodes around each
-    #      kernel group, replayed on the same stream
-    S.reset()
-    torch.cuda.synchronize()
-    ev = make_events(torch, N_LAYERS + 2)
-    per = None
-    if ev is not None:
-        g2 = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g2, stream=stream):
-            S.step(ev)
-        torch.cuda.synchronize()
-        S.reset()
-        for _ in range(args.warmup):
-            g2.replay()
-        torch.cuda.synchronize()
-        acc = np.zeros(N_LAYERS + 2)
-        for _ in range(args.steps):
-            g2.replay()
-            torch.cuda.synchronize()
-            acc += [a.elapsed_time(b) for a, b in ev]
-        acc /= args.steps
-        per = dict(gdn=float(np.mean([acc[i] for i in range(N_LAYERS) if not is_attn(i)])),
-                   attn=float(np.mean([acc[i] for i in range(N_LAYERS) if is_attn(i)])),
-                   accept=float(acc[N_LAYERS]), commit=float(acc[N_LAYERS + 1]))
-
+    # ---- per-kernel durations: every kernel kind of the step launched back
+    #      to back as in the step (all its layers, same buffers, same launch
+    #      overlap), one CUDA graph per kind, timed with events on the
+    #      launching stream; per launch = chain time / launches
+    per = kernel_chain_ms(S, torch, stream, args.steps, args.warmup)
     # ---- end to end: pinned host inputs -> device, step, result -> host, every step
     S.reset()
     torch.cuda.synchronize()
@@ -609,6 +619,8 @@ def main():
                      "peak_source": f"{peak_kind} hbm_gbs",
                      "algorithmic_bytes_per_launch": ab[dom],
                      "avg_launch_ms": dur_ms,
+                     "launch_timing": "chain of all launches of this kernel in the step, back to back, "
+                                      "CUDA events on the launching stream",
                      "traffic": profiled_traffic(dom)},
         "kernels_ms_per_launch": per,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},

@@ -181,9 +181,11 @@ typedef struct {
  *   n_past [B] int32 (device): P, the committed tokens of each sequence
  *   q      [B][N_max][Hq][D] bf16; k_new, v_new [B][N_max][Hkv][D] bf16
  *   cache  host pointer to the layer's planes: slots [P, P + n) are
- *          overwritten with the tree's quantised keys/values (quantiser:
- *          d = fp16(amax / 127) resp. fp16(amax / 7) of each 32-block,
- *          codes = round-half-away(x / d) clamped; slots < P are only read)
+ *          overwritten with the tree's quantised keys/values (quantiser, per
+ *          32-block: d = amax / 127 resp. amax / 7 in fp32, stored as fp16
+ *          (round to nearest); codes = round-half-away(x * (1/d)) with the
+ *          fp32 reciprocal of the fp32 d, clamped to [-127, 127] resp.
+ *          [-8, 7] (+8); slots < P are only read)
  *   out    [B][N_max][Hq][D] f32
  *   workspace reserved: dflv_attn_workspace_size() returns 0; may be NULL
  * Every node attends to the cached positions j < P inside its window and to
