@@ -56,6 +56,7 @@ constexpr int kThreads = (kLoadWarp + 1) * 32;
 constexpr int kStage0 = kSoftWarps * 32;             // first stage thread
 constexpr int kStageThreads = kStageWarps * 32;
 constexpr int kStageBarrier = 2;                     // named barrier of the stage warps
+constexpr int kTreeCost = 3;                         // a tree tile (quantise + attend) in cache tiles
 
 template <int D, int TYPE>
 struct TcLayout {
@@ -261,13 +262,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
     uint8_t* vq = reinterpret_cast<uint8_t*>(a.vq);
 
     // tiles: visible cache keys [lo, P) in 32-key tiles starting at a
-    // multiple of 32, then the tree slots [P, P + n); the whole list is split
-    // evenly over the cluster, so the tree tiles go to the last ranks
+    // multiple of 32, then the tree slots [P, P + n).  The list is split over
+    // the cluster by cost, a tree tile counting kTreeCost cache tiles (its
+    // CTA also quantises it), so the tree tiles go to the last ranks
     const int lo = (W > 0) ? max(0, P - W + 1) : 0;
     const int c0 = (lo / kTK) * kTK;
     const int n_cache_tiles = (P > lo) ? (P - c0 + kTK - 1) / kTK : 0;
-    const int n_all = n_cache_tiles + (n + kTK - 1) / kTK;
-    const int g0 = (int)((long)n_all * rank / CS), T = (int)((long)n_all * (rank + 1) / CS) - g0;
+    const int n_tree_tiles = (n + kTK - 1) / kTK;
+    const int n_all = n_cache_tiles + n_tree_tiles;
+    const long total_cost = (long)n_cache_tiles + (long)kTreeCost * n_tree_tiles;
+    auto tile_at_cost = [&](long c) {  // first tile whose cumulative cost reaches c
+        return (int)(c <= n_cache_tiles ? c : n_cache_tiles + (c - n_cache_tiles + kTreeCost - 1) / kTreeCost);
+    };
+    const int g0 = tile_at_cost(total_cost * rank / CS);
+    const int T = min(n_all, tile_at_cost(total_cost * (rank + 1) / CS)) - g0;
     auto tile = [&](int u) {
         const int g = g0 + u;
         TileInfo ti;
@@ -731,18 +739,34 @@ cudaError_t launch_tc(const AttnVerifyArgs& a, cudaStream_t stream) {
     cudaError_t e = ensure_smem(kern, L::total);
     if (e != cudaSuccess) return e;
     const int rows = (a.Hq / a.Hkv) * a.N_max;
-    const int n_rt = (rows + kRows - 1) / kRows;
-    const int RT = (rows + n_rt - 1) / n_rt;
     const long range = (a.window > 0) ? (long)a.window - 1 : (long)a.cap;
     const long tiles = (range + kTK - 1) / kTK + 3;
-    const long clusters = (long)n_rt * a.Hkv * a.B;
     const int sms = sm_count_cached();
     // the largest cluster (<= 16) that still lets every cluster be resident
     // at once and that the key range can feed
-    int cs = 1;
-    while (cs < 16 && clusters * cs * 2 <= sms && cs * 2 <= tiles &&
-           active_clusters(kern, L::total, cs * 2) >= clusters)
-        cs *= 2;
+    auto choose_cs = [&](int n_rt) {
+        const long clusters = (long)n_rt * a.Hkv * a.B;
+        int cs = 1;
+        while (cs < 16 && clusters * cs * 2 <= sms && cs * 2 <= tiles &&
+               active_clusters(kern, L::total, cs * 2) >= clusters)
+            cs *= 2;
+        return cs;
+    };
+    // row tiles: as few as the 128-row MMA allows; when the key range is
+    // short (latency-bound: a few tiles per CTA) one more row tile is taken
+    // if it buys clearly more CTAs with every cluster still resident
+    int n_rt = (rows + kRows - 1) / kRows;
+    int cs = choose_cs(n_rt);
+    {
+        const int n2 = n_rt + 1, cs2 = choose_cs(n2);
+        const long ctas = (long)n_rt * a.Hkv * a.B * cs, ctas2 = (long)n2 * a.Hkv * a.B * cs2;
+        if ((rows + n2 - 1) / n2 >= 32 && tiles <= 16L * cs2 && ctas2 * 4 > ctas * 5 &&
+            active_clusters(kern, L::total, cs2) >= (long)n2 * a.Hkv * a.B) {
+            n_rt = n2;
+            cs = cs2;
+        }
+    }
+    const int RT = (rows + n_rt - 1) / n_rt;
     return launch_pdl(kern, dim3(cs, n_rt * a.Hkv, a.B), dim3(kThreads), L::total, stream, cs, a, RT, cs);
 }
 
