@@ -80,9 +80,12 @@ def make_host_inputs(rng, n_layers=N_LAYERS):
 
 
 # ---------------------------------------------------------------------------- algorithmic bytes
-def gdn_bytes():
+def gdn_bytes(L=0):
+    """One GDN verify with the previous step's accepted path of length L
+    pending: the state is read, brought up to date and written back."""
     Hk, Hv, dk, dv, N = GDN["Hk"], GDN["Hv"], GDN["dk"], GDN["dv"], BUDGET
-    state = Hv * dv * dk * 4
+    state = Hv * dv * dk * 4 * (2 if L else 1)
+    pend = L * (Hv * dv * 4 + Hv * 4 + Hk * dk * 2)
     qk = 2 * N * Hk * dk * 2
     v = N * Hv * dv * 2
     scal = 2 * N * Hv * 4
@@ -90,7 +93,7 @@ def gdn_bytes():
     u = N * Hv * dv * 4
     g = N * Hv * 4
     kc = N * Hk * dk * 2
-    return state + qk + v + scal + out + u + g + kc
+    return state + pend + qk + v + scal + out + u + g + kc
 
 
 def attn_bytes():
@@ -109,12 +112,10 @@ def accept_bytes():
 
 
 def commit_bytes(L):
-    Hk, Hv, dk, dv = GDN["Hk"], GDN["Hv"], GDN["dk"], GDN["dv"]
-    st = N_GDN * 2 * Hv * dv * dk * 4
-    fac = N_GDN * (L * Hv * dv * 4 + L * Hv * 4 + L * Hk * dk * 2)
+    """Commit of the KV caches (the GDN states are committed inside the
+    next step's verify)."""
     row = ATT["D"] + ATT["D"] // 32 * 2
-    kv = N_ATTN * 2 * 2 * L * ATT["Hkv"] * row
-    return st + fac + kv
+    return N_ATTN * 2 * 2 * L * ATT["Hkv"] * row
 
 
 # ---------------------------------------------------------------------------- clocks
@@ -279,12 +280,12 @@ class GpuStep:
                 L = dict(kind="gdn", q=view(f"{li}.q"), k=view(f"{li}.k"), v=view(f"{li}.v"),
                          beta=view(f"{li}.beta"), log_alpha=view(f"{li}.log_alpha"), state=st,
                          out=t.empty((1, N, GDN["Hv"], GDN["dv"]), device=dev),
-                         u=t.empty((1, N, GDN["Hv"], GDN["dv"]), device=dev),
-                         g=t.empty((1, N, GDN["Hv"]), device=dev),
-                         kc=t.empty((1, N, GDN["Hk"], GDN["dk"]), dtype=t.int16, device=dev))
-                L["fac"] = dflv.gdn_factors(L["u"], L["g"], L["kc"])
+                         u=[t.empty((1, N, GDN["Hv"], GDN["dv"]), device=dev) for _ in range(2)],
+                         g=[t.empty((1, N, GDN["Hv"]), device=dev) for _ in range(2)],
+                         kc=[t.empty((1, N, GDN["Hk"], GDN["dk"]), dtype=t.int16, device=dev) for _ in range(2)])
+                # two factor sets: a step writes one and applies the other (deferred commit)
+                L["fac"] = [dflv.gdn_factors(L["u"][i], L["g"][i], L["kc"][i]) for i in range(2)]
                 self.states.append(st)
-                self.factors.append(L["fac"])
                 self.state0.append(st.clone())
             else:
                 c = d["cache"]
@@ -296,29 +297,36 @@ class GpuStep:
             self.layers.append(L)
         self.launches_per_step = N_GDN + N_ATTN + 2 + 2  # accept and commit: two kernels each
 
-    # one pass of the hot path: every layer's verify, acceptance, commit
-    def step(self):
+    # one pass of the hot path: every layer's verify (the GDN layers first
+    # commit the previous step's accepted path into their state: deferred
+    # commit), acceptance, commit of the KV caches.  Step `par` writes
+    # factor set par and applies set 1 - par.
+    def gdn_verify(self, li, L, par):
+        return self.dflv.dflv_tree_gdn_verify_pending(
+            self.gdn_desc if li == 0 else self.gdn_desc_next, self.parent, self.n_nodes, L["q"], L["k"], L["v"],
+            L["beta"], L["log_alpha"], L["state"], L["fac"][1 - par], self.path, self.path_len, L["out"],
+            L["fac"][par], self.status)
+
+    def step(self, par):
         dflv, chk = self.dflv, self.dflv.check
         for li, L in enumerate(self.layers):
             if L["kind"] == "gdn":
-                chk(dflv.dflv_tree_gdn_verify(self.gdn_desc if li == 0 else self.gdn_desc_next, self.parent,
-                                              self.n_nodes, L["q"], L["k"], L["v"], L["beta"], L["log_alpha"],
-                                              L["state"], L["out"], L["fac"], self.status), "gdn verify")
+                chk(self.gdn_verify(li, L, par), "gdn verify")
             else:
                 chk(dflv.dflv_tree_attn_verify(self.attn_desc_next, self.parent, self.n_nodes, self.n_past, L["q"],
                                                L["k_new"], L["v_new"], L["kv"], L["out"], self.status),
                     "attn verify")
         chk(dflv.dflv_accept_greedy(1, BUDGET, VOCAB, self.logits, self.tokens, self.parent, self.n_nodes,
                                     self.path, self.path_len, self.next_token, self.best, self.status), "accept")
-        chk(dflv.dflv_commit_rollback(self.gdn_desc, len(self.states), self.states, self.factors, self.attn_desc,
-                                      len(self.caches), self.caches, self.path, self.path_len, self.n_past,
-                                      self.status), "commit")
+        chk(dflv.dflv_commit_rollback(None, 0, [], [], self.attn_desc, len(self.caches), self.caches, self.path,
+                                      self.path_len, self.n_past, self.status), "commit")
 
     def reset(self):
         """Committed state back to its initial value (between passes)."""
         for s, s0 in zip(self.states, self.state0):
             s.copy_(s0)
         self.n_past.fill_(CTX)
+        self.path_len.zero_()  # nothing pending
 
 
 def kernel_chain_ms(S, torch, stream, steps, warmup):
@@ -328,9 +336,7 @@ def kernel_chain_ms(S, torch, stream, steps, warmup):
     def gdn_chain():
         for li, L in enumerate(S.layers):
             if L["kind"] == "gdn":
-                chk(dflv.dflv_tree_gdn_verify(S.gdn_desc if li == 0 else S.gdn_desc_next, S.parent, S.n_nodes,
-                                              L["q"], L["k"], L["v"], L["beta"], L["log_alpha"], L["state"],
-                                              L["out"], L["fac"], S.status), "gdn verify")
+                chk(S.gdn_verify(li, L, 0), "gdn verify")
 
     def attn_chain():
         for L in S.layers:
@@ -343,8 +349,8 @@ def kernel_chain_ms(S, torch, stream, steps, warmup):
                                     S.path_len, S.next_token, S.best, S.status), "accept")
 
     def commit():
-        chk(dflv.dflv_commit_rollback(S.gdn_desc, len(S.states), S.states, S.factors, S.attn_desc,
-                                      len(S.caches), S.caches, S.path, S.path_len, S.n_past, S.status), "commit")
+        chk(dflv.dflv_commit_rollback(None, 0, [], [], S.attn_desc, len(S.caches), S.caches, S.path, S.path_len,
+                                      S.n_past, S.status), "commit")
 
     out = {}
     for name, fn, n in (("gdn", gdn_chain, N_GDN), ("attn", attn_chain, N_ATTN), ("accept", accept, 1),
@@ -353,6 +359,9 @@ def kernel_chain_ms(S, torch, stream, steps, warmup):
         with torch.cuda.graph(g, stream=stream):
             fn()
         S.reset()
+        with torch.cuda.stream(stream):
+            accept()  # an accepted path: the GDN verifies apply it as their pending commit
+        torch.cuda.synchronize()
         for _ in range(warmup):
             g.replay()
         torch.cuda.synchronize()
@@ -382,22 +391,32 @@ def run_gpu(args, rank, world):
     S = GpuStep(host, torch, dflv)
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
-    # eager warm-up on the capture stream (sets kernel attributes once), then capture
+    # eager warm-up on the capture stream (sets kernel attributes once), then
+    # capture the two step parities (factor sets alternate between steps)
     with torch.cuda.stream(stream):
-        S.step()
+        S.step(0)
+        S.step(1)
     torch.cuda.synchronize()
     S.reset()
     torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        S.step()
+    graphs = [torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()]
+    for par in range(2):
+        with torch.cuda.graph(graphs[par], stream=stream):
+            S.step(par)
     torch.cuda.synchronize()
     assert int(S.status.item()) == 0, f"device status {int(S.status.item())}"
+    count = [0]
+
+    def replay():
+        graphs[count[0] % 2].replay()
+        count[0] += 1
+
 
     # ---- device-resident timing
     S.reset()
+    count[0] = 0
     for _ in range(args.warmup):
-        graph.replay()
+        replay()
     torch.cuda.synchronize()
     barrier(world)
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
@@ -408,7 +427,7 @@ def run_gpu(args, rank, world):
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record()
     for _ in range(args.steps):
-        graph.replay()
+        replay()
     t1.record()
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
@@ -426,10 +445,11 @@ def run_gpu(args, rank, world):
     per = kernel_chain_ms(S, torch, stream, args.steps, args.warmup)
     # ---- end to end: pinned host inputs -> device, step, result -> host, every step
     S.reset()
+    count[0] = 0
     torch.cuda.synchronize()
     for _ in range(args.warmup):
         S.d_in.copy_(S.h_in, non_blocking=True)
-        graph.replay()
+        replay()
         S.h_out[: BUDGET].copy_(S.path[0], non_blocking=True)
         torch.cuda.synchronize()
     barrier(world)
@@ -437,7 +457,7 @@ def run_gpu(args, rank, world):
     e0.record()
     for _ in range(args.steps):
         S.d_in.copy_(S.h_in, non_blocking=True)
-        graph.replay()
+        replay()
         S.h_out[: BUDGET].copy_(S.path[0], non_blocking=True)
         S.h_out[BUDGET].copy_(S.path_len[0], non_blocking=True)
         S.h_out[BUDGET + 1].copy_(S.next_token[0], non_blocking=True)
@@ -528,11 +548,13 @@ def profile_one(kind, launches):
     rng = np.random.default_rng(SEED)
     host = make_host_inputs(rng, n_layers=4)
     S = GpuStep(host, torch, dflv)
-    L = next(L for L in S.layers if L["kind"] == ("attn" if kind == "attn" else "gdn"))
+    li, L = next((i, L) for i, L in enumerate(S.layers) if L["kind"] == ("attn" if kind == "attn" else "gdn"))
+    # one step first: both factor sets written and an accepted path pending
+    S.step(1)
+    S.n_past.fill_(CTX)
     for _ in range(launches):
         if kind == "gdn":
-            dflv.check(dflv.dflv_tree_gdn_verify(S.gdn_desc, S.parent, S.n_nodes, L["q"], L["k"], L["v"], L["beta"],
-                                                 L["log_alpha"], L["state"], L["out"], L["fac"], S.status))
+            dflv.check(S.gdn_verify(li, L, 0))
         elif kind == "attn":
             dflv.check(dflv.dflv_tree_attn_verify(S.attn_desc, S.parent, S.n_nodes, S.n_past, L["q"], L["k_new"],
                                                   L["v_new"], L["kv"], L["out"], S.status))
@@ -540,7 +562,7 @@ def profile_one(kind, launches):
             dflv.check(dflv.dflv_accept_greedy(1, BUDGET, VOCAB, S.logits, S.tokens, S.parent, S.n_nodes, S.path,
                                                S.path_len, S.next_token, S.best, S.status))
         else:
-            S.step()
+            S.step(0)
             S.n_past.fill_(CTX)
     torch.cuda.synchronize()
     print(json.dumps({"kernel": kind, "launches": launches, "status": int(S.status.item())}))
@@ -596,7 +618,7 @@ def main():
     peak, peak_kind = hbm_peak()
     per = r["per"] or {}
     L = r["L"]
-    ab = dict(gdn=gdn_bytes(), attn=attn_bytes(), accept=accept_bytes(), commit=commit_bytes(L))
+    ab = dict(gdn=gdn_bytes(L), attn=attn_bytes(), accept=accept_bytes(), commit=commit_bytes(L))
     launches = dict(gdn=N_GDN, attn=N_ATTN, accept=1, commit=1)
     # dominant kernel: the largest share of the step
     shares = {k: per[k] * launches[k] for k in per} if per else {}

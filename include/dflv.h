@@ -144,6 +144,42 @@ dflv_status dflv_tree_gdn_verify(const dflv_gdn_desc* desc, const int32_t* paren
                                  int32_t* status_dev, void* workspace, size_t ws_bytes,
                                  dflv_stream_t stream);
 
+/* Deferred commit ([PR606]: SpecLA keeps the accepted path's factors pending
+ * and applies them while the state streams into the next verify).  Tree
+ * verify of one gated-DeltaNet layer whose committed state still owes the
+ * previous step's accepted path:
+ *   state        [B][Hv][dv][dk] f32, IN/OUT: on entry the state before the
+ *                previous step's commit of this layer; every row is first
+ *                brought up to date,
+ *                  S <- e^{g_e} S + sum_{m<L} e^{g_e - g_{p_m}} u_{p_m} k_{p_m}^T
+ *                (p_m = pending_path[b][m], e = p_{L-1}, u/g/kcopy from
+ *                pending: the update dflv_commit_rollback applies), written
+ *                back, and the tree is verified against the updated state.
+ *   pending      the previous verify's factors of this layer (read only; must
+ *                not alias `factors`, which receives this verify's factors)
+ *   pending_path [B][N_max] int32, pending_len [B] int32: the previous step's
+ *                accepted path (dflv_accept_greedy output); pending_len[b] = 0
+ *                leaves sequence b's state as it is.  A length outside
+ *                [0, N_max] or a node outside [0, N_max) raises
+ *                DFLV_DEV_PATH and that sequence's update is skipped.
+ * Everything else as dflv_tree_gdn_verify (same descriptor, N_max equal to
+ * the previous verify's).  With DFLV_FLAG_EARLY_PREFETCH the tree, pending
+ * factors and pending path are read, and the state rows are read, brought up
+ * to date and written back, before the dependency wait: the kernel
+ * immediately before the call must not write those buffers, nor read the
+ * state.
+ * A step then commits only the KV caches (dflv_commit_rollback with
+ * n_gdn = 0); the final pending update of a sequence can be applied with
+ * dflv_commit_rollback as usual. */
+dflv_status dflv_tree_gdn_verify_pending(const dflv_gdn_desc* desc, const int32_t* parent,
+                                         const int32_t* n_nodes, const uint16_t* q, const uint16_t* k,
+                                         const uint16_t* v, const float* beta, const float* log_alpha,
+                                         float* state, const dflv_gdn_factors* pending,
+                                         const int32_t* pending_path, const int32_t* pending_len,
+                                         float* out, const dflv_gdn_factors* factors,
+                                         int32_t* status_dev, void* workspace, size_t ws_bytes,
+                                         dflv_stream_t stream);
+
 size_t dflv_gdn_workspace_size(const dflv_gdn_desc* desc);
 
 /* ------------------------------------------------------------------------ */

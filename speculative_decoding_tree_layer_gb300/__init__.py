@@ -11,6 +11,7 @@ from .dflv import (DFLV_DEV_CAPACITY, DFLV_DEV_PATH, DFLV_DEV_TIMEOUT, DFLV_DEV_
                    DflvError,
                    attn_desc, check, dflv_accept_greedy, dflv_attn_workspace_size, dflv_commit_rollback,
                    dflv_gdn_workspace_size, dflv_status_string, dflv_tree_attn_verify, dflv_tree_gdn_verify,
+                   dflv_tree_gdn_verify_pending,
                    gdn_desc, gdn_factors, kv_layer, load)
 
 __all__ = [n for n in dir() if n.startswith(("dflv", "DFLV", "Dflv")) or n in (

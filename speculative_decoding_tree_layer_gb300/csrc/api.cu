@@ -58,6 +58,42 @@ dflv_status check_kv_layer(const dflv_attn_desc* d, const dflv_kv_layer* c) {
     return DFLV_OK;
 }
 
+dflv_status fill_gdn_args(const dflv_gdn_desc* desc, const int32_t* parent, const int32_t* n_nodes,
+                          const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* beta,
+                          const float* log_alpha, const float* state, float* out, const dflv_gdn_factors* factors,
+                          int32_t* status_dev, dflv::GdnVerifyArgs& a) {
+    dflv_status s = check_gdn_desc(desc);
+    if (s != DFLV_OK) return s;
+    if (!parent || !n_nodes || !q || !k || !v || !beta || !log_alpha || !state || !out || !factors ||
+        !factors->u || !factors->g || !factors->kcopy || !status_dev)
+        return DFLV_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(state) || !aligned16(factors->kcopy) ||
+        !aligned4(parent) || !aligned4(n_nodes) || !aligned4(beta) || !aligned4(log_alpha) ||
+        !aligned4(out) || !aligned4(factors->u) || !aligned4(factors->g) || !aligned4(status_dev))
+        return DFLV_ERR_INVALID_ARG;
+    a.B = desc->B;
+    a.N_max = desc->N_max;
+    a.Hk = desc->Hk;
+    a.Hv = desc->Hv;
+    a.dk = desc->dk;
+    a.dv = desc->dv;
+    a.flags = desc->flags;
+    a.parent = parent;
+    a.n_nodes = n_nodes;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.beta = beta;
+    a.log_alpha = log_alpha;
+    a.state = state;
+    a.out = out;
+    a.u = factors->u;
+    a.g = factors->g;
+    a.kcopy = factors->kcopy;
+    a.status = status_dev;
+    return DFLV_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -85,36 +121,40 @@ dflv_status dflv_tree_gdn_verify(const dflv_gdn_desc* desc, const int32_t* paren
                                  dflv_stream_t stream) {
     (void)workspace;
     (void)ws_bytes;
-    dflv_status s = check_gdn_desc(desc);
+    dflv::GdnVerifyArgs a = {};
+    dflv_status s = fill_gdn_args(desc, parent, n_nodes, q, k, v, beta, log_alpha, state, out, factors,
+                                  status_dev, a);
     if (s != DFLV_OK) return s;
-    if (!parent || !n_nodes || !q || !k || !v || !beta || !log_alpha || !state || !out || !factors ||
-        !factors->u || !factors->g || !factors->kcopy || !status_dev)
+    return from_cuda(dflv::launch_gdn_tree_verify(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dflv_status dflv_tree_gdn_verify_pending(const dflv_gdn_desc* desc, const int32_t* parent,
+                                         const int32_t* n_nodes, const uint16_t* q, const uint16_t* k,
+                                         const uint16_t* v, const float* beta, const float* log_alpha,
+                                         float* state, const dflv_gdn_factors* pending,
+                                         const int32_t* pending_path, const int32_t* pending_len,
+                                         float* out, const dflv_gdn_factors* factors,
+                                         int32_t* status_dev, void* workspace, size_t ws_bytes,
+                                         dflv_stream_t stream) {
+    (void)workspace;
+    (void)ws_bytes;
+    dflv::GdnVerifyArgs a = {};
+    dflv_status s = fill_gdn_args(desc, parent, n_nodes, q, k, v, beta, log_alpha, state, out, factors,
+                                  status_dev, a);
+    if (s != DFLV_OK) return s;
+    if (!pending || !pending->u || !pending->g || !pending->kcopy || !pending_path || !pending_len)
         return DFLV_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(state) || !aligned16(factors->kcopy) ||
-        !aligned4(parent) || !aligned4(n_nodes) || !aligned4(beta) || !aligned4(log_alpha) ||
-        !aligned4(out) || !aligned4(factors->u) || !aligned4(factors->g) || !aligned4(status_dev))
+    if (!aligned16(pending->u) || !aligned16(pending->kcopy) || !aligned4(pending->g) || !aligned4(pending_path) ||
+        !aligned4(pending_len))
         return DFLV_ERR_INVALID_ARG;
-    dflv::GdnVerifyArgs a;
-    a.B = desc->B;
-    a.N_max = desc->N_max;
-    a.Hk = desc->Hk;
-    a.Hv = desc->Hv;
-    a.dk = desc->dk;
-    a.dv = desc->dv;
-    a.flags = desc->flags;
-    a.parent = parent;
-    a.n_nodes = n_nodes;
-    a.q = q;
-    a.k = k;
-    a.v = v;
-    a.beta = beta;
-    a.log_alpha = log_alpha;
-    a.state = state;
-    a.out = out;
-    a.u = factors->u;
-    a.g = factors->g;
-    a.kcopy = factors->kcopy;
-    a.status = status_dev;
+    if (pending->u == factors->u || pending->g == factors->g || pending->kcopy == factors->kcopy)
+        return DFLV_ERR_INVALID_ARG;  // the new factors would overwrite the pending ones
+    a.pend_u = pending->u;
+    a.pend_g = pending->g;
+    a.pend_k = pending->kcopy;
+    a.pend_path = pending_path;
+    a.pend_len = pending_len;
+    a.state_out = state;
     return from_cuda(dflv::launch_gdn_tree_verify(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -46,7 +46,7 @@ constexpr int kHalfWarps = kGdnWarps / 2;
 
 struct GdnSmemLayout {
     int NP, DK, RB, KS;
-    size_t off_S, off_V, off_K, off_Q, off_A, off_M, off_R, off_SQ, total;
+    size_t off_S, off_V, off_K, off_Q, off_A, off_M, off_R, off_SQ, off_PK, off_PU, off_PC, total;
     __host__ __device__ GdnSmemLayout(int np, int dk, int rb) : NP(np), DK(dk), RB(rb), KS(dk + 16) {
         off_S = 3200;  // header: mbarrier + per-node arrays (3136 B), rounded up to 128
         off_V = off_S + (size_t)RB * DK * 4;     // bf16 v of this CTA's rows, [node][RB]
@@ -56,7 +56,10 @@ struct GdnSmemLayout {
         off_M = off_A + (size_t)NP * NP * 4;     // dense [NP][NP], zero off the ancestors-or-self
         off_R = off_M + (size_t)NP * NP * 4;     // [node][RB]: S_0 k, then u
         off_SQ = off_R + (size_t)NP * RB * 4;    // [node][RB]: S_0 q
-        total = off_SQ + (size_t)NP * RB * 4;
+        off_PK = off_SQ + (size_t)NP * RB * 4;   // deferred commit: k of the pending path, [m][KS]
+        off_PU = off_PK + (size_t)NP * KS * 2;   // u of the pending path for this CTA's rows, [m][RB]
+        off_PC = off_PU + (size_t)NP * RB * 4;   // e^{g_e - g_{p_m}} per m, then e^{g_e}
+        total = off_PC + (size_t)(64 + 4) * 4;
     }
 };
 
@@ -196,6 +199,42 @@ DFLV_DEVINL void gdn_state_products(const float* S_s, const uint16_t* K_s, const
     }
 }
 
+// Deferred commit, by the 128 threads of the second half (ht = 0..127):
+// S <- e^{g_e} S + sum_{m<PL} e^{g_e - g_{p_m}} u_{p_m} k_{p_m}^T on this CTA's
+// rows in shared memory, and the updated rows back to the state in HBM.
+// PC_s holds g_{p_m} on entry.
+template <int DK, int RB>
+DFLV_DEVINL void gdn_apply_pending(const GdnVerifyArgs& a, float* S_s, const uint16_t* PK_s, const float* PU_s,
+                                   float* PC_s, int PL, int b, int h, int r0, int ht) {
+    constexpr int KS = DK + 16;
+    const float ge = PC_s[PL - 1];  // g of the path's end node
+    named_barrier_sync(2, kGdnThreads / 2);  // every thread has read ge
+    if (ht < PL) PC_s[ht] = expf(ge - PC_s[ht]);
+    if (ht == 0) PC_s[kMaxNodes] = expf(ge);
+    named_barrier_sync(2, kGdnThreads / 2);
+    const float Ge = PC_s[kMaxNodes];
+    float* dst = a.state_out + (((size_t)b * a.Hv + h) * a.dv + r0) * DK;
+    for (int e4 = ht; e4 < RB * DK / 4; e4 += kGdnThreads / 2) {
+        const int r = (e4 * 4) / DK, c = (e4 * 4) % DK;
+        float4 x = *reinterpret_cast<const float4*>(S_s + r * DK + c);
+        x.x *= Ge;
+        x.y *= Ge;
+        x.z *= Ge;
+        x.w *= Ge;
+        for (int m = 0; m < PL; ++m) {
+            const float w = PC_s[m] * PU_s[m * RB + r];
+            const uint2 kk = *reinterpret_cast<const uint2*>(PK_s + m * KS + c);
+            x.x = fmaf(w, bf16_bits_to_float((uint16_t)(kk.x & 0xffff)), x.x);
+            x.y = fmaf(w, bf16_bits_to_float((uint16_t)(kk.x >> 16)), x.y);
+            x.z = fmaf(w, bf16_bits_to_float((uint16_t)(kk.y & 0xffff)), x.z);
+            x.w = fmaf(w, bf16_bits_to_float((uint16_t)(kk.y >> 16)), x.w);
+        }
+        *reinterpret_cast<float4*>(S_s + r * DK + c) = x;
+        *reinterpret_cast<float4*>(dst + r * DK + c) = x;
+    }
+    named_barrier_sync(2, kGdnThreads / 2);  // every row is updated before the products read them
+}
+
 template <int DK, int RB, int NPT>
 __global__ void __launch_bounds__(kGdnThreads, 2)
     gdn_tree_verify_kernel(GdnVerifyArgs a) {
@@ -207,6 +246,7 @@ __global__ void __launch_bounds__(kGdnThreads, 2)
     int32_t* misc_s = reinterpret_cast<int32_t*>(smem + 16);  // [1]: the state copy timed out
     int32_t* par_s = reinterpret_cast<int32_t*>(smem + 64);
     int32_t* depth_s = par_s + kMaxNodes;
+    int32_t* ppath_s = depth_s + kMaxNodes;  // deferred commit: the pending path
     uint64_t* amask_s = reinterpret_cast<uint64_t*>(smem + 64 + 4 * 256 + 512);
     float* beta_s = reinterpret_cast<float*>(smem + 64 + 4 * 256 + 512 + 512);
     float* la_s = beta_s + kMaxNodes;
@@ -220,6 +260,9 @@ __global__ void __launch_bounds__(kGdnThreads, 2)
     float* M_s = reinterpret_cast<float*>(smem + L.off_M);
     float* R_s = reinterpret_cast<float*>(smem + L.off_R);
     float* SQ_s = reinterpret_cast<float*>(smem + L.off_SQ);
+    uint16_t* PK_s = reinterpret_cast<uint16_t*>(smem + L.off_PK);
+    float* PU_s = reinterpret_cast<float*>(smem + L.off_PU);
+    float* PC_s = reinterpret_cast<float*>(smem + L.off_PC);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gq = lane >> 2, tq = lane & 3;  // MMA fragment row group / thread in quad
@@ -250,28 +293,40 @@ __global__ void __launch_bounds__(kGdnThreads, 2)
         bulk_g2s(S_s, src, RB * DK * 4, bar);
     }
     for (int i = tid; i < N; i += kGdnThreads) cp_async4(par_s + i, a.parent + (size_t)b * N + i);
+    const bool pending = a.pend_path != nullptr;
+    if (pending) {
+        for (int i = tid; i < N; i += kGdnThreads) cp_async4(ppath_s + i, a.pend_path + (size_t)b * N + i);
+        if (tid == 0) cp_async4(misc_s + 2, a.pend_len + b);
+    }
     cp_async_commit();
+    // The first half (warps 0-3) requests this layer's inputs; the second
+    // half (warps 4-7) fetches the pending commit's rows and brings the state
+    // rows up to date -- before the dependency wait with early prefetch, as
+    // all of that was written by the previous step.
+    const bool gram_half = warp < kHalfWarps;
+    const int ht = gram_half ? tid : tid - kGdnThreads / 2;  // thread index within the half
+    constexpr int kHalf = kGdnThreads / 2;
     constexpr int CH = DK / 8;  // 16-byte chunks per bf16 row
     auto issue_layer_inputs = [&]() {
-        for (int idx = tid; idx < N * CH; idx += kGdnThreads) {
+        for (int idx = ht; idx < N * CH; idx += kHalf) {
             const int i = idx / CH, c = idx % CH;
             const size_t off = (((size_t)b * N + i) * a.Hk + hk) * DK + c * 8;
             cp_async16(K_s + i * KS + c * 8, a.k + off);
             cp_async16(Q_s + i * KS + c * 8, a.q + off);
         }
         constexpr int VCH = RB / 8;  // 16-byte chunks of this CTA's v rows
-        for (int idx = tid; idx < N * VCH; idx += kGdnThreads) {
+        for (int idx = ht; idx < N * VCH; idx += kHalf) {
             const int i = idx / VCH, c = idx % VCH;
             cp_async16(V_s + i * RB + c * 8, a.v + (((size_t)b * N + i) * a.Hv + h) * a.dv + r0 + c * 8);
         }
-        for (int i = tid; i < N; i += kGdnThreads) {
+        for (int i = ht; i < N; i += kHalf) {
             const size_t sidx = ((size_t)b * N + i) * a.Hv + h;
             cp_async4(beta_s + i, a.beta + sidx);
             cp_async4(la_s + i, a.log_alpha + sidx);
         }
         cp_async_commit();
     };
-    if (!early) {
+    if (!early && gram_half) {
         grid_launch_dependents();
         issue_layer_inputs();
     }
@@ -282,8 +337,8 @@ __global__ void __launch_bounds__(kGdnThreads, 2)
         *reinterpret_cast<uint4*>(Q_s + i * KS + c * 8) = make_uint4(0, 0, 0, 0);
     }
     const int n = __ldg(a.n_nodes + b);
-    if (early) cp_async_wait<0>();
-    else cp_async_wait<1>();
+    if (!early && gram_half) cp_async_wait<1>();
+    else cp_async_wait<0>();
     __syncthreads();
 
     // 2. Tree topology (from the staged parent array).
@@ -296,13 +351,52 @@ __global__ void __launch_bounds__(kGdnThreads, 2)
         }
         return;
     }
-    if (early) {
-        grid_dependency_wait();
-        grid_launch_dependents();
-        issue_layer_inputs();
+    // Deferred commit: the pending path (validated by every thread alike).
+    int PL = 0;
+    if (pending) {
+        const int Lp = misc_s[2];
+        bool valid = Lp >= 0 && Lp <= N;
+        for (int m = 0; valid && m < Lp; ++m) valid = ppath_s[m] >= 0 && ppath_s[m] < N;
+        if (!valid) {
+            if (tid == 0) raise_status(a.status, DFLV_DEV_PATH);
+        } else {
+            PL = Lp;
+        }
     }
-    cp_async_wait<0>();
-    __syncthreads();
+    if (!gram_half) {
+        // the pending path's k rows, this CTA's u rows and the path's decays
+        if (PL > 0) {
+            constexpr int UCH = RB / 4;  // 16-byte chunks of this CTA's u row block
+            for (int idx = ht; idx < PL * (CH + UCH); idx += kHalf) {
+                const int m = idx / (CH + UCH), c = idx % (CH + UCH), p = ppath_s[m];
+                if (c < CH)
+                    cp_async16(PK_s + m * KS + c * 8, a.pend_k + (((size_t)b * N + p) * a.Hk + hk) * DK + c * 8);
+                else
+                    cp_async16(PU_s + m * RB + (c - CH) * 4,
+                               a.pend_u + (((size_t)b * N + p) * a.Hv + h) * a.dv + r0 + (c - CH) * 4);
+            }
+            for (int m = ht; m < PL; m += kHalf)
+                cp_async4(PC_s + m, a.pend_g + ((size_t)b * N + ppath_s[m]) * a.Hv + h);
+            cp_async_commit();
+            cp_async_wait<0>();
+            named_barrier_sync(2, kHalf);
+        }
+        if (!mbar_wait_bounded(bar, 0, a.status)) {
+            if (lane == 0) atomicOr(misc_s + 1, 1);
+        } else if (PL > 0) {
+            gdn_apply_pending<DK, RB>(a, S_s, PK_s, PU_s, PC_s, PL, b, h, r0, ht);
+        }
+        if (early) grid_dependency_wait();  // before any output is written
+    } else {
+        if (early) {
+            grid_dependency_wait();
+            grid_launch_dependents();
+            issue_layer_inputs();
+        }
+        cp_async_wait<0>();
+    }
+    __syncthreads();  // layer inputs and the up-to-date state rows are in place
+    if (misc_s[1]) return;  // the state copy never landed (status already raised)
 
     if (warp < kHalfWarps) {
         // 3. cumulative log decay over the ancestors-or-self
@@ -331,13 +425,9 @@ __global__ void __launch_bounds__(kGdnThreads, 2)
         }
     } else {
         // 6. S_0[rows] . [K | Q]
-        if (mbar_wait_bounded(bar, 0, a.status))
-            gdn_state_products<DK, RB, NPT>(S_s, K_s, Q_s, R_s, SQ_s, warp - kHalfWarps, gq, tq);
-        else if (lane == 0)
-            atomicOr(misc_s + 1, 1);
+        gdn_state_products<DK, RB, NPT>(S_s, K_s, Q_s, R_s, SQ_s, warp - kHalfWarps, gq, tq);
     }
     __syncthreads();
-    if (misc_s[1]) return;  // the state copy never landed (status already raised)
 
     // 7-8. Rows are independent: lane r of the first RB threads solves
     //    u_i = R_i - sum_{l < i} A_il u_l,  R_i = beta_i (v_i - e^{g_i} S_0 k_i),

@@ -24,6 +24,14 @@ struct GdnVerifyArgs {
     float* g;
     uint16_t* kcopy;
     int32_t* status;
+    // deferred commit (null pointers: none): the previous verify's factors
+    // and accepted path; the updated state rows are written to state_out
+    const float* pend_u;
+    const float* pend_g;
+    const uint16_t* pend_k;
+    const int32_t* pend_path;
+    const int32_t* pend_len;
+    float* state_out;
 };
 
 cudaError_t launch_gdn_tree_verify(const GdnVerifyArgs& a, cudaStream_t stream);

@@ -68,6 +68,8 @@ def load():
     S = ctypes.c_size_t
     lib.dflv_tree_gdn_verify.argtypes = [ctypes.POINTER(dflv_gdn_desc)] + [P] * 9 + \
         [ctypes.POINTER(dflv_gdn_factors), P, P, S, P]
+    lib.dflv_tree_gdn_verify_pending.argtypes = [ctypes.POINTER(dflv_gdn_desc)] + [P] * 8 + \
+        [ctypes.POINTER(dflv_gdn_factors), P, P, P, ctypes.POINTER(dflv_gdn_factors), P, P, S, P]
     lib.dflv_tree_attn_verify.argtypes = [ctypes.POINTER(dflv_attn_desc)] + [P] * 6 + \
         [ctypes.POINTER(dflv_kv_layer), P, P, P, S, P]
     lib.dflv_accept_greedy.argtypes = [_c_i32, _c_i32, _c_i32] + [P] * 10
@@ -80,7 +82,8 @@ def load():
     lib.dflv_attn_workspace_size.restype = S
     lib.dflv_status_string.argtypes = [ctypes.c_int]
     lib.dflv_status_string.restype = ctypes.c_char_p
-    for f in ("dflv_tree_gdn_verify", "dflv_tree_attn_verify", "dflv_accept_greedy", "dflv_commit_rollback"):
+    for f in ("dflv_tree_gdn_verify", "dflv_tree_gdn_verify_pending", "dflv_tree_attn_verify", "dflv_accept_greedy",
+              "dflv_commit_rollback"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -145,6 +148,15 @@ def dflv_tree_gdn_verify(desc, parent, n_nodes, q, k, v, beta, log_alpha, state,
         ctypes.byref(desc), _ptr(parent), _ptr(n_nodes), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
         _ptr(log_alpha), _ptr(state), _ptr(out), ctypes.byref(factors), _ptr(status_dev),
         _ptr(workspace), ws_bytes, _stream(stream))
+
+
+def dflv_tree_gdn_verify_pending(desc, parent, n_nodes, q, k, v, beta, log_alpha, state, pending, pending_path,
+                                 pending_len, out, factors, status_dev, workspace=None, ws_bytes=0,
+                                 stream=None) -> int:
+    return load().dflv_tree_gdn_verify_pending(
+        ctypes.byref(desc), _ptr(parent), _ptr(n_nodes), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+        _ptr(log_alpha), _ptr(state), ctypes.byref(pending), _ptr(pending_path), _ptr(pending_len), _ptr(out),
+        ctypes.byref(factors), _ptr(status_dev), _ptr(workspace), ws_bytes, _stream(stream))
 
 
 def dflv_tree_attn_verify(desc, parent, n_nodes, n_past, q, k_new, v_new, cache, out, status_dev,

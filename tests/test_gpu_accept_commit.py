@@ -257,3 +257,78 @@ def test_tiny_case_full_step_twice(dflv, orc):
         assert_close(host(state), gstate_ref, what=f"step {step} state")
         hc = host(dcache["kq"])
         assert np.array_equal(hc[:, :, :ref_P], ref_cache["kq"][:, :, :ref_P])
+
+
+def test_deferred_commit_matches_eager(dflv, orc):
+    """Deferred commit: each verify applies the previous step's accepted path
+    to the state it streams (and writes it back), so a step commits only the
+    KV caches.  Three steps on two sequences (one with an empty pending
+    path), outputs and states against the oracle's eager commit."""
+    rng = np.random.default_rng(77)
+    Hk, Hv, dk, dv, B, N = 2, 6, 128, 64, 2, 22
+    state0 = (rng.standard_normal((B, Hv, dv, dk)) * 0.3).astype(np.float32)
+    state = dev(state0)
+    ref_state = state0.copy()
+    fac = [dict(u=torch.empty((B, N, Hv, dv), device="cuda"), g=torch.empty((B, N, Hv), device="cuda"),
+                kc=torch.empty((B, N, Hk, dk), dtype=torch.int16, device="cuda")) for _ in range(2)]
+    prev = None
+    for step in range(3):
+        parents = [synth.ddtree(rng, N, 1000)[0] for _ in range(B)]
+        parent, n_nodes = synth.batch_trees(parents, N)
+        gi = synth.gdn_inputs(rng, B, N, Hk, Hv, dk, dv, state=False)
+        keep = {k: dev(v) for k, v in gi.items()}
+        out = torch.full((B, N, Hv, dv), float("nan"), device="cuda")
+        f = fac[step % 2]
+        st = zeros_status()
+        args = (dflv.gdn_desc(B, N, Hk, Hv, dk, dv), dev(parent), dev(n_nodes), keep["q"], keep["k"], keep["v"],
+                keep["beta"], keep["log_alpha"], state)
+        if prev is None:
+            dflv.check(dflv.dflv_tree_gdn_verify(*args, out, dflv.gdn_factors(f["u"], f["g"], f["kc"]), st))
+        else:
+            pf, ppath, plen = prev
+            dflv.check(dflv.dflv_tree_gdn_verify_pending(*args, dflv.gdn_factors(pf["u"], pf["g"], pf["kc"]),
+                                                         dev(ppath), dev(plen), out,
+                                                         dflv.gdn_factors(f["u"], f["g"], f["kc"]), st))
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        ref_out = orc.tree_gdn_verify(parent, n_nodes, gi["q"], gi["k"], gi["v"], gi["beta"], gi["log_alpha"],
+                                      ref_state)
+        for b in range(B):
+            assert_close(host(out)[b], ref_out[b], what=f"step {step} out b={b}")
+        if prev is not None:
+            assert_close(host(state), ref_state, what=f"state written by step {step}")
+        # this step's accepted paths: a prefix of the deepest path (empty for b = 1 at step 1)
+        path = np.full((B, N), -1, np.int32)
+        plen = np.zeros(B, np.int32)
+        for b in range(B):
+            dp = synth.deepest_path(parents[b])
+            L = 0 if (b == 1 and step == 1) else int(rng.integers(1, len(dp) + 1))
+            path[b, :L] = dp[:L]
+            plen[b] = L
+        ref_state = np.stack([
+            orc.gdn_commit(gi["q"][b:b + 1], gi["k"][b:b + 1], gi["v"][b:b + 1], gi["beta"][b:b + 1],
+                           gi["log_alpha"][b:b + 1], path[b:b + 1], plen[b:b + 1], ref_state[b:b + 1])[0]
+            if plen[b] > 0 else ref_state[b] for b in range(B)])
+        prev = (f, path, plen)
+
+
+def test_deferred_commit_bad_path_sets_status(dflv):
+    rng = np.random.default_rng(78)
+    Hk, Hv, dk, dv, B, N = 1, 2, 64, 32, 1, 6
+    par = synth.uniform_tree(rng, N)
+    parent, n_nodes = synth.batch_trees([par], N)
+    gi = synth.gdn_inputs(rng, B, N, Hk, Hv, dk, dv)
+    keep = {k: dev(v) for k, v in gi.items()}
+    fa = [dict(u=torch.zeros((B, N, Hv, dv), device="cuda"), g=torch.zeros((B, N, Hv), device="cuda"),
+               kc=torch.zeros((B, N, Hk, dk), dtype=torch.int16, device="cuda")) for _ in range(2)]
+    out = torch.empty((B, N, Hv, dv), device="cuda")
+    before = keep["state"].clone()
+    st = zeros_status()
+    dflv.check(dflv.dflv_tree_gdn_verify_pending(
+        dflv.gdn_desc(B, N, Hk, Hv, dk, dv), dev(parent), dev(n_nodes), keep["q"], keep["k"], keep["v"],
+        keep["beta"], keep["log_alpha"], keep["state"], dflv.gdn_factors(fa[0]["u"], fa[0]["g"], fa[0]["kc"]),
+        dev(np.arange(N, dtype=np.int32)[None]), dev(np.array([N + 1], np.int32)), out,
+        dflv.gdn_factors(fa[1]["u"], fa[1]["g"], fa[1]["kc"]), st))
+    torch.cuda.synchronize()
+    assert int(st.item()) == dflv.DFLV_DEV_PATH
+    assert torch.equal(keep["state"], before)
