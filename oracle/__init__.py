@@ -72,6 +72,8 @@ def _load():
             lib.orc_tree_attn_verify.argtypes = [I] * 8 + [ctypes.c_double] + [P] * 11 + [P, I]
             lib.orc_accept_greedy.argtypes = [I, I, I] + [P] * 8
             lib.orc_kv_commit.argtypes = [I] * 6 + [P] * 7
+            lib.orc_tree_conv_verify.argtypes = [I] * 4 + [P] * 6
+            lib.orc_conv_commit.argtypes = [I] * 4 + [P] * 4
             _lib = lib
     return _lib
 
@@ -272,3 +274,31 @@ def kv_commit(cache, kv_type, path, path_len, n_past):
                                _p(n_past), _p(cache["kq"]), _p(cache["vq"]),
                                _p(cache.get("ks")), _p(cache.get("vs")))
     _check(rc, "kv_commit")
+
+
+# ---------------------------------------------------------------- short convolution
+def tree_conv_verify(parent, n_nodes, x, state, w):
+    """x [B][N][C] bf16 bits, state [B][K-1][C] bf16 bits, w [C][K] f32 ->
+    out [B][N][C] f32: each node's window of K inputs along its parent chain,
+    continued into the conv state before the root."""
+    parent, n_nodes = _c(parent, np.int32), _c(n_nodes, np.int32)
+    x, state, w = _c(x, np.uint16), _c(state, np.uint16), _c(w, np.float32)
+    B, N, C = x.shape
+    K = w.shape[1]
+    assert state.shape == (B, K - 1, C)
+    out = np.zeros((B, N, C), np.float32)
+    rc = _load().orc_tree_conv_verify(B, N, C, K, _p(parent), _p(n_nodes), _p(x), _p(state), _p(w), _p(out))
+    _check(rc, "tree_conv_verify")
+    return out
+
+
+def conv_commit(x, path, path_len, state):
+    """Returns the committed conv state (a new array): the last K-1 entries
+    of [state ; x of the accepted path]."""
+    x, path, path_len = _c(x, np.uint16), _c(path, np.int32), _c(path_len, np.int32)
+    st = np.array(state, dtype=np.uint16, order="C", copy=True)
+    B, N, C = x.shape
+    K = st.shape[1] + 1
+    rc = _load().orc_conv_commit(B, N, C, K, _p(x), _p(path), _p(path_len), _p(st))
+    _check(rc, "conv_commit")
+    return st

@@ -565,3 +565,62 @@ int orc_kv_commit(int B, int N, int Hkv, int D, int cap, int kv_type,
     free(tmp);
     return ORC_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* tree-aware short convolution                                              */
+/* ------------------------------------------------------------------------ */
+
+int orc_tree_conv_verify(int B, int N, int C, int K, const int32_t* parent, const int32_t* n_nodes,
+                         const uint16_t* x, const uint16_t* state, const float* w, float* out) {
+    if (B < 1 || N < 1 || N > 64 || C < 1 || K < 2) return ORC_ERR_ARG;
+    for (int b = 0; b < B; ++b) {
+        int n = n_nodes[b];
+        int32_t depth[64];
+        uint64_t anc[64];
+        if (n < 1 || n > N) return ORC_ERR_TOPOLOGY;
+        int rc = orc_tree_topology(n, parent + (size_t)b * N, depth, anc);
+        if (rc != ORC_OK) return rc;
+        for (int i = 0; i < n; ++i)
+            for (int c = 0; c < C; ++c) {
+                double acc = 0.0;
+                /* walk back from node i: window position j = K-1, K-2, ... */
+                int node = i, before_root = 0;
+                for (int j = K - 1; j >= 0; --j) {
+                    double v;
+                    if (node >= 0) {
+                        v = orc_bf16_to_double(x[((size_t)b * N + node) * C + c]);
+                        node = parent[(size_t)b * N + node];
+                    } else {
+                        /* the (before_root+1)-th input before the root */
+                        v = orc_bf16_to_double(state[((size_t)b * (K - 1) + (K - 2 - before_root)) * C + c]);
+                        ++before_root;
+                    }
+                    acc += (double)w[(size_t)c * K + j] * v;
+                }
+                out[((size_t)b * N + i) * C + c] = (float)acc;
+            }
+    }
+    return ORC_OK;
+}
+
+int orc_conv_commit(int B, int N, int C, int K, const uint16_t* x, const int32_t* path,
+                    const int32_t* path_len, uint16_t* state) {
+    if (B < 1 || N < 1 || C < 1 || K < 2) return ORC_ERR_ARG;
+    uint16_t* seq = malloc((size_t)(K - 1 + N) * sizeof(uint16_t));
+    for (int b = 0; b < B; ++b) {
+        int L = path_len[b];
+        if (L < 0 || L > N) { free(seq); return ORC_ERR_ARG; }
+        for (int m = 0; m < L; ++m) {
+            int p = path[(size_t)b * N + m];
+            if (p < 0 || p >= N) { free(seq); return ORC_ERR_ARG; }
+        }
+        for (int c = 0; c < C; ++c) {
+            /* the sequence [state ; x of the path], then its last K-1 entries */
+            for (int t = 0; t < K - 1; ++t) seq[t] = state[((size_t)b * (K - 1) + t) * C + c];
+            for (int m = 0; m < L; ++m) seq[K - 1 + m] = x[((size_t)b * N + path[(size_t)b * N + m]) * C + c];
+            for (int t = 0; t < K - 1; ++t) state[((size_t)b * (K - 1) + t) * C + c] = seq[L + t];
+        }
+    }
+    free(seq);
+    return ORC_OK;
+}

@@ -26,6 +26,12 @@
  *   - Commit / rollback ("How it works", "Per-step rollback"): after accept
  *     the recurrent state and KV cache equal those of decoding only the
  *     accepted path.
+ *   - The tree-aware short convolution before a gated-DeltaNet layer ("How
+ *     it works": ggml_ssm_conv_tree reads each node's K-1 window along the
+ *     parent chain; the conv window is part of the rolled-back state).  The
+ *     pages do not write the op; the oracle uses a depthwise causal conv
+ *     (tap K-1 on the current token, no bias, no activation) and commits the
+ *     window of the accepted path.
  *
  * Precision: fp64 arithmetic for everything the method computes in floating
  * point; the committed recurrent state is stored as fp32 between steps.  The
@@ -126,6 +132,25 @@ int orc_tree_attn_verify(int B, int N, int Hq, int Hkv, int D, int cap, int wind
 int orc_accept_greedy(int B, int N, int V, const float* logits, const int32_t* tokens,
                       const int32_t* parent, const int32_t* n_nodes,
                       int32_t* path, int32_t* path_len, int32_t* next_token, int32_t* best);
+
+/* ---- tree-aware short convolution ---- */
+/* Depthwise causal convolution of width K over the tree ("Luce DFlash"
+ * README, "How it works": ggml_ssm_conv_tree, each node reads its K-1 window
+ * along the DDTree parent chain).  Window position K-1 is node i itself,
+ * K-2 its parent, and so on; once the chain has passed the root, the
+ * positions read the conv state, the K-1 inputs before the root (state
+ * entry K-2 just before the root, entry 0 the oldest):
+ *   out[b][i][c] = sum_{j<K} w[c][j] * window_j[c].
+ * x [B][N][C] and state [B][K-1][C] are bf16 bits, w [C][K] f32, out
+ * [B][N][C] f32 (fp64 sums). */
+int orc_tree_conv_verify(int B, int N, int C, int K, const int32_t* parent, const int32_t* n_nodes,
+                         const uint16_t* x, const uint16_t* state, const float* w, float* out);
+
+/* Conv state commit: the state becomes the last K-1 entries of the sequence
+ * [state ; x of path[b][0..L)], i.e. what decoding the accepted nodes in
+ * order would leave behind. */
+int orc_conv_commit(int B, int N, int C, int K, const uint16_t* x, const int32_t* path,
+                    const int32_t* path_len, uint16_t* state);
 
 /* ---- KV commit: move slot P+path[m] to P+m for m < L (all reads first) ---- */
 int orc_kv_commit(int B, int N, int Hkv, int D, int cap, int kv_type,

@@ -11,6 +11,8 @@ Workloads (the pages give the model geometry; the draws are synthetic):
   * gated-DeltaNet layer of a 27B-class hybrid target: 16 q/k heads, 48 v
     heads, dk = dv = 128 ("Luce DFlash" README, "Architecture note": 64
     layers, every 4th full attention, the rest Gated DeltaNet);
+  * the short convolution over that layer's q/k/v channels (10240
+    channels, width 4: a reading, the pages name the op but not its sizes);
   * full-attention layer: 24 query heads, 4 KV heads, head size 256 (same
     section), over a q8_0 / q4_0 KV cache ("Asymmetric K/V quantization");
   * draft trees built best-first over top-K branches with a rank-0 chain
@@ -27,6 +29,10 @@ KV_Q8_0, KV_Q4_0, KV_F32 = 0, 1, 2
 
 GDN_27B = dict(Hk=16, Hv=48, dk=128, dv=128)
 ATTN_27B = dict(Hq=24, Hkv=4, D=256)
+# The short convolution in front of that gated-DeltaNet layer runs over its
+# q, k and v channels together (2*16*128 + 48*128); the pages give neither
+# the channel count nor the width, the width 4 is the common choice.
+CONV_27B = dict(C=2 * 16 * 128 + 48 * 128, K=4)
 
 
 # ------------------------------------------------------------------ encodings
@@ -178,6 +184,17 @@ def gdn_inputs(rng, B, N, Hk, Hv, dk, dv, state_std=0.02, state=True):
     if state:
         out["state"] = (rng.standard_normal((B, Hv, dv, dk), dtype=np.float32) * state_std).astype(np.float32)
     return out
+
+
+# ------------------------------------------------------------------ short convolution
+def conv_inputs(rng, B, N, C, K, w_std=0.5):
+    """Tree-conv inputs: x [B][N][C] and the conv state [B][K-1][C] as bf16
+    ~ N(0, 1), weights [C][K] fp32 ~ N(0, w_std)."""
+    return dict(
+        x=bf16_bits(rng.standard_normal((B, N, C), dtype=np.float32)),
+        state=bf16_bits(rng.standard_normal((B, K - 1, C), dtype=np.float32)),
+        w=(rng.standard_normal((C, K), dtype=np.float32) * w_std).astype(np.float32),
+    )
 
 
 # ------------------------------------------------------------------ attention layer
