@@ -44,6 +44,7 @@ N_LAYERS, N_GDN, N_ATTN = 64, 48, 16
 BUDGET, VOCAB, CTX, WINDOW, PLANT = 22, 151936, 32768, 2048, 8
 GDN = synth.GDN_27B
 ATT = synth.ATTN_27B
+CONV = synth.CONV_27B
 SEED = 1234 + 3
 WORKLOAD = ("64-layer hybrid verify step: 48 gated-DeltaNet layers (16 qk / 48 v heads, dk=dv=128) + "
             "16 attention layers (24 q / 4 kv heads, D=256, q8_0 KV 32768 tokens, window 2048), "
@@ -75,8 +76,13 @@ def make_host_inputs(rng, n_layers=N_LAYERS):
             layers.append(("attn", a))
         else:
             layers.append(("gdn", synth.gdn_inputs(rng, 1, BUDGET, **GDN)))
+    # the short convolution in front of every GDN layer (measured beside the
+    # step, not inside it); drawn from its own stream so the step's inputs
+    # stay the same
+    crng = np.random.default_rng(SEED + 7919)
+    conv = [synth.conv_inputs(crng, 1, BUDGET, CONV["C"], CONV["K"]) for kind, _ in layers if kind == "gdn"]
     return dict(parent=parent, n_nodes=n_nodes, tokens=tokens, logits=logits, layers=layers, cap=cap,
-                planted=planted)
+                planted=planted, conv=conv)
 
 
 # ---------------------------------------------------------------------------- algorithmic bytes
@@ -105,6 +111,19 @@ def attn_bytes():
     new = 2 * N * Hkv * D * 2
     tree = 2 * 2 * N * Hkv * row               # tree slots written, then read
     return kv + q + out + new + tree
+
+
+def conv_bytes():
+    """One tree conv: x read, conv state read, taps read, output written."""
+    C, K, N = CONV["C"], CONV["K"], BUDGET
+    return N * C * 2 + (K - 1) * C * 2 + C * K * 4 + N * C * 4
+
+
+def conv_commit_bytes(L):
+    """Conv-state commit of all GDN layers: K-1 rows gathered from the state
+    and the accepted inputs, K-1 rows written."""
+    C, K = CONV["C"], CONV["K"]
+    return N_GDN * 2 * (K - 1) * C * 2 if L else 0
 
 
 def accept_bytes():
@@ -296,6 +315,15 @@ class GpuStep:
                 self.caches.append(L["kv"])
             self.layers.append(L)
         self.launches_per_step = N_GDN + N_ATTN + 2 + 2  # accept and commit: two kernels each
+        # ---- the short convolution of every GDN layer (measured beside the step)
+        self.conv_desc = dflv.conv_desc(1, N, CONV["C"], CONV["K"])
+        self.conv_desc_next = dflv.conv_desc(1, N, CONV["C"], CONV["K"], early)
+        self.conv = []
+        for d in host["conv"]:
+            c = {k: t.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).to(dev) for k, v in d.items()}
+            c["state0"] = c["state"].clone()
+            c["out"] = t.empty((1, N, CONV["C"]), device=dev)
+            self.conv.append(c)
 
     # one pass of the hot path: every layer's verify (the GDN layers first
     # commit the previous step's accepted path into their state: deferred
@@ -327,6 +355,17 @@ class GpuStep:
             s.copy_(s0)
         self.n_past.fill_(CTX)
         self.path_len.zero_()  # nothing pending
+        for c in self.conv:
+            c["state"].copy_(c["state0"])
+
+    def conv_verify(self, i):
+        c = self.conv[i]
+        return self.dflv.dflv_tree_conv_verify(self.conv_desc if i == 0 else self.conv_desc_next, self.parent,
+                                               self.n_nodes, c["x"], c["state"], c["w"], c["out"], self.status)
+
+    def conv_commit(self):
+        return self.dflv.dflv_conv_commit(self.conv_desc, len(self.conv), [c["state"] for c in self.conv],
+                                          [c["x"] for c in self.conv], self.path, self.path_len, self.status)
 
 
 def kernel_chain_ms(S, torch, stream, steps, warmup):
@@ -352,9 +391,16 @@ def kernel_chain_ms(S, torch, stream, steps, warmup):
         chk(dflv.dflv_commit_rollback(None, 0, [], [], S.attn_desc, len(S.caches), S.caches, S.path, S.path_len,
                                       S.n_past, S.status), "commit")
 
+    def conv_chain():
+        for i in range(len(S.conv)):
+            chk(S.conv_verify(i), "conv verify")
+
+    def conv_commit():
+        chk(S.conv_commit(), "conv commit")
+
     out = {}
     for name, fn, n in (("gdn", gdn_chain, N_GDN), ("attn", attn_chain, N_ATTN), ("accept", accept, 1),
-                        ("commit", commit, 1)):
+                        ("commit", commit, 1), ("conv", conv_chain, N_GDN), ("conv_commit", conv_commit, 1)):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             fn()
@@ -549,6 +595,14 @@ def profile_one(kind, launches):
     host = make_host_inputs(rng, n_layers=4)
     S = GpuStep(host, torch, dflv)
     li, L = next((i, L) for i, L in enumerate(S.layers) if L["kind"] == ("attn" if kind == "attn" else "gdn"))
+    if kind in ("conv", "conv_commit"):
+        S.step(1)
+        torch.cuda.synchronize()
+        for _ in range(launches):
+            dflv.check(S.conv_verify(0) if kind == "conv" else S.conv_commit())
+        torch.cuda.synchronize()
+        print(json.dumps({"kernel": kind, "launches": launches, "status": int(S.status.item())}))
+        return
     # one step first: both factor sets written and an accepted path pending
     S.step(1)
     S.n_past.fill_(CTX)
@@ -576,7 +630,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel", choices=["gdn", "attn", "accept", "commit"], default=None,
+    ap.add_argument("--kernel", choices=["gdn", "attn", "accept", "commit", "conv", "conv_commit"], default=None,
                     help="profiling mode: launch one kernel of the step --launches times on its "
                          "single-layer workload and exit (for ncu captures)")
     ap.add_argument("--launches", type=int, default=3)
@@ -618,10 +672,18 @@ def main():
     peak, peak_kind = hbm_peak()
     per = r["per"] or {}
     L = r["L"]
-    ab = dict(gdn=gdn_bytes(L), attn=attn_bytes(), accept=accept_bytes(), commit=commit_bytes(L))
+    ab = dict(gdn=gdn_bytes(L), attn=attn_bytes(), accept=accept_bytes(), commit=commit_bytes(L),
+              conv=conv_bytes(), conv_commit=conv_commit_bytes(L))
     launches = dict(gdn=N_GDN, attn=N_ATTN, accept=1, commit=1)
     # dominant kernel: the largest share of the step
-    shares = {k: per[k] * launches[k] for k in per} if per else {}
+    shares = {k: per[k] * launches[k] for k in per if k in launches} if per else {}
+    beside = {}
+    for k in ("conv", "conv_commit"):
+        if per.get(k):
+            gbs = ab[k] / (per[k] * 1e-3) / 1e9
+            beside[k] = {"ms_per_launch": per[k], "algorithmic_bytes_per_launch": ab[k], "achieved": gbs,
+                         "unit": "GB/s", "frac": gbs / peak,
+                         "launches": N_GDN if k == "conv" else 1}
     dom = max(shares, key=shares.get) if shares else "commit"
     dur_ms = per.get(dom)
     achieved = ab[dom] / (dur_ms * 1e-3) / 1e9 if dur_ms else None
@@ -645,6 +707,10 @@ def main():
                                       "CUDA events on the launching stream",
                      "traffic": profiled_traffic(dom)},
         "kernels_ms_per_launch": per,
+        "beside_the_step": {"what": "the short convolution in front of each GDN layer (48 tree-conv launches "
+                                    "back to back, C=10240, K=4) and the commit of its window (one launch, 48 "
+                                    "layers); timed like the step's kernels, not part of the step",
+                            **beside},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
         "gpu_launches": r["launches"] * args.steps,
         "clocks": r["clocks"],

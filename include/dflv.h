@@ -29,6 +29,9 @@
  *   - Commit / rollback leaves the recurrent state and KV cache as if only
  *     the accepted path had been decoded ([README] "How it works",
  *     "Per-step rollback"; [PR606] review note naming the commit routines).
+ *   - The short convolution in front of each gated-DeltaNet layer reads
+ *     each node's window along its parent chain ([README] "How it works":
+ *     ggml_ssm_conv_tree).
  *
  * General conventions
  *   - Every array argument is a DEVICE pointer unless marked "host".  The
@@ -181,6 +184,62 @@ dflv_status dflv_tree_gdn_verify_pending(const dflv_gdn_desc* desc, const int32_
                                          dflv_stream_t stream);
 
 size_t dflv_gdn_workspace_size(const dflv_gdn_desc* desc);
+
+/* ------------------------------------------------------------------------ */
+/* Short convolution in front of a gated-DeltaNet layer                      */
+/* ------------------------------------------------------------------------ */
+
+/* The depthwise causal convolution of width K that feeds a gated-DeltaNet
+ * layer, evaluated on the tree ([README] "How it works": ggml_ssm_conv_tree,
+ * each node reads its K-1 window along the parent chain).  The pages name
+ * the op but do not write it; this library computes, per channel c,
+ *     out[b][i][c] = sum_{j<K} weight[c][j] * w_j,
+ * where w_{K-1} is node i's own input, w_{K-2} its parent's, and so on up
+ * the parent chain; once the chain has passed the root, w continues with
+ * the conv state (the K-1 inputs before the root, newest last).  No bias and
+ * no activation (the caller applies those).  A chain tree therefore gives
+ * the sequential causal convolution.
+ * Supported: 1 <= N_max <= 64, 2 <= K <= 8, C a multiple of 4. */
+typedef struct {
+    int32_t B, N_max, C, K;
+    uint32_t flags; /* 0 or DFLV_FLAG_EARLY_PREFETCH */
+} dflv_conv_desc;
+
+/* Tree verify of one short-convolution layer.
+ *   parent     [B][N_max] int32; n_nodes [B] int32
+ *   x          [B][N_max][C] bf16: the nodes' inputs (the layer's q/k/v
+ *              projections before the convolution)
+ *   conv_state [B][K-1][C] bf16: the committed window, oldest first; READ
+ *              ONLY here
+ *   weight     [C][K] f32: tap K-1 multiplies the current node
+ *   out        [B][N_max][C] f32; rows of padded nodes are not written
+ * With DFLV_FLAG_EARLY_PREFETCH the tree, weight and conv_state are read
+ * before the dependency wait (x after it).  A malformed tree raises
+ * DFLV_DEV_TOPOLOGY and that sequence writes nothing. */
+dflv_status dflv_tree_conv_verify(const dflv_conv_desc* desc, const int32_t* parent,
+                                  const int32_t* n_nodes, const uint16_t* x,
+                                  const uint16_t* conv_state, const float* weight, float* out,
+                                  int32_t* status_dev, dflv_stream_t stream);
+
+/* Commits the accepted path into the conv state of n_layers layers in one
+ * launch: each state becomes the last K-1 entries of
+ * [conv_state ; x of path[b][0..L)], the window that decoding only the
+ * accepted tokens leaves behind ([README] "How it works", per-step rollback
+ * of the recurrent state).
+ *   states  host array of n_layers device pointers, [B][K-1][C] bf16 (in/out)
+ *   xs      host array of n_layers device pointers, [B][N_max][C] bf16: the
+ *           inputs that layer's verify read
+ *   path, path_len  [B][N_max], [B] int32 (dflv_accept_greedy output);
+ *           path_len[b] = 0 leaves sequence b unchanged; a length outside
+ *           [0, N_max] or a node outside [0, N_max) raises DFLV_DEV_PATH
+ *           and that sequence is left unchanged.
+ * 1 <= n_layers <= DFLV_MAX_CONV_LAYERS.  All reads of a state precede its
+ * writes (each thread owns its channels). */
+dflv_status dflv_conv_commit(const dflv_conv_desc* desc, int32_t n_layers, uint16_t* const* states,
+                             const uint16_t* const* xs, const int32_t* path,
+                             const int32_t* path_len, int32_t* status_dev, dflv_stream_t stream);
+
+#define DFLV_MAX_CONV_LAYERS 128
 
 /* ------------------------------------------------------------------------ */
 /* Attention layer                                                           */

@@ -94,6 +94,14 @@ dflv_status fill_gdn_args(const dflv_gdn_desc* desc, const int32_t* parent, cons
     return DFLV_OK;
 }
 
+dflv_status check_conv_desc(const dflv_conv_desc* d) {
+    if (!d) return DFLV_ERR_INVALID_ARG;
+    if (d->B < 1 || d->N_max < 1 || d->C < 1 || d->K < 1) return DFLV_ERR_INVALID_ARG;
+    if (d->flags & ~(uint32_t)DFLV_FLAG_EARLY_PREFETCH) return DFLV_ERR_INVALID_ARG;
+    if (d->N_max > 64 || d->K < 2 || d->K > 8 || d->C % 4 != 0) return DFLV_ERR_UNSUPPORTED;
+    return DFLV_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -298,6 +306,62 @@ dflv_status dflv_commit_rollback(const dflv_gdn_desc* gdn, int32_t n_gdn, float*
     a.B = B;
     a.N_max = N_max;
     return from_cuda(dflv::launch_commit_rollback(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"
+
+extern "C" {
+
+dflv_status dflv_tree_conv_verify(const dflv_conv_desc* desc, const int32_t* parent,
+                                  const int32_t* n_nodes, const uint16_t* x,
+                                  const uint16_t* conv_state, const float* weight, float* out,
+                                  int32_t* status_dev, dflv_stream_t stream) {
+    dflv_status s = check_conv_desc(desc);
+    if (s != DFLV_OK) return s;
+    if (!parent || !n_nodes || !x || !conv_state || !weight || !out || !status_dev) return DFLV_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(conv_state) || !aligned16(weight) || !aligned16(out) || !aligned4(parent) ||
+        !aligned4(n_nodes) || !aligned4(status_dev))
+        return DFLV_ERR_INVALID_ARG;
+    dflv::ConvVerifyArgs a;
+    a.B = desc->B;
+    a.N_max = desc->N_max;
+    a.C = desc->C;
+    a.K = desc->K;
+    a.flags = desc->flags;
+    a.parent = parent;
+    a.n_nodes = n_nodes;
+    a.x = x;
+    a.state = conv_state;
+    a.w = weight;
+    a.out = out;
+    a.status = status_dev;
+    return from_cuda(dflv::launch_conv_tree_verify(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dflv_status dflv_conv_commit(const dflv_conv_desc* desc, int32_t n_layers, uint16_t* const* states,
+                             const uint16_t* const* xs, const int32_t* path,
+                             const int32_t* path_len, int32_t* status_dev, dflv_stream_t stream) {
+    dflv_status s = check_conv_desc(desc);
+    if (s != DFLV_OK) return s;
+    if (n_layers < 1 || n_layers > DFLV_MAX_CONV_LAYERS || !states || !xs || !path || !path_len || !status_dev)
+        return DFLV_ERR_INVALID_ARG;
+    if (!aligned4(path) || !aligned4(path_len) || !aligned4(status_dev)) return DFLV_ERR_INVALID_ARG;
+    static_assert(DFLV_MAX_CONV_LAYERS == dflv::kMaxConvLayers, "layer limits differ");
+    dflv::ConvCommitArgs a = {};
+    a.B = desc->B;
+    a.N_max = desc->N_max;
+    a.C = desc->C;
+    a.K = desc->K;
+    a.n_layers = n_layers;
+    a.path = path;
+    a.path_len = path_len;
+    a.status = status_dev;
+    for (int l = 0; l < n_layers; ++l) {
+        if (!states[l] || !xs[l] || !aligned16(states[l]) || !aligned16(xs[l])) return DFLV_ERR_INVALID_ARG;
+        a.state[l] = states[l];
+        a.x[l] = xs[l];
+    }
+    return from_cuda(dflv::launch_conv_commit(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -107,4 +107,32 @@ struct CommitArgs {
 
 cudaError_t launch_commit_rollback(const CommitArgs& a, cudaStream_t stream);
 
+struct ConvVerifyArgs {
+    int B, N_max, C, K;
+    unsigned flags;  // DFLV_FLAG_*
+    const int32_t* parent;
+    const int32_t* n_nodes;
+    const uint16_t* x;
+    const uint16_t* state;
+    const float* w;
+    float* out;
+    int32_t* status;
+};
+
+cudaError_t launch_conv_tree_verify(const ConvVerifyArgs& a, cudaStream_t stream);
+
+constexpr int kMaxConvLayers = 128;
+
+// Passed by value as a kernel parameter (2 KB of pointers).
+struct ConvCommitArgs {
+    int B, N_max, C, K, n_layers;
+    const int32_t* path;
+    const int32_t* path_len;
+    int32_t* status;
+    uint16_t* state[kMaxConvLayers];
+    const uint16_t* x[kMaxConvLayers];
+};
+
+cudaError_t launch_conv_commit(const ConvCommitArgs& a, cudaStream_t stream);
+
 }  // namespace dflv

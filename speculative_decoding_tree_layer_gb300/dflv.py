@@ -23,6 +23,7 @@ DFLV_DEV_TOPOLOGY, DFLV_DEV_CAPACITY, DFLV_DEV_PATH, DFLV_DEV_TIMEOUT = 1, 2, 4,
 DFLV_KV_Q8_0, DFLV_KV_Q4_0, DFLV_KV_F32 = 0, 1, 2
 DFLV_FLAG_EARLY_PREFETCH = 1
 DFLV_MAX_COMMIT_GDN_LAYERS, DFLV_MAX_COMMIT_ATTN_LAYERS = 128, 64
+DFLV_MAX_CONV_LAYERS = 128
 
 _c_i32 = ctypes.c_int32
 _vp = ctypes.c_void_p
@@ -45,6 +46,10 @@ class dflv_attn_desc(ctypes.Structure):
 
 class dflv_kv_layer(ctypes.Structure):
     _fields_ = [("kq", _vp), ("vq", _vp), ("ks", _vp), ("vs", _vp)]
+
+
+class dflv_conv_desc(ctypes.Structure):
+    _fields_ = [("B", _c_i32), ("N_max", _c_i32), ("C", _c_i32), ("K", _c_i32), ("flags", ctypes.c_uint32)]
 
 
 class DflvError(RuntimeError):
@@ -76,6 +81,8 @@ def load():
     lib.dflv_commit_rollback.argtypes = [ctypes.POINTER(dflv_gdn_desc), _c_i32, P, ctypes.POINTER(dflv_gdn_factors),
                                          ctypes.POINTER(dflv_attn_desc), _c_i32, ctypes.POINTER(dflv_kv_layer),
                                          P, P, P, P, P]
+    lib.dflv_tree_conv_verify.argtypes = [ctypes.POINTER(dflv_conv_desc)] + [P] * 7 + [P]
+    lib.dflv_conv_commit.argtypes = [ctypes.POINTER(dflv_conv_desc), _c_i32, P, P, P, P, P, P]
     lib.dflv_gdn_workspace_size.argtypes = [ctypes.POINTER(dflv_gdn_desc)]
     lib.dflv_gdn_workspace_size.restype = S
     lib.dflv_attn_workspace_size.argtypes = [ctypes.POINTER(dflv_attn_desc)]
@@ -83,7 +90,7 @@ def load():
     lib.dflv_status_string.argtypes = [ctypes.c_int]
     lib.dflv_status_string.restype = ctypes.c_char_p
     for f in ("dflv_tree_gdn_verify", "dflv_tree_gdn_verify_pending", "dflv_tree_attn_verify", "dflv_accept_greedy",
-              "dflv_commit_rollback"):
+              "dflv_commit_rollback", "dflv_tree_conv_verify", "dflv_conv_commit"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -185,6 +192,24 @@ def dflv_commit_rollback(gdn, n_gdn, states, factors, attn, n_attn, caches, path
         ctypes.byref(gdn) if gdn is not None else None, n_gdn, ctypes.cast(st, ctypes.c_void_p), fa,
         ctypes.byref(attn) if attn is not None else None, n_attn, ca, _ptr(path), _ptr(path_len),
         _ptr(n_past), _ptr(status_dev), _stream(stream))
+
+
+def conv_desc(B, N_max, C, K, flags=0):
+    return dflv_conv_desc(B, N_max, C, K, flags)
+
+
+def dflv_tree_conv_verify(desc, parent, n_nodes, x, conv_state, weight, out, status_dev, stream=None) -> int:
+    return load().dflv_tree_conv_verify(ctypes.byref(desc), _ptr(parent), _ptr(n_nodes), _ptr(x), _ptr(conv_state),
+                                        _ptr(weight), _ptr(out), _ptr(status_dev), _stream(stream))
+
+
+def dflv_conv_commit(desc, n_layers, states, xs, path, path_len, status_dev, stream=None) -> int:
+    """``states``, ``xs``: sequences of tensors (or addresses), one per layer."""
+    st = (ctypes.c_void_p * max(1, n_layers))(*[_ptr(s) for s in states][:n_layers])
+    xa = (ctypes.c_void_p * max(1, n_layers))(*[_ptr(x) for x in xs][:n_layers])
+    return load().dflv_conv_commit(ctypes.byref(desc), n_layers, ctypes.cast(st, ctypes.c_void_p),
+                                   ctypes.cast(xa, ctypes.c_void_p), _ptr(path), _ptr(path_len), _ptr(status_dev),
+                                   _stream(stream))
 
 
 def dflv_gdn_workspace_size(desc) -> int:

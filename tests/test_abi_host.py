@@ -19,7 +19,7 @@ def test_exports_every_declared_symbol(lib):
     names = dflv.header_symbols()
     assert set(names) >= {"dflv_tree_gdn_verify", "dflv_tree_attn_verify", "dflv_accept_greedy",
                           "dflv_commit_rollback", "dflv_gdn_workspace_size", "dflv_attn_workspace_size",
-                          "dflv_status_string"}
+                          "dflv_status_string", "dflv_tree_conv_verify", "dflv_conv_commit"}
     for n in names:
         assert hasattr(lib, n), n
 
@@ -93,3 +93,27 @@ def test_accept_and_commit_host_validation(lib):
     a = dflv.attn_desc(2, 22, 24, 4, 256, 40000, 0, 0, 0.0625)
     assert dflv.dflv_commit_rollback(g, 1, [P], [fac], a, 1, [dflv.dflv_kv_layer(P, P, P, P)], P, P, P, P,
                                      stream=0) == dflv.DFLV_ERR_INVALID_ARG   # batch mismatch
+
+
+def test_conv_host_validation(lib):
+    P = 16
+
+    def call(desc, **over):
+        args = dict(parent=P, n_nodes=P, x=P, conv_state=P, weight=P, out=P, status_dev=P)
+        args.update(over)
+        return dflv.dflv_tree_conv_verify(desc, stream=0, **args)
+
+    ok = dflv.conv_desc(1, 22, 10240, 4)
+    assert call(dflv.conv_desc(1, 22, 10, 4)) == dflv.DFLV_ERR_UNSUPPORTED      # C not a multiple of 4
+    assert call(dflv.conv_desc(1, 22, 16, 9)) == dflv.DFLV_ERR_UNSUPPORTED      # K > 8
+    assert call(dflv.conv_desc(1, 22, 16, 1)) == dflv.DFLV_ERR_UNSUPPORTED      # K < 2
+    assert call(dflv.conv_desc(1, 65, 16, 4)) == dflv.DFLV_ERR_UNSUPPORTED
+    assert call(dflv.conv_desc(0, 22, 16, 4)) == dflv.DFLV_ERR_INVALID_ARG
+    assert call(dflv.conv_desc(1, 22, 16, 4, 2)) == dflv.DFLV_ERR_INVALID_ARG   # unknown flag
+    assert call(ok, x=None) == dflv.DFLV_ERR_INVALID_ARG
+    assert call(ok, x=24) == dflv.DFLV_ERR_INVALID_ARG                          # misaligned
+    assert call(ok, parent=18) == dflv.DFLV_ERR_INVALID_ARG
+    assert dflv.dflv_conv_commit(ok, 0, [], [], P, P, P, stream=0) == dflv.DFLV_ERR_INVALID_ARG
+    assert dflv.dflv_conv_commit(ok, 129, [P] * 129, [P] * 129, P, P, P, stream=0) == dflv.DFLV_ERR_INVALID_ARG
+    assert dflv.dflv_conv_commit(ok, 2, [P, None], [P, P], P, P, P, stream=0) == dflv.DFLV_ERR_INVALID_ARG
+    assert dflv.dflv_conv_commit(ok, 1, [P], [24], P, P, P, stream=0) == dflv.DFLV_ERR_INVALID_ARG
