@@ -8,11 +8,13 @@
 //     out[i][c] = sum_{j<K} w[c][j] * win_j(i)[c],  win_{K-1}(i) = x_i,
 //     win_{K-1-d}(i) = x of the d-th ancestor, or state[K-1+depth(i)-d].
 // The work is a few multiply-adds per byte, so the kernel is a memory
-// stream: every input byte is read once (x rows into shared memory, taps and
-// the state into registers) and every output written once with coalesced
-// 8/16-byte accesses.  One thread owns 4 channels of one sequence for all
-// nodes; the window table (which shared-memory row feeds which tap of which
-// node) is built once per CTA from the parent array and read as a warp-wide
+// stream: every input byte is read once from HBM (x and state rows into
+// shared memory, taps into registers) and every output written once with
+// coalesced 8/16-byte accesses.  A CTA owns 128 channels of one sequence;
+// its 8 warps split the nodes (warp q takes nodes q, q+8, ...), so a
+// thread's serial work is a few nodes rather than the whole tree.  The
+// window table (which shared-memory row feeds which tap of which node) is
+// built once per CTA from the parent array and read as a warp-wide
 // broadcast.
 //
 // The commit leaves the state that decoding only the accepted path would
@@ -27,9 +29,13 @@ namespace dflv {
 
 namespace {
 
-constexpr int kConvThreads = 64;
-constexpr int kConvCh = 4;                            // channels per thread: one 8-byte bf16x4 access
-constexpr int kConvBlockCh = kConvThreads * kConvCh;  // channels per CTA
+constexpr int kConvLanes = 32;                       // channel lanes of a CTA
+constexpr int kConvCh = 4;                           // channels per lane: one 8-byte bf16x4 access
+constexpr int kConvGroups = 8;                       // node groups: lane l of group q takes nodes q, q+8, ...
+constexpr int kConvThreads = kConvLanes * kConvGroups;
+constexpr int kConvBlockCh = kConvLanes * kConvCh;   // channels per CTA
+constexpr int kCommitThreads = 64;
+constexpr int kCommitBlockCh = kCommitThreads * kConvCh;
 
 DFLV_DEVINL void cp_async8(void* dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
@@ -42,18 +48,23 @@ DFLV_DEVINL void bf16x4_to_float(uint2 v, float (&f)[4]) {
     f[3] = __uint_as_float(v.y & 0xffff0000u);
 }
 
-// grid (ceil(C / 256), B), 64 threads.  Dynamic shared memory: the x rows of
-// the CTA's channels for nodes [0, N_max), then the K-1 state rows, each row
-// one uint2 per thread.
+// grid (ceil(C / 128), B), 256 threads = 32 channel lanes x 8 node groups.
+// Dynamic shared memory: the x rows of the CTA's channels for nodes
+// [0, N_max), then the K-1 state rows; a row is one uint2 per lane.  Every
+// thread copies the rows of its own nodes (and group s < K-1 state row s);
+// after one barrier any thread reads any row, since a node's window reaches
+// into other groups' nodes.
 template <int K>
 __global__ void __launch_bounds__(kConvThreads) conv_tree_verify_kernel(const ConvVerifyArgs a) {
+    static_assert(K - 1 <= kConvGroups, "one node group per state row");
     __shared__ int32_t par_s[kMaxNodes];
     __shared__ int32_t depth_s[kMaxNodes];
     __shared__ uint64_t amask_s[kMaxNodes];
     __shared__ int32_t win_s[kMaxNodes][K];  // win_s[i][d]: row feeding ancestor distance d
     extern __shared__ uint2 rows_s[];
-    const int tid = threadIdx.x, b = blockIdx.y, N = a.N_max, C = a.C;
-    const int c0 = blockIdx.x * kConvBlockCh + tid * kConvCh;
+    const int tid = threadIdx.x, lane = tid % kConvLanes, grp = tid / kConvLanes;
+    const int b = blockIdx.y, N = a.N_max, C = a.C;
+    const int c0 = blockIdx.x * kConvBlockCh + lane * kConvCh;
     const bool active = c0 < C;
     const bool early = (a.flags & DFLV_FLAG_EARLY_PREFETCH) != 0;
     if (!early) grid_dependency_wait();
@@ -76,9 +87,8 @@ __global__ void __launch_bounds__(kConvThreads) conv_tree_verify_kernel(const Co
         for (int j = 0; j < K; ++j)
 #pragma unroll
             for (int cc = 0; cc < kConvCh; ++cc) w[j][cc] = t[cc * K + j];
-#pragma unroll
-        for (int s = 0; s < K - 1; ++s)
-            cp_async8(rows_s + (N + s) * kConvThreads + tid, a.state + ((size_t)b * (K - 1) + s) * C + c0);
+        if (grp < K - 1)
+            cp_async8(rows_s + (N + grp) * kConvLanes + lane, a.state + ((size_t)b * (K - 1) + grp) * C + c0);
     }
     const int n = __ldg(a.n_nodes + b);
     if (!block_tree_topology(a.parent + (size_t)b * N, n, N, par_s, depth_s, amask_s, a.status)) {
@@ -102,20 +112,21 @@ __global__ void __launch_bounds__(kConvThreads) conv_tree_verify_kernel(const Co
     if (early) grid_dependency_wait();
     grid_launch_dependents();
 
-    // The nodes' inputs: all rows in flight at once.
+    // The nodes' inputs, all in flight at once.
     if (active)
-        for (int i = 0; i < n; ++i)
-            cp_async8(rows_s + i * kConvThreads + tid, a.x + ((size_t)b * N + i) * C + c0);
+        for (int i = grp; i < n; i += kConvGroups)
+            cp_async8(rows_s + i * kConvLanes + lane, a.x + ((size_t)b * N + i) * C + c0);
     cp_async_commit();
-    __syncthreads();  // win_s
     cp_async_wait<0>();
+    __syncthreads();  // rows_s and win_s
     if (!active) return;
-    for (int i = 0; i < n; ++i) {
+#pragma unroll 2
+    for (int i = grp; i < n; i += kConvGroups) {
         float acc[kConvCh] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int j = 0; j < K; ++j) {
             float f[kConvCh];
-            bf16x4_to_float(rows_s[win_s[i][K - 1 - j] * kConvThreads + tid], f);
+            bf16x4_to_float(rows_s[win_s[i][K - 1 - j] * kConvLanes + lane], f);
 #pragma unroll
             for (int cc = 0; cc < kConvCh; ++cc) acc[cc] = fmaf(w[j][cc], f[cc], acc[cc]);
         }
@@ -126,10 +137,10 @@ __global__ void __launch_bounds__(kConvThreads) conv_tree_verify_kernel(const Co
 
 // grid (ceil(C / 256), B, n_layers), 64 threads.
 template <int K>
-__global__ void __launch_bounds__(kConvThreads) conv_commit_kernel(const ConvCommitArgs a) {
+__global__ void __launch_bounds__(kCommitThreads) conv_commit_kernel(const ConvCommitArgs a) {
     grid_dependency_wait();
     const int tid = threadIdx.x, b = blockIdx.y, layer = blockIdx.z, N = a.N_max, C = a.C;
-    const int c0 = blockIdx.x * kConvBlockCh + tid * kConvCh;
+    const int c0 = blockIdx.x * kCommitBlockCh + tid * kConvCh;
     const int L = __ldg(a.path_len + b);
     bool bad = L < 0 || L > N;
     if (!bad)
@@ -163,14 +174,14 @@ __global__ void __launch_bounds__(kConvThreads) conv_commit_kernel(const ConvCom
 template <int K>
 cudaError_t launch_verify_k(const ConvVerifyArgs& a, cudaStream_t stream) {
     const dim3 grid((a.C + kConvBlockCh - 1) / kConvBlockCh, a.B);
-    const size_t smem = (size_t)(a.N_max + K - 1) * kConvThreads * sizeof(uint2);
+    const size_t smem = (size_t)(a.N_max + K - 1) * kConvLanes * sizeof(uint2);
     return launch_pdl(conv_tree_verify_kernel<K>, grid, dim3(kConvThreads), smem, stream, 1, a);
 }
 
 template <int K>
 cudaError_t launch_commit_k(const ConvCommitArgs& a, cudaStream_t stream) {
-    const dim3 grid((a.C + kConvBlockCh - 1) / kConvBlockCh, a.B, a.n_layers);
-    return launch_pdl(conv_commit_kernel<K>, grid, dim3(kConvThreads), 0, stream, 1, a);
+    const dim3 grid((a.C + kCommitBlockCh - 1) / kCommitBlockCh, a.B, a.n_layers);
+    return launch_pdl(conv_commit_kernel<K>, grid, dim3(kCommitThreads), 0, stream, 1, a);
 }
 
 }  // namespace
