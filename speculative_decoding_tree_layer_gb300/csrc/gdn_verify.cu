@@ -68,15 +68,21 @@ DFLV_DEVINL void named_barrier_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-// 4. [K ; Q] K^T on the tensor cores by the kHalfWarps warps of the first
-//    half: K K^T into A_s, Q K^T into M_s.  Only the 16 x 8 tiles that reach
-//    the diagonal or below are formed (ancestors have smaller indices); a
-//    warp keeps all of its tiles in flight at once.  The MMA's k index is
-//    permuted consistently on both operands: thread tq of a quad holds
-//    columns 4tq .. 4tq+3 of each 16-wide k step, so one 8-byte load fills
-//    both halves of its fragment registers.
+// 4-5. [K ; Q] K^T on the tensor cores by the kHalfWarps warps of the first
+//    half, with the decays and the ancestor mask applied to the accumulators:
+//      A_il = beta_i e^{g_i-g_l} k_i.k_l for strict ancestors l of i,
+//      M_il = e^{g_i-g_l} q_i.k_l for l in anc*(i), zero elsewhere
+//    (including every row of a node >= n).  Only the 16 x 8 tiles that reach
+//    the diagonal or below are formed (ancestors have smaller indices), and
+//    only those are ever read back.  A warp keeps all of its tiles in flight
+//    at once.  The MMA's k index is permuted consistently on both operands:
+//    thread tq of a quad holds columns 4tq .. 4tq+3 of each 16-wide k step,
+//    so one 8-byte load fills both halves of its fragment registers.  The
+//    cumulative decays g_s (written by the half before the call) are read
+//    only after the half's barrier, once the products are in registers.
 template <int DK, int NPT>
-DFLV_DEVINL void gdn_gram_tiles(const uint16_t* K_s, const uint16_t* Q_s, float* A_s, float* M_s, int warp,
+DFLV_DEVINL void gdn_gram_tiles(const uint16_t* K_s, const uint16_t* Q_s, float* A_s, float* M_s,
+                                const float* g_s, const float* beta_s, const uint64_t* amask_s, int n, int warp,
                                 int gq, int tq) {
     constexpr int KS = DK + 16;
     constexpr int MT = NPT / 16;                 // 16-row tiles per half
@@ -85,7 +91,8 @@ DFLV_DEVINL void gdn_gram_tiles(const uint16_t* K_s, const uint16_t* Q_s, float*
     static_assert((2 * PER) % kHalfWarps == 0, "tiles must split evenly over the warps");
     const uint16_t* Ap[TPW];
     const uint16_t* Bp[TPW];
-    float* dst[TPW];
+    int row0[TPW], col0[TPW];
+    bool isM[TPW];
 #pragma unroll
     for (int t = 0; t < TPW; ++t) {
         const int tile = warp + kHalfWarps * t;
@@ -98,7 +105,9 @@ DFLV_DEVINL void gdn_gram_tiles(const uint16_t* K_s, const uint16_t* Q_s, float*
         const int nt = q;
         Ap[t] = (half ? Q_s : K_s) + (m * 16 + gq) * KS;
         Bp[t] = K_s + (nt * 8 + gq) * KS;
-        dst[t] = (half ? M_s : A_s) + (m * 16 + gq) * NPT + nt * 8 + tq * 2;
+        row0[t] = m * 16 + gq;
+        col0[t] = nt * 8 + tq * 2;
+        isM[t] = half != 0;
     }
     float d[TPW][4];
 #pragma unroll
@@ -120,12 +129,19 @@ DFLV_DEVINL void gdn_gram_tiles(const uint16_t* K_s, const uint16_t* Q_s, float*
             mma_bf16_16816(d[t], af, bf);
         }
     }
+    named_barrier_sync(1, kGdnThreads / 2);  // g_s complete
 #pragma unroll
     for (int t = 0; t < TPW; ++t) {
-        dst[t][0] = d[t][0];
-        dst[t][1] = d[t][1];
-        dst[t][8 * NPT] = d[t][2];
-        dst[t][8 * NPT + 1] = d[t][3];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = row0[t] + (e >> 1) * 8, l = col0[t] + (e & 1);
+            float v = 0.f;
+            if (i < n && ((amask_s[i] >> l) & 1ull) && (isM[t] || l != i)) {
+                const float dec = expf(g_s[i] - g_s[l]);
+                v = isM[t] ? dec * d[t][e] : beta_s[i] * dec * d[t][e];
+            }
+            (isM[t] ? M_s : A_s)[i * NPT + l] = v;
+        }
     }
 }
 
@@ -406,23 +422,7 @@ __global__ void __launch_bounds__(kGdnThreads, 2)
             g_s[i] = g;
             G_s[i] = expf(g);
         }
-        gdn_gram_tiles<DK, NPT>(K_s, Q_s, A_s, M_s, warp, gq, tq);
-        named_barrier_sync(1, kGdnThreads / 2);
-        // 5. Decays and the ancestor mask, in place over the whole [NPT][NPT]:
-        //    A_il = beta_i e^{g_i-g_l} k_i.k_l for strict ancestors l of i,
-        //    M_il = e^{g_i-g_l} q_i.k_l for l in anc*(i), zero elsewhere
-        //    (including every row or column of a node >= n).
-        for (int idx = tid; idx < NPT * NPT; idx += kGdnThreads / 2) {
-            const int i = idx / NPT, l = idx % NPT;
-            float av = 0.f, mv = 0.f;
-            if (i < n && l <= i && ((amask_s[i] >> l) & 1ull)) {
-                const float dec = expf(g_s[i] - g_s[l]);
-                mv = dec * M_s[idx];
-                if (l != i) av = beta_s[i] * dec * A_s[idx];
-            }
-            A_s[idx] = av;
-            M_s[idx] = mv;
-        }
+        gdn_gram_tiles<DK, NPT>(K_s, Q_s, A_s, M_s, g_s, beta_s, amask_s, n, warp, gq, tq);
     } else {
         // 6. S_0[rows] . [K | Q]
         gdn_state_products<DK, RB, NPT>(S_s, K_s, Q_s, R_s, SQ_s, warp - kHalfWarps, gq, tq);
@@ -432,28 +432,36 @@ __global__ void __launch_bounds__(kGdnThreads, 2)
     // 7-8. Rows are independent: lane r of the first RB threads solves
     //    u_i = R_i - sum_{l < i} A_il u_l,  R_i = beta_i (v_i - e^{g_i} S_0 k_i),
     //    for all nodes in index order (a node's ancestors precede it) with
-    //    u in registers.  A is dense and zero off the ancestors, so every
+    //    u in registers.  A is zero off the ancestors in every tile read, so every
     //    trip count is fixed; the rows of A are read by all lanes at once.
     if (tid < RB) {
         const int r = tid;
         float u[NPT];
 #pragma unroll
         for (int i = 0; i < NPT; ++i) u[i] = 0.f;
+        // Nodes go in chunks of 8 with no branch inside a chunk, so the loads
+        // of a chunk (rows of A, v, S_0 k) are scheduled ahead of the FMA
+        // chain.  Nodes n .. chunk end compute values that are never read:
+        // a valid node i reads u_l for l < 4 ceil(i/4) only, and u_l with
+        // l > i is still zero when node i is solved.
 #pragma unroll
-        for (int i = 0; i < NPT; ++i) {
-            if (i < n) {
-                float acc[4] = {beta_s[i] * (bf16_bits_to_float(V_s[i * RB + r]) - G_s[i] * R_s[i * RB + r]),
-                                0.f, 0.f, 0.f};
-                const float4* Ar = reinterpret_cast<const float4*>(A_s + i * NPT);
+        for (int c = 0; c < NPT / 8; ++c) {
+            if (8 * c < n) {
 #pragma unroll
-                for (int l4 = 0; l4 < (i + 3) / 4; ++l4) {
-                    const float4 w = Ar[l4];
-                    acc[0] = fmaf(-w.x, u[4 * l4], acc[0]);
-                    acc[1] = fmaf(-w.y, u[4 * l4 + 1], acc[1]);
-                    acc[2] = fmaf(-w.z, u[4 * l4 + 2], acc[2]);
-                    acc[3] = fmaf(-w.w, u[4 * l4 + 3], acc[3]);
+                for (int i = 8 * c; i < 8 * c + 8; ++i) {
+                    float acc[4] = {beta_s[i] * (bf16_bits_to_float(V_s[i * RB + r]) - G_s[i] * R_s[i * RB + r]),
+                                    0.f, 0.f, 0.f};
+                    const float4* Ar = reinterpret_cast<const float4*>(A_s + i * NPT);
+#pragma unroll
+                    for (int l4 = 0; l4 < (i + 3) / 4; ++l4) {
+                        const float4 w = Ar[l4];
+                        acc[0] = fmaf(-w.x, u[4 * l4], acc[0]);
+                        acc[1] = fmaf(-w.y, u[4 * l4 + 1], acc[1]);
+                        acc[2] = fmaf(-w.z, u[4 * l4 + 2], acc[2]);
+                        acc[3] = fmaf(-w.w, u[4 * l4 + 3], acc[3]);
+                    }
+                    u[i] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
                 }
-                u[i] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
             }
         }
 #pragma unroll
