@@ -202,8 +202,9 @@ def hbm_peak():
 
 
 def kernel_source_hash(kind):
-    files = {"gdn": ["gdn_verify.cu"], "attn": ["attn_verify.cu", "attn_verify_tc.cu", "attn_common.cuh", "tcgen05.cuh"],
-             "accept": ["accept.cu"], "commit": ["commit.cu"]}
+    files = {"gdn": ["gdn_verify.cu"],
+             "attn": ["attn_verify.cu", "attn_verify_tc.cu", "attn_common.cuh", "tcgen05.cuh", "cluster.cuh"],
+             "accept": ["accept.cu"], "commit": ["commit.cu"], "conv": ["conv_tree.cu"], "conv_commit": ["conv_tree.cu"]}
     h = hashlib.sha256()
     for f in files[kind] + ["common.cuh", "tree.cuh"]:
         with open(os.path.join(ROOT, "speculative_decoding_tree_layer_gb300", "csrc", f), "rb") as fh:

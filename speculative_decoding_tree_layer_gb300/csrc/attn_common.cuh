@@ -1,49 +1,16 @@
 // attn_common.cuh -- pieces shared by the attention tree-verify kernels:
-// thread-block-cluster and distributed-shared-memory helpers, exact
-// conversion of int8 / 4-bit codes to fp16, and the block quantiser that
-// writes the tree's keys and values into the cache.
+// exact conversion of int8 / 4-bit codes to fp16 and the block quantiser
+// that writes the tree's keys and values into the cache (the cluster and
+// distributed-shared-memory helpers come from cluster.cuh).
 #pragma once
 
+#include "cluster.cuh"
 #include "common.cuh"
 
 namespace dflv {
 namespace attn {
 
 constexpr float kLog2e = 1.4426950408889634f;
-
-// ---------------------------------------------------------------- cluster helpers
-DFLV_DEVINL uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
-    return r;
-}
-DFLV_DEVINL void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::
-                     : "memory");
-}
-DFLV_DEVINL uint32_t map_to_rank(uint32_t smem_addr, uint32_t rank) {
-    uint32_t r;
-    asm("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(smem_addr), "r"(rank));
-    return r;
-}
-// Loads from a peer CTA's shared memory.  They keep a memory clobber so they
-// stay after the cluster barrier that publishes the data; callers issue all
-// loads of a batch before using any, so the hardware overlaps them.
-DFLV_DEVINL float ld_dsmem_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
-DFLV_DEVINL float2 ld_dsmem_f2(uint32_t addr) {
-    float2 v;
-    asm volatile("ld.shared::cluster.v2.f32 {%0,%1}, [%2];\n" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
-    return v;
-}
-DFLV_DEVINL float4 ld_dsmem_f4(uint32_t addr) {
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];\n" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
-    return v;
-}
 
 // ---------------------------------------------------------------- exact code -> fp16
 // fp16 with exponent field 25 (0x6400 = 1024) has unit spacing on
