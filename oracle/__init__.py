@@ -7,7 +7,8 @@ never does, and this package never imports the product.
 The arithmetic lives in ``oracle.c`` (plain C, fp64; see ``oracle.h`` for what
 each function computes and which passage of the pages it follows).  This
 module compiles it with gcc and wraps each entry point for numpy arrays laid
-out exactly as the library's C ABI lays them out.
+out exactly as the library's C ABI lays them out.  The draft-tree
+construction is plain numpy / Python in ``ddtree.py`` (small, sequential).
 """
 from __future__ import annotations
 
@@ -17,6 +18,8 @@ import subprocess
 import threading
 
 import numpy as np
+
+from .ddtree import build_ddtree, draft_topk  # noqa: F401
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _BUILD_DIR = os.path.join(_HERE, "_build")
