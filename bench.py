@@ -42,6 +42,7 @@ METRIC = "verified tree nodes/s per layer at budget 22, 32K ctx; % of HBM roofli
 UNIT = "nodes/s/layer"
 N_LAYERS, N_GDN, N_ATTN = 64, 48, 16
 BUDGET, VOCAB, CTX, WINDOW, PLANT = 22, 151936, 32768, 2048, 8
+DRAFT_BLOCK, TOPK, TAU = 16, 4, 6.0   # draft positions per tree, expansion width, pruning margin
 GDN = synth.GDN_27B
 ATT = synth.ATTN_27B
 CONV = synth.CONV_27B
@@ -81,8 +82,10 @@ def make_host_inputs(rng, n_layers=N_LAYERS):
     # stay the same
     crng = np.random.default_rng(SEED + 7919)
     conv = [synth.conv_inputs(crng, 1, BUDGET, CONV["C"], CONV["K"]) for kind, _ in layers if kind == "gdn"]
+    # the draft's logits for the next tree (its construction is measured beside the step)
+    draft = synth.draft_logits(np.random.default_rng(SEED + 104729), 1, DRAFT_BLOCK, VOCAB)
     return dict(parent=parent, n_nodes=n_nodes, tokens=tokens, logits=logits, layers=layers, cap=cap,
-                planted=planted, conv=conv)
+                planted=planted, conv=conv, draft=draft)
 
 
 # ---------------------------------------------------------------------------- algorithmic bytes
@@ -124,6 +127,12 @@ def conv_commit_bytes(L):
     and the accepted inputs, K-1 rows written."""
     C, K = CONV["C"], CONV["K"]
     return N_GDN * 2 * (K - 1) * C * 2 if L else 0
+
+
+def ddtree_bytes():
+    """Tree construction: the draft's logits read once; top-K lists and the
+    tree written."""
+    return DRAFT_BLOCK * VOCAB * 4 + DRAFT_BLOCK * TOPK * 8 + BUDGET * 12 + 8
 
 
 def accept_bytes():
@@ -204,7 +213,8 @@ def hbm_peak():
 def kernel_source_hash(kind):
     files = {"gdn": ["gdn_verify.cu"],
              "attn": ["attn_verify.cu", "attn_verify_tc.cu", "attn_common.cuh", "tcgen05.cuh", "cluster.cuh"],
-             "accept": ["accept.cu"], "commit": ["commit.cu"], "conv": ["conv_tree.cu"], "conv_commit": ["conv_tree.cu"]}
+             "accept": ["accept.cu"], "commit": ["commit.cu"], "conv": ["conv_tree.cu"], "conv_commit": ["conv_tree.cu"],
+             "ddtree": ["ddtree.cu", "cluster.cuh"]}
     h = hashlib.sha256()
     for f in files[kind] + ["common.cuh", "tree.cuh"]:
         with open(os.path.join(ROOT, "speculative_decoding_tree_layer_gb300", "csrc", f), "rb") as fh:
@@ -325,6 +335,15 @@ class GpuStep:
             c["state0"] = c["state"].clone()
             c["out"] = t.empty((1, N, CONV["C"]), device=dev)
             self.conv.append(c)
+        # ---- draft-tree construction (measured beside the step)
+        self.draft = t.from_numpy(host["draft"]).to(dev)
+        self.root_token = t.zeros(1, dtype=t.int32, device=dev)
+        self.tree = dict(topk_tok=t.empty((1, DRAFT_BLOCK, TOPK), dtype=t.int32, device=dev),
+                         topk_logp=t.empty((1, DRAFT_BLOCK, TOPK), device=dev),
+                         parent=t.empty((1, N), dtype=t.int32, device=dev),
+                         tokens=t.empty((1, N), dtype=t.int32, device=dev),
+                         n_nodes=t.empty(1, dtype=t.int32, device=dev), score=t.empty((1, N), device=dev))
+        self.ddtree_desc = dflv.ddtree_desc(1, DRAFT_BLOCK, VOCAB, TOPK, N, TAU)
 
     # one pass of the hot path: every layer's verify (the GDN layers first
     # commit the previous step's accepted path into their state: deferred
@@ -364,6 +383,12 @@ class GpuStep:
         return self.dflv.dflv_tree_conv_verify(self.conv_desc if i == 0 else self.conv_desc_next, self.parent,
                                                self.n_nodes, c["x"], c["state"], c["w"], c["out"], self.status)
 
+    def ddtree_build(self):
+        tr = self.tree
+        return self.dflv.dflv_ddtree_build(self.ddtree_desc, self.draft, self.root_token, tr["topk_tok"],
+                                           tr["topk_logp"], tr["parent"], tr["tokens"], tr["n_nodes"], tr["score"],
+                                           self.status)
+
     def conv_commit(self):
         return self.dflv.dflv_conv_commit(self.conv_desc, len(self.conv), [c["state"] for c in self.conv],
                                           [c["x"] for c in self.conv], self.path, self.path_len, self.status)
@@ -399,12 +424,21 @@ def kernel_chain_ms(S, torch, stream, steps, warmup):
     def conv_commit():
         chk(S.conv_commit(), "conv commit")
 
+    def ddtree():
+        chk(S.ddtree_build(), "ddtree build")
+
+    # A kind with a single launch per step is captured REPS times per graph,
+    # so that the host's graph submission stays off the measured interval.
+    REPS = 16
     out = {}
-    for name, fn, n in (("gdn", gdn_chain, N_GDN), ("attn", attn_chain, N_ATTN), ("accept", accept, 1),
-                        ("commit", commit, 1), ("conv", conv_chain, N_GDN), ("conv_commit", conv_commit, 1)):
+    for name, fn, n, reps in (("gdn", gdn_chain, N_GDN, 1), ("attn", attn_chain, N_ATTN, 1),
+                              ("accept", accept, 1, REPS), ("commit", commit, 1, REPS),
+                              ("conv", conv_chain, N_GDN, 1), ("conv_commit", conv_commit, 1, REPS),
+                              ("ddtree", ddtree, 1, REPS)):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            fn()
+            for _ in range(reps):
+                fn()
         S.reset()
         with torch.cuda.stream(stream):
             accept()  # an accepted path: the GDN verifies apply it as their pending commit
@@ -419,7 +453,7 @@ def kernel_chain_ms(S, torch, stream, steps, warmup):
                 g.replay()
             e1.record()
         torch.cuda.synchronize()
-        out[name] = e0.elapsed_time(e1) / (steps * n)
+        out[name] = e0.elapsed_time(e1) / (steps * n * reps)
         S.reset()
         torch.cuda.synchronize()
     return out
@@ -596,11 +630,12 @@ def profile_one(kind, launches):
     host = make_host_inputs(rng, n_layers=4)
     S = GpuStep(host, torch, dflv)
     li, L = next((i, L) for i, L in enumerate(S.layers) if L["kind"] == ("attn" if kind == "attn" else "gdn"))
-    if kind in ("conv", "conv_commit"):
+    if kind in ("conv", "conv_commit", "ddtree"):
         S.step(1)
         torch.cuda.synchronize()
         for _ in range(launches):
-            dflv.check(S.conv_verify(0) if kind == "conv" else S.conv_commit())
+            dflv.check(S.conv_verify(0) if kind == "conv" else S.conv_commit() if kind == "conv_commit"
+                       else S.ddtree_build())
         torch.cuda.synchronize()
         print(json.dumps({"kernel": kind, "launches": launches, "status": int(S.status.item())}))
         return
@@ -631,7 +666,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel", choices=["gdn", "attn", "accept", "commit", "conv", "conv_commit"], default=None,
+    ap.add_argument("--kernel", choices=["gdn", "attn", "accept", "commit", "conv", "conv_commit", "ddtree"],
+                    default=None,
                     help="profiling mode: launch one kernel of the step --launches times on its "
                          "single-layer workload and exit (for ncu captures)")
     ap.add_argument("--launches", type=int, default=3)
@@ -674,17 +710,20 @@ def main():
     per = r["per"] or {}
     L = r["L"]
     ab = dict(gdn=gdn_bytes(L), attn=attn_bytes(), accept=accept_bytes(), commit=commit_bytes(L),
-              conv=conv_bytes(), conv_commit=conv_commit_bytes(L))
+              conv=conv_bytes(), conv_commit=conv_commit_bytes(L), ddtree=ddtree_bytes())
     launches = dict(gdn=N_GDN, attn=N_ATTN, accept=1, commit=1)
     # dominant kernel: the largest share of the step
     shares = {k: per[k] * launches[k] for k in per if k in launches} if per else {}
     beside = {}
-    for k in ("conv", "conv_commit"):
+    for k in ("conv", "conv_commit", "ddtree"):
         if per.get(k):
             gbs = ab[k] / (per[k] * 1e-3) / 1e9
             beside[k] = {"ms_per_launch": per[k], "algorithmic_bytes_per_launch": ab[k], "achieved": gbs,
                          "unit": "GB/s", "frac": gbs / peak,
                          "launches": N_GDN if k == "conv" else 1}
+    if "ddtree" in beside:
+        beside["ddtree"]["launches"] = 1
+        beside["ddtree"]["kernels_per_launch"] = 2
     dom = max(shares, key=shares.get) if shares else "commit"
     dur_ms = per.get(dom)
     achieved = ab[dom] / (dur_ms * 1e-3) / 1e9 if dur_ms else None
@@ -704,13 +743,17 @@ def main():
                      "peak_source": f"{peak_kind} hbm_gbs",
                      "algorithmic_bytes_per_launch": ab[dom],
                      "avg_launch_ms": dur_ms,
-                     "launch_timing": "chain of all launches of this kernel in the step, back to back, "
-                                      "CUDA events on the launching stream",
+                     "launch_timing": "chain of all launches of this kernel in the step, back to back (a kernel "
+                                      "launched once per step: 16 launches per graph), CUDA events on the "
+                                      "launching stream",
                      "traffic": profiled_traffic(dom)},
         "kernels_ms_per_launch": per,
         "beside_the_step": {"what": "the short convolution in front of each GDN layer (48 tree-conv launches "
-                                    "back to back, C=10240, K=4) and the commit of its window (one launch, 48 "
-                                    "layers); timed like the step's kernels, not part of the step",
+                                    "back to back, C=10240, K=4), the commit of its window (one launch, 48 "
+                                    "layers) and the construction of the next draft tree from the draft's "
+                                    "logits (16 positions x 151936, top-4, budget 22, tau 6: a top-K/log-sum-exp "
+                                    "kernel and a best-first kernel); timed like the step's kernels, not part "
+                                    "of the step",
                             **beside},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
         "gpu_launches": r["launches"] * args.steps,

@@ -29,6 +29,8 @@
  *   - Commit / rollback leaves the recurrent state and KV cache as if only
  *     the accepted path had been decoded ([README] "How it works",
  *     "Per-step rollback"; [PR606] review note naming the commit routines).
+ *   - The draft tree itself is built best-first over the draft's top-K
+ *     tokens per position after a rank-0 chain ([README] "How it works").
  *   - The short convolution in front of each gated-DeltaNet layer reads
  *     each node's window along its parent chain ([README] "How it works":
  *     ggml_ssm_conv_tree).
@@ -240,6 +242,49 @@ dflv_status dflv_conv_commit(const dflv_conv_desc* desc, int32_t n_layers, uint1
                              const int32_t* path_len, int32_t* status_dev, dflv_stream_t stream);
 
 #define DFLV_MAX_CONV_LAYERS 128
+
+/* ------------------------------------------------------------------------ */
+/* Draft-tree construction                                                   */
+/* ------------------------------------------------------------------------ */
+
+/* Builds the draft tree that the verify calls take ([README] "How it works":
+ * a best-first tree of up to `budget` nodes over the top-K branches at each
+ * position, the rank-0 chain placed first (chain pre-seed); [PR606] options
+ * table: --specla-top-k is the expansion width K, --ddtree-tau a cumulative
+ * log-probability pruning margin).  The pages do not write the procedure;
+ * this library computes, for every sequence b:
+ *   1. per draft position d (0 .. D-1, predicting the token at depth d+1):
+ *      logp_d = log-softmax of draft_logits[b][d], and the K tokens with the
+ *      largest logits (ties to the lower token id), in that order;
+ *   2. the root (node 0, token root_token[b], score 0); then the chain: node
+ *      e = 1 .. min(D, budget-1) is the rank-0 token of position e-1, child of
+ *      node e-1; a node's score is the sum of logp over its root path;
+ *   3. best-first: while fewer than `budget` nodes exist, add the candidate
+ *      with the highest score, ties to the lower parent index; the
+ *      candidates are, for every node at depth < D, its child of the next
+ *      rank not yet in the tree (the child of rank r at depth e scores
+ *      parent + logp_{e-1}[rank r]); with tau >= 0 a candidate at depth e is
+ *      admitted only if its score >= the chain's score at depth e minus tau
+ *      (so the tree may stay below `budget`).
+ * Nodes are numbered in insertion order (parent[i] < i), as verify expects.
+ * Scores are accumulated in fp32 in path order.
+ *   draft_logits [B][D][V] f32 (finite), root_token [B] int32
+ *   topk_tok [B][D][K] int32, topk_logp [B][D][K] f32: step 1's result
+ *                (written; the tree is built from them)
+ *   parent, tokens [B][budget] int32 (-1 past n_nodes), n_nodes [B] int32,
+ *   score [B][budget] f32 (0 past n_nodes)
+ * Supported: 1 <= D <= 64, 1 <= K <= 8, 1 <= budget <= 64, V a multiple of
+ * 4 and >= K.  tau: < 0 = no pruning (NaN is rejected). */
+typedef struct {
+    int32_t B, D, V, K, budget;
+    float tau;
+    uint32_t flags; /* 0 */
+} dflv_ddtree_desc;
+
+dflv_status dflv_ddtree_build(const dflv_ddtree_desc* desc, const float* draft_logits,
+                              const int32_t* root_token, int32_t* topk_tok, float* topk_logp,
+                              int32_t* parent, int32_t* tokens, int32_t* n_nodes, float* score,
+                              int32_t* status_dev, dflv_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Attention layer                                                           */

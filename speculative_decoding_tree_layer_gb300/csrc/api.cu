@@ -365,3 +365,42 @@ dflv_status dflv_conv_commit(const dflv_conv_desc* desc, int32_t n_layers, uint1
 }
 
 }  // extern "C"
+
+extern "C" {
+
+dflv_status dflv_ddtree_build(const dflv_ddtree_desc* desc, const float* draft_logits,
+                              const int32_t* root_token, int32_t* topk_tok, float* topk_logp,
+                              int32_t* parent, int32_t* tokens, int32_t* n_nodes, float* score,
+                              int32_t* status_dev, dflv_stream_t stream) {
+    if (!desc) return DFLV_ERR_INVALID_ARG;
+    if (desc->B < 1 || desc->D < 1 || desc->K < 1 || desc->budget < 1 || desc->V < 1 || desc->flags != 0 ||
+        desc->tau != desc->tau)
+        return DFLV_ERR_INVALID_ARG;
+    if (desc->D > dflv::kMaxTreeDepth || desc->K > 8 || desc->budget > 64 || desc->V % 4 != 0 || desc->V < desc->K)
+        return DFLV_ERR_UNSUPPORTED;
+    if (!draft_logits || !root_token || !topk_tok || !topk_logp || !parent || !tokens || !n_nodes || !score ||
+        !status_dev)
+        return DFLV_ERR_INVALID_ARG;
+    if (!aligned16(draft_logits) || !aligned4(root_token) || !aligned4(topk_tok) || !aligned4(topk_logp) ||
+        !aligned4(parent) || !aligned4(tokens) || !aligned4(n_nodes) || !aligned4(score) || !aligned4(status_dev))
+        return DFLV_ERR_INVALID_ARG;
+    dflv::DdtreeArgs a;
+    a.B = desc->B;
+    a.D = desc->D;
+    a.V = desc->V;
+    a.K = desc->K;
+    a.budget = desc->budget;
+    a.tau = desc->tau;
+    a.logits = draft_logits;
+    a.root_token = root_token;
+    a.topk_tok = topk_tok;
+    a.topk_logp = topk_logp;
+    a.parent = parent;
+    a.tokens = tokens;
+    a.n_nodes = n_nodes;
+    a.score = score;
+    a.status = status_dev;
+    return from_cuda(dflv::launch_ddtree_build(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

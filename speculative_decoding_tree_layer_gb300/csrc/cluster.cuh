@@ -37,6 +37,11 @@ DFLV_DEVINL float ld_dsmem_f32(uint32_t addr) {
     asm volatile("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(v) : "r"(addr) : "memory");
     return v;
 }
+DFLV_DEVINL int ld_dsmem_s32(uint32_t addr) {
+    int v;
+    asm volatile("ld.shared::cluster.s32 %0, [%1];\n" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
 DFLV_DEVINL float2 ld_dsmem_f2(uint32_t addr) {
     float2 v;
     asm volatile("ld.shared::cluster.v2.f32 {%0,%1}, [%2];\n" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");

@@ -135,4 +135,22 @@ struct ConvCommitArgs {
 
 cudaError_t launch_conv_commit(const ConvCommitArgs& a, cudaStream_t stream);
 
+constexpr int kMaxTreeDepth = 64;
+
+struct DdtreeArgs {
+    int B, D, V, K, budget;
+    float tau;  // < 0: no pruning
+    const float* logits;
+    const int32_t* root_token;
+    int32_t* topk_tok;
+    float* topk_logp;
+    int32_t* parent;
+    int32_t* tokens;
+    int32_t* n_nodes;
+    float* score;
+    int32_t* status;
+};
+
+cudaError_t launch_ddtree_build(const DdtreeArgs& a, cudaStream_t stream);
+
 }  // namespace dflv

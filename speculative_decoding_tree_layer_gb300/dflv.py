@@ -52,6 +52,11 @@ class dflv_conv_desc(ctypes.Structure):
     _fields_ = [("B", _c_i32), ("N_max", _c_i32), ("C", _c_i32), ("K", _c_i32), ("flags", ctypes.c_uint32)]
 
 
+class dflv_ddtree_desc(ctypes.Structure):
+    _fields_ = [("B", _c_i32), ("D", _c_i32), ("V", _c_i32), ("K", _c_i32), ("budget", _c_i32),
+                ("tau", ctypes.c_float), ("flags", ctypes.c_uint32)]
+
+
 class DflvError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
@@ -83,6 +88,7 @@ def load():
                                          P, P, P, P, P]
     lib.dflv_tree_conv_verify.argtypes = [ctypes.POINTER(dflv_conv_desc)] + [P] * 7 + [P]
     lib.dflv_conv_commit.argtypes = [ctypes.POINTER(dflv_conv_desc), _c_i32, P, P, P, P, P, P]
+    lib.dflv_ddtree_build.argtypes = [ctypes.POINTER(dflv_ddtree_desc)] + [P] * 10
     lib.dflv_gdn_workspace_size.argtypes = [ctypes.POINTER(dflv_gdn_desc)]
     lib.dflv_gdn_workspace_size.restype = S
     lib.dflv_attn_workspace_size.argtypes = [ctypes.POINTER(dflv_attn_desc)]
@@ -90,7 +96,7 @@ def load():
     lib.dflv_status_string.argtypes = [ctypes.c_int]
     lib.dflv_status_string.restype = ctypes.c_char_p
     for f in ("dflv_tree_gdn_verify", "dflv_tree_gdn_verify_pending", "dflv_tree_attn_verify", "dflv_accept_greedy",
-              "dflv_commit_rollback", "dflv_tree_conv_verify", "dflv_conv_commit"):
+              "dflv_commit_rollback", "dflv_tree_conv_verify", "dflv_conv_commit", "dflv_ddtree_build"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -210,6 +216,18 @@ def dflv_conv_commit(desc, n_layers, states, xs, path, path_len, status_dev, str
     return load().dflv_conv_commit(ctypes.byref(desc), n_layers, ctypes.cast(st, ctypes.c_void_p),
                                    ctypes.cast(xa, ctypes.c_void_p), _ptr(path), _ptr(path_len), _ptr(status_dev),
                                    _stream(stream))
+
+
+def ddtree_desc(B, D, V, K, budget, tau=-1.0, flags=0):
+    """tau < 0 (default): no pruning."""
+    return dflv_ddtree_desc(B, D, V, K, budget, tau, flags)
+
+
+def dflv_ddtree_build(desc, draft_logits, root_token, topk_tok, topk_logp, parent, tokens, n_nodes, score,
+                      status_dev, stream=None) -> int:
+    return load().dflv_ddtree_build(ctypes.byref(desc), _ptr(draft_logits), _ptr(root_token), _ptr(topk_tok),
+                                    _ptr(topk_logp), _ptr(parent), _ptr(tokens), _ptr(n_nodes), _ptr(score),
+                                    _ptr(status_dev), _stream(stream))
 
 
 def dflv_gdn_workspace_size(desc) -> int:

@@ -197,6 +197,19 @@ def conv_inputs(rng, B, N, C, K, w_std=0.5):
     )
 
 
+# ------------------------------------------------------------------ draft logits
+def draft_logits(rng, B, D, V, std=2.0, n_hot=3, boost=(3.0, 9.0)):
+    """Draft logits [B][D][V] fp32: N(0, std) plus, at every position,
+    n_hot random tokens raised by U(boost) -- a confident head over a flat
+    tail, as a trained draft gives."""
+    x = (rng.standard_normal((B, D, V), dtype=np.float32) * std).astype(np.float32)
+    for b in range(B):
+        for d in range(D):
+            hot = rng.choice(V, size=n_hot, replace=False)
+            x[b, d, hot] += rng.uniform(boost[0], boost[1], size=n_hot).astype(np.float32)
+    return x
+
+
 # ------------------------------------------------------------------ attention layer
 def attn_inputs(rng, B, N, Hq, Hkv, D):
     """Tree queries and the tree's new keys/values, bf16 ~ N(0,1)."""

@@ -19,7 +19,7 @@ def test_exports_every_declared_symbol(lib):
     names = dflv.header_symbols()
     assert set(names) >= {"dflv_tree_gdn_verify", "dflv_tree_attn_verify", "dflv_accept_greedy",
                           "dflv_commit_rollback", "dflv_gdn_workspace_size", "dflv_attn_workspace_size",
-                          "dflv_status_string", "dflv_tree_conv_verify", "dflv_conv_commit"}
+                          "dflv_status_string", "dflv_tree_conv_verify", "dflv_conv_commit", "dflv_ddtree_build"}
     for n in names:
         assert hasattr(lib, n), n
 
@@ -117,3 +117,25 @@ def test_conv_host_validation(lib):
     assert dflv.dflv_conv_commit(ok, 129, [P] * 129, [P] * 129, P, P, P, stream=0) == dflv.DFLV_ERR_INVALID_ARG
     assert dflv.dflv_conv_commit(ok, 2, [P, None], [P, P], P, P, P, stream=0) == dflv.DFLV_ERR_INVALID_ARG
     assert dflv.dflv_conv_commit(ok, 1, [P], [24], P, P, P, stream=0) == dflv.DFLV_ERR_INVALID_ARG
+
+
+def test_ddtree_host_validation(lib):
+    P = 16
+
+    def call(desc, **over):
+        args = dict(draft_logits=P, root_token=P, topk_tok=P, topk_logp=P, parent=P, tokens=P, n_nodes=P, score=P,
+                    status_dev=P)
+        args.update(over)
+        return dflv.dflv_ddtree_build(desc, stream=0, **args)
+
+    assert call(dflv.ddtree_desc(1, 16, 151936, 9, 22)) == dflv.DFLV_ERR_UNSUPPORTED      # K > 8
+    assert call(dflv.ddtree_desc(1, 65, 151936, 4, 22)) == dflv.DFLV_ERR_UNSUPPORTED      # D > 64
+    assert call(dflv.ddtree_desc(1, 16, 151936, 4, 65)) == dflv.DFLV_ERR_UNSUPPORTED      # budget > 64
+    assert call(dflv.ddtree_desc(1, 16, 151937, 4, 22)) == dflv.DFLV_ERR_UNSUPPORTED      # V not a multiple of 4
+    assert call(dflv.ddtree_desc(0, 16, 151936, 4, 22)) == dflv.DFLV_ERR_INVALID_ARG
+    assert call(dflv.ddtree_desc(1, 16, 151936, 4, 22, float("nan"))) == dflv.DFLV_ERR_INVALID_ARG
+    assert call(dflv.ddtree_desc(1, 16, 151936, 4, 22, 6.0, 1)) == dflv.DFLV_ERR_INVALID_ARG   # flags
+    ok = dflv.ddtree_desc(1, 16, 151936, 4, 22, 6.0)
+    assert call(ok, draft_logits=None) == dflv.DFLV_ERR_INVALID_ARG
+    assert call(ok, draft_logits=24) == dflv.DFLV_ERR_INVALID_ARG                        # misaligned
+    assert call(ok, parent=18) == dflv.DFLV_ERR_INVALID_ARG
