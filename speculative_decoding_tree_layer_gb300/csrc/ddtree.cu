@@ -14,8 +14,9 @@
 //
 // Step 1 is the HBM-bound part (D x vocab fp32 logits per sequence): a
 // thread-block cluster per position splits the vocabulary; each thread keeps
-// a running (max, sum of exponentials) and a sorted top-K list in registers
-// while it streams its share with 16-byte loads; lists merge warp-wide by K
+// a running (max, sum of exponentials), updated once per chunk of 32 values,
+// and a sorted top-K list in registers while it streams its share with
+// 16-byte loads; lists merge warp-wide by K
 // rounds of a shuffle argmax, then across the block in shared memory and
 // across the cluster through distributed shared memory.  Step 2 builds the
 // tree with one warp per sequence: because a node's children enter in rank
@@ -141,36 +142,37 @@ __global__ void __launch_bounds__(kTopkThreads) draft_topk_kernel(const DdtreeAr
         ix[j] = INT_MAX;
     }
     float m = -INFINITY, s = 0.f;
-    auto take = [&](float x, int c) {
-        topk_insert<K>(v, ix, x, c);
-        if (x > m) {
-            s = s * exp2f((m - x) * kLog2e) + 1.f;  // exp2(-inf) = 0 on the first value
-            m = x;
-        } else {
-            s += exp2f((x - m) * kLog2e);
-        }
-    };
-    int q = q0 + tid;
-    // eight independent 16-byte loads in flight per thread
-    for (; q + 7 * kTopkThreads < q1; q += 8 * kTopkThreads) {
+    // Chunks of 8 float4 per thread, all loads in flight at once (past the
+    // share's end they read as -inf).  Per chunk: its max updates the running
+    // max once, then every value adds 2^((x - m) log2 e) and is offered to
+    // the top-K list (indices increase within and across chunks).
+    for (int q = q0 + tid; q < q1; q += 8 * kTopkThreads) {
         float4 x[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) x[u] = __ldcs(r4 + q + u * kTopkThreads);
+        for (int u = 0; u < 8; ++u) {
+            const int qq = q + u * kTopkThreads;
+            x[u] = qq < q1 ? __ldcs(r4 + qq) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        }
+        float cm = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) cm = fmaxf(cm, fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w)));
+        if (cm > m) {  // the chunk's first value is always in range, so cm is finite
+            s *= exp2f((m - cm) * kLog2e);
+            m = cm;
+        }
+        const float mb = m * kLog2e;
+        float cs = 0.f;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
+            cs += exp2f(fmaf(x[u].x, kLog2e, -mb)) + exp2f(fmaf(x[u].y, kLog2e, -mb)) +
+                  exp2f(fmaf(x[u].z, kLog2e, -mb)) + exp2f(fmaf(x[u].w, kLog2e, -mb));
             const int c = (q + u * kTopkThreads) * 4;
-            take(x[u].x, c);
-            take(x[u].y, c + 1);
-            take(x[u].z, c + 2);
-            take(x[u].w, c + 3);
+            topk_insert<K>(v, ix, x[u].x, c);
+            topk_insert<K>(v, ix, x[u].y, c + 1);
+            topk_insert<K>(v, ix, x[u].z, c + 2);
+            topk_insert<K>(v, ix, x[u].w, c + 3);
         }
-    }
-    for (; q < q1; q += kTopkThreads) {
-        const float4 x = __ldcs(r4 + q);
-        take(x.x, q * 4);
-        take(x.y, q * 4 + 1);
-        take(x.z, q * 4 + 2);
-        take(x.w, q * 4 + 3);
+        s += cs;
     }
 
     // warp, then block
