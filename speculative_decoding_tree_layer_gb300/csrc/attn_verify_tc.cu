@@ -9,17 +9,18 @@
 // cached positions inside its window and to its ancestors-or-self.
 //
 // How: one thread-block cluster per (sequence, KV head, row tile of <= 128
-// query rows); the cluster's CTAs split the visible cache keys evenly into
-// 32-key tiles (tile starts aligned to 32 keys), and the tree block is one
+// query rows); the cluster's CTAs split the visible cache keys into 32-key
+// tiles (tile starts aligned to 32 keys) by cost, and the tree block is one
 // or two extra tiles.  Inside a CTA the tiles flow through a pipeline of
-// three warp roles that hand over through mbarriers (every wait bounded):
-//   * stage warps (4): raw codes and scales arrive by bulk copies (TMA
-//     engine, double-buffered, requested for the first tiles before the
-//     kernel waits for its predecessor when early prefetch is on); they are
-//     expanded into fp16 hi + lo tiles with the block scale folded in
-//     (d * code is exact in fp32; hi = fp16(x), lo = fp16(x - hi)).  K tiles
-//     are double-buffered.  A tree tile is quantised from the new keys and
-//     values in place (and written to the cache);
+// warp roles that hand over through mbarriers (every wait bounded):
+//   * load warps (2, one per plane): the raw codes and scales of each tile
+//     by 16-byte cp.async into double buffers, completion counted on an
+//     mbarrier; the first two tiles are requested before the kernel waits
+//     for its predecessor when early prefetch is on.  The CTA that attends
+//     to a tree tile first quantises the tree's rows into the cache;
+//   * stage warps (4): each raw tile is expanded into fp16 hi + lo tiles
+//     with the block scale folded in (d * code is exact in fp32; hi =
+//     fp16(x), lo = fp16(x - hi)).  K tiles are double-buffered;
 //   * the MMA warp (1) issues tcgen05.mma: [S_hi | S_lo] = Q [K_hi ; K_lo]^T
 //     into one of two S buffers in tensor memory (M = 128, N = 64, K = head
 //     size), so the next tile's scores are formed while the softmax works on
@@ -51,8 +52,8 @@ constexpr int kRows = 128;       // MMA M: query rows per CTA
 constexpr int kSoftWarps = 4;    // warps 0-3
 constexpr int kStageWarps = 4;   // warps 4-7
 constexpr int kMmaWarp = kSoftWarps + kStageWarps;  // warp 8
-constexpr int kLoadWarp = kMmaWarp + 1;              // warp 9: raw tile copies
-constexpr int kThreads = (kLoadWarp + 1) * 32;
+constexpr int kLoadWarp = kMmaWarp + 1;              // warp 9: raw K tile copies, warp 10: raw V
+constexpr int kThreads = (kLoadWarp + 2) * 32;
 constexpr int kStage0 = kSoftWarps * 32;             // first stage thread
 constexpr int kStageThreads = kStageWarps * 32;
 constexpr int kStageBarrier = 2;                     // named barrier of the stage warps
@@ -313,9 +314,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
                                bars + kRawV0 + (u & 1), lane);
     };
     // the first two tiles' raw planes are requested at once
-    if (warp == kLoadWarp)
+    if (warp == kLoadWarp || warp == kLoadWarp + 1)
         for (int u = 0; u < min(T, 2); ++u)
-            if (!tile(u).tree) issue_tile_raw(u, true, true);
+            if (!tile(u).tree) issue_tile_raw(u, warp == kLoadWarp, warp != kLoadWarp);
 
     if (early) grid_dependency_wait();
 
@@ -543,16 +544,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
                 break;
             }
         }
-    } else if (warp == kLoadWarp) {
+    } else if (warp == kLoadWarp || warp == kLoadWarp + 1) {
         // ================================================ raw tile copies: tile u
-        // goes into buffer u & 1 once the stage warps have released tile u - 2
+        // goes into buffer u & 1 once the stage warps have released tile u - 2.
+        // One warp per plane, so a K request never waits behind a V buffer.
+        const bool kside = warp == kLoadWarp;
         bool ok = true;
         for (int u = 0; u < T && ok; ++u) {
             if (u < 2 && !tile(u).tree) continue;  // requested before the loop
-            if (u >= 2) ok = wait_phase(bars + kKFree0 + (u & 1), ((u - 2) >> 1) & 1);
-            if (ok) issue_tile_raw(u, true, false);
-            if (u >= 2) ok = ok && wait_phase(bars + kVFree0 + (u & 1), ((u - 2) >> 1) & 1);
-            if (ok) issue_tile_raw(u, false, true);
+            if (u >= 2) ok = wait_phase(bars + (kside ? kKFree0 : kVFree0) + (u & 1), ((u - 2) >> 1) & 1);
+            if (ok) issue_tile_raw(u, kside, !kside);
         }
         if (!__all_sync(0xffffffffu, ok) && lane == 0) atomicOr(fail_s, 1);
         cp_async_wait<0>();  // this lane's copies have landed before the CTA moves on
