@@ -415,10 +415,15 @@ __global__ void __launch_bounds__(kGdnThreads, 2)
     if (misc_s[1]) return;  // the state copy never landed (status already raised)
 
     if (warp < kHalfWarps) {
-        // 3. cumulative log decay over the ancestors-or-self
+        // 3. cumulative log decay over the ancestors-or-self: a masked sum
+        //    over all NPT slots with a fixed trip count (the loads are the
+        //    same address across the warp and need no data-dependent loop)
         for (int i = tid; i < n; i += kGdnThreads / 2) {
-            float g = 0.f;
-            for (uint64_t m = amask_s[i]; m; m &= m - 1) g += la_s[ffs64(m)];
+            const uint64_t am = amask_s[i];
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int l = 0; l < NPT; ++l) acc[l & 3] += ((am >> l) & 1ull) ? la_s[l] : 0.f;
+            const float g = (acc[0] + acc[1]) + (acc[2] + acc[3]);
             g_s[i] = g;
             G_s[i] = expf(g);
         }
