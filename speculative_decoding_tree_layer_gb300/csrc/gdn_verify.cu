@@ -252,7 +252,7 @@ DFLV_DEVINL void gdn_apply_pending(const GdnVerifyArgs& a, float* S_s, const uin
 }
 
 template <int DK, int RB, int NPT>
-__global__ void __launch_bounds__(kGdnThreads, 2)
+__global__ void __launch_bounds__(kGdnThreads, NPT == 32 ? 3 : 2)
     gdn_tree_verify_kernel(GdnVerifyArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     const GdnSmemLayout L(NPT, DK, RB);
