@@ -28,7 +28,7 @@ _SOURCES = [os.path.join(_HERE, "oracle.c"), os.path.join(_HERE, "oracle.h")]
 _lock = threading.Lock()
 _lib = None
 
-KV_Q8_0, KV_Q4_0, KV_F32 = 0, 1, 2
+KV_Q8_0, KV_Q4_0, KV_F32, KV_Q8_0_Q4_0, KV_Q4_0_Q8_0 = 0, 1, 2, 3, 4
 OK, ERR_ARG, ERR_TOPOLOGY, ERR_CAPACITY = 0, 1, 2, 4
 
 
@@ -272,7 +272,7 @@ def kv_commit(cache, kv_type, path, path_len, n_past):
     B, N = path.shape
     kq = cache["kq"]
     Hkv, cap = kq.shape[1], kq.shape[2]
-    D = kq.shape[3] * (2 if kv_type == KV_Q4_0 else 1)
+    D = kq.shape[3] * (2 if kv_type in (KV_Q4_0, KV_Q4_0_Q8_0) else 1)
     rc = _load().orc_kv_commit(B, N, Hkv, D, cap, int(kv_type), _p(path), _p(path_len),
                                _p(n_past), _p(cache["kq"]), _p(cache["vq"]),
                                _p(cache.get("ks")), _p(cache.get("vs")))

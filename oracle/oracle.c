@@ -308,6 +308,15 @@ typedef struct {
     uint16_t *ks, *vs;
 } kv_cache;
 
+/* The format of one plane (which = 0: keys, 1: values) of a cache type: the
+ * asymmetric types quantise keys and values differently ("Luce DFlash"
+ * README, "Asymmetric K/V quantization"). */
+static int plane_type(int type, int which) {
+    if (type == ORC_KV_Q8_0_Q4_0) return which ? ORC_KV_Q4_0 : ORC_KV_Q8_0;
+    if (type == ORC_KV_Q4_0_Q8_0) return which ? ORC_KV_Q8_0 : ORC_KV_Q4_0;
+    return type;
+}
+
 static size_t kv_row_bytes(int type, int D) {
     return type == ORC_KV_Q8_0 ? (size_t)D : type == ORC_KV_Q4_0 ? (size_t)D / 2 : (size_t)D * 4;
 }
@@ -321,15 +330,16 @@ static void kv_read_row(const kv_cache* c, int which, int b, int h, int pos, dou
     size_t row = kv_row_index(c, b, h, pos);
     const uint8_t* plane = (const uint8_t*)(which ? c->vq : c->kq);
     const uint16_t* sc = which ? c->vs : c->ks;
-    const uint8_t* qrow = plane + row * kv_row_bytes(c->type, c->D);
-    if (c->type == ORC_KV_F32) {
+    const int type = plane_type(c->type, which);
+    const uint8_t* qrow = plane + row * kv_row_bytes(type, c->D);
+    if (type == ORC_KV_F32) {
         const float* f = (const float*)qrow;
         for (int d = 0; d < c->D; ++d) x[d] = (double)f[d];
         return;
     }
     const uint16_t* srow = sc + row * (c->D / 32);
     for (int blk = 0; blk < c->D / 32; ++blk) {
-        if (c->type == ORC_KV_Q8_0)
+        if (type == ORC_KV_Q8_0)
             orc_dequantize_q8_0((const int8_t*)qrow + 32 * blk, srow[blk], x + 32 * blk);
         else
             orc_dequantize_q4_0(qrow + 16 * blk, srow[blk], x + 32 * blk);
@@ -341,9 +351,10 @@ static void kv_write_row(kv_cache* c, int which, int b, int h, int pos, const ui
     size_t row = kv_row_index(c, b, h, pos);
     uint8_t* plane = (uint8_t*)(which ? c->vq : c->kq);
     uint16_t* sc = which ? c->vs : c->ks;
-    uint8_t* qrow = plane + row * kv_row_bytes(c->type, c->D);
+    const int type = plane_type(c->type, which);
+    uint8_t* qrow = plane + row * kv_row_bytes(type, c->D);
     float x[32];
-    if (c->type == ORC_KV_F32) {
+    if (type == ORC_KV_F32) {
         float* f = (float*)qrow;
         for (int d = 0; d < c->D; ++d) f[d] = (float)orc_bf16_to_double(src[d]);
         return;
@@ -351,7 +362,7 @@ static void kv_write_row(kv_cache* c, int which, int b, int h, int pos, const ui
     uint16_t* srow = sc + row * (c->D / 32);
     for (int blk = 0; blk < c->D / 32; ++blk) {
         for (int j = 0; j < 32; ++j) x[j] = (float)orc_bf16_to_double(src[32 * blk + j]);
-        if (c->type == ORC_KV_Q8_0)
+        if (type == ORC_KV_Q8_0)
             orc_quantize_q8_0(x, (int8_t*)qrow + 32 * blk, &srow[blk]);
         else
             orc_quantize_q4_0(x, qrow + 16 * blk, &srow[blk]);
@@ -361,7 +372,7 @@ static void kv_write_row(kv_cache* c, int which, int b, int h, int pos, const ui
 static int attn_dims_ok(int B, int N, int Hq, int Hkv, int D, int cap, int window, int type) {
     if (B < 1 || N < 1 || N > 64 || Hkv < 1 || Hq < Hkv || Hq % Hkv != 0) return 0;
     if (D < 1 || cap < 1 || window < 0) return 0;
-    if (type != ORC_KV_Q8_0 && type != ORC_KV_Q4_0 && type != ORC_KV_F32) return 0;
+    if (type < ORC_KV_Q8_0 || type > ORC_KV_Q4_0_Q8_0) return 0;
     if (type != ORC_KV_F32 && D % 32 != 0) return 0;
     return 1;
 }
@@ -534,11 +545,10 @@ int orc_kv_commit(int B, int N, int Hkv, int D, int cap, int kv_type,
      * source rows are read before any is written, because a destination can
      * be another accepted node's source (path [0, 2, 3]: 2 -> 1, 3 -> 2). */
     if (B < 1 || N < 1 || N > 64 || Hkv < 1 || D < 1 || cap < 1) return ORC_ERR_ARG;
-    if (kv_type != ORC_KV_Q8_0 && kv_type != ORC_KV_Q4_0 && kv_type != ORC_KV_F32) return ORC_ERR_ARG;
+    if (kv_type < ORC_KV_Q8_0 || kv_type > ORC_KV_Q4_0_Q8_0) return ORC_ERR_ARG;
     kv_cache c = {B, Hkv, D, cap, kv_type, kq, vq, ks, vs};
-    size_t qb = kv_row_bytes(kv_type, D);
     size_t sb = (kv_type == ORC_KV_F32) ? 0 : (size_t)(D / 32) * sizeof(uint16_t);
-    uint8_t* tmp = malloc((size_t)N * (qb + sb));
+    uint8_t* tmp = malloc((size_t)N * ((size_t)D * 4 + sb));
     for (int b = 0; b < B; ++b) {
         int L = path_len[b], P = n_past[b];
         if (L < 1 || L > N) { free(tmp); return ORC_ERR_ARG; }
@@ -548,6 +558,7 @@ int orc_kv_commit(int B, int N, int Hkv, int D, int cap, int kv_type,
         }
         for (int h = 0; h < Hkv; ++h)
             for (int which = 0; which < 2; ++which) {
+                const size_t qb = kv_row_bytes(plane_type(kv_type, which), D);
                 uint8_t* plane = (uint8_t*)(which ? c.vq : c.kq);
                 uint8_t* sc = (uint8_t*)(which ? c.vs : c.ks);
                 for (int m = 0; m < L; ++m) {

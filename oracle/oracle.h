@@ -67,7 +67,10 @@ extern "C" {
 #endif
 
 enum { ORC_OK = 0, ORC_ERR_ARG = 1, ORC_ERR_TOPOLOGY = 2, ORC_ERR_CAPACITY = 4 };
-enum { ORC_KV_Q8_0 = 0, ORC_KV_Q4_0 = 1, ORC_KV_F32 = 2 };
+/* Cache types; the last two quantise keys and values differently ("Luce
+ * DFlash" README, "Asymmetric K/V quantization"): K q8_0 with V q4_0, and
+ * K q4_0 with V q8_0. */
+enum { ORC_KV_Q8_0 = 0, ORC_KV_Q4_0 = 1, ORC_KV_F32 = 2, ORC_KV_Q8_0_Q4_0 = 3, ORC_KV_Q4_0_Q8_0 = 4 };
 
 /* ---- scalar conversions (the oracle's own) ---- */
 double orc_bf16_to_double(uint16_t h);

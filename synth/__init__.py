@@ -25,7 +25,7 @@ import heapq
 
 import numpy as np
 
-KV_Q8_0, KV_Q4_0, KV_F32 = 0, 1, 2
+KV_Q8_0, KV_Q4_0, KV_F32, KV_Q8_0_Q4_0, KV_Q4_0_Q8_0 = 0, 1, 2, 3, 4
 
 GDN_27B = dict(Hk=16, Hv=48, dk=128, dv=128)
 ATTN_27B = dict(Hq=24, Hkv=4, D=256)
@@ -225,7 +225,8 @@ def kv_cache(rng, B, Hkv, cap, D, kv_type, scale_std=0.02):
 
     q8_0: int8 codes ~ U[-127, 127], fp16 scales ~ |N(0, scale_std)|;
     q4_0: 4-bit codes ~ U[0, 15] (two per byte), same scales;
-    f32:  values ~ N(0, 1), no scale planes."""
+    f32:  values ~ N(0, 1), no scale planes;
+    the asymmetric types draw each plane in its own format."""
     if kv_type == KV_F32:
         return dict(kq=rng.standard_normal((B, Hkv, cap, D), dtype=np.float32),
                     vq=rng.standard_normal((B, Hkv, cap, D), dtype=np.float32), ks=None, vs=None)
@@ -234,14 +235,18 @@ def kv_cache(rng, B, Hkv, cap, D, kv_type, scale_std=0.02):
     def scales():
         return f16_bits(np.abs(rng.standard_normal((B, Hkv, cap, nb), dtype=np.float32)) * scale_std)
 
-    if kv_type == KV_Q8_0:
-        kq = rng.integers(-127, 128, size=(B, Hkv, cap, D), dtype=np.int8)
-        vq = rng.integers(-127, 128, size=(B, Hkv, cap, D), dtype=np.int8)
-    elif kv_type == KV_Q4_0:
-        kq = rng.integers(0, 256, size=(B, Hkv, cap, D // 2), dtype=np.uint8)
-        vq = rng.integers(0, 256, size=(B, Hkv, cap, D // 2), dtype=np.uint8)
-    else:
+    def plane(t):
+        if t == KV_Q8_0:
+            return rng.integers(-127, 128, size=(B, Hkv, cap, D), dtype=np.int8)
+        return rng.integers(0, 256, size=(B, Hkv, cap, D // 2), dtype=np.uint8)
+
+    planes = {KV_Q8_0: (KV_Q8_0, KV_Q8_0), KV_Q4_0: (KV_Q4_0, KV_Q4_0), KV_Q8_0_Q4_0: (KV_Q8_0, KV_Q4_0),
+              KV_Q4_0_Q8_0: (KV_Q4_0, KV_Q8_0)}
+    if kv_type not in planes:
         raise ValueError(kv_type)
+    kt, vt = planes[kv_type]
+    kq = plane(kt)
+    vq = plane(vt)
     return dict(kq=kq, vq=vq, ks=scales(), vs=scales())
 
 

@@ -112,7 +112,8 @@ def test_planted_path_gives_known_length(orc):
 
 
 # ---------------------------------------------------------------- KV commit
-@pytest.mark.parametrize("kv_type", [synth.KV_Q8_0, synth.KV_Q4_0, synth.KV_F32])
+@pytest.mark.parametrize("kv_type", [synth.KV_Q8_0, synth.KV_Q4_0, synth.KV_F32, synth.KV_Q8_0_Q4_0,
+                                     synth.KV_Q4_0_Q8_0])
 def test_kv_compaction_moves_bytes_including_aliasing(orc, kv_type):
     rng = np.random.default_rng(10 + kv_type)
     B, Hkv, cap, D, P = 2, 3, 24, 64, 9

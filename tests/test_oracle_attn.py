@@ -14,6 +14,16 @@ import torch
 import synth
 
 TYPES = [synth.KV_Q8_0, synth.KV_Q4_0, synth.KV_F32]
+# keys and values in different formats ("Asymmetric K/V quantization")
+ASYM = [synth.KV_Q8_0_Q4_0, synth.KV_Q4_0_Q8_0]
+
+
+def _plane_type(kv_type, which):
+    if kv_type == synth.KV_Q8_0_Q4_0:
+        return synth.KV_Q4_0 if which else synth.KV_Q8_0
+    if kv_type == synth.KV_Q4_0_Q8_0:
+        return synth.KV_Q8_0 if which else synth.KV_Q4_0
+    return kv_type
 
 
 def _case(rng, kv_type, parents, P, cap, Hq=4, Hkv=2, D=64):
@@ -36,6 +46,7 @@ def _run(orc, parent, n_nodes, n_past, inp, cache, window, kv_type):
 def _dequant_rows(cache, which, kv_type, b, h, D):
     """numpy dequantisation of every slot of one (sequence, kv head)."""
     q = cache["kq" if which == 0 else "vq"][b, h]
+    kv_type = _plane_type(kv_type, which)
     if kv_type == synth.KV_F32:
         return q.astype(np.float64)
     s = cache["ks" if which == 0 else "vs"][b, h].view(np.float16).astype(np.float64)
@@ -56,7 +67,7 @@ def _ancestors(par, i):
     return set(a)
 
 
-@pytest.mark.parametrize("kv_type", TYPES)
+@pytest.mark.parametrize("kv_type", TYPES + ASYM)
 @pytest.mark.parametrize("window", [0, 5, 13])
 def test_matches_torch_sdpa_with_explicit_mask(orc, kv_type, window):
     # Library cross-check: fp64 scaled_dot_product_attention over the
@@ -195,3 +206,35 @@ def test_row_selection_matches_full_computation(orc):
     flat_part = part.reshape(-1, part.shape[-1])
     for r in rows:
         assert np.array_equal(flat_full[r], flat_part[r])
+
+
+@pytest.mark.parametrize("kv_type", ASYM)
+def test_asymmetric_planes_match_their_symmetric_formats(orc, kv_type):
+    # An asymmetric cache writes the tree's keys exactly as the symmetric
+    # cache of the key format does and its values as the cache of the value
+    # format (compared byte for byte), and reads each plane in its own format
+    # (the output equals fp64 attention over the per-plane dequantised rows).
+    rng = np.random.default_rng(300 + kv_type)
+    par = synth.ddtree(rng, 11, 50)[0]
+    P, cap, Hq, Hkv, D = 17, 32, 4, 2, 64
+    parent, n_nodes, n_past, inp, cache = _case(rng, kv_type, [par], P, cap, Hq, Hkv, D)
+    out, c = _run(orc, parent, n_nodes, n_past, inp, cache, 0, kv_type)
+    kt, vt = _plane_type(kv_type, 0), _plane_type(kv_type, 1)
+    _, ck = _run(orc, parent, n_nodes, n_past, inp, synth.kv_cache(rng, 1, Hkv, cap, D, kt), 0, kt)
+    _, cv = _run(orc, parent, n_nodes, n_past, inp, synth.kv_cache(rng, 1, Hkv, cap, D, vt), 0, vt)
+    n = len(par)
+    for key, src in (("kq", ck), ("ks", ck), ("vq", cv), ("vs", cv)):
+        np.testing.assert_array_equal(c[key][:, :, P:P + n], src[key][:, :, P:P + n])
+    G = Hq // Hkv
+    mask = np.zeros((n, P + n), bool)
+    for i in range(n):
+        mask[i, :P] = True
+        for l in _ancestors(par, i):
+            mask[i, P + l] = True
+    for h in range(Hq):
+        K = torch.from_numpy(_dequant_rows(c, 0, kv_type, 0, h // G, D)[:P + n])
+        V = torch.from_numpy(_dequant_rows(c, 1, kv_type, 0, h // G, D)[:P + n])
+        Q = torch.from_numpy(synth.bf16_to_f32(inp["q"][0, :n, h]).astype(np.float64))
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            Q[None, None], K[None, None], V[None, None], attn_mask=torch.from_numpy(mask)[None, None])
+        np.testing.assert_allclose(out[0, :n, h], ref[0, 0].numpy(), rtol=1e-6, atol=1e-6)
