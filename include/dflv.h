@@ -88,7 +88,11 @@ enum {
 typedef enum {
     DFLV_KV_Q8_0 = 0, /* 32 int8 codes + one fp16 scale d per block: x = d * q */
     DFLV_KV_Q4_0 = 1, /* 32 4-bit codes c + one fp16 scale d per block: x = d * (c - 8) */
-    DFLV_KV_F32 = 2   /* plain fp32 cache (small exactness checks) */
+    DFLV_KV_F32 = 2,  /* plain fp32 cache (small exactness checks) */
+    /* Asymmetric caches ([README] "Asymmetric K/V quantization": keys and
+     * values quantised independently), head sizes 128 and 256: */
+    DFLV_KV_Q8_0_Q4_0 = 3, /* keys q8_0, values q4_0 */
+    DFLV_KV_Q4_0_Q8_0 = 4  /* keys q4_0, values q8_0 */
 } dflv_kv_type;
 
 /* Launch overlap.  Every kernel of this library is launched with
@@ -295,8 +299,9 @@ dflv_status dflv_ddtree_build(const dflv_ddtree_desc* desc, const float* draft_l
  * head) in the cache planes.  window W >= 0: a key at position j is visible
  * to a node at position p iff j <= p and (W == 0 or j > p - W).  Node i sits
  * at position P + depth(i).  scale multiplies q.k (usually 1/sqrt(D)).
- * Supported: 1 <= N_max <= 64; q8_0/q4_0 with D in {64, 128, 256}; f32 with
- * D a multiple of 4, D <= 256. */
+ * Supported: 1 <= N_max <= 64; q8_0/q4_0 with D in {64, 128, 256}; the
+ * asymmetric types with D in {128, 256}; f32 with D a multiple of 4,
+ * D <= 256. */
 typedef struct {
     int32_t B, N_max, Hq, Hkv, D, cap, window;
     dflv_kv_type type;
@@ -304,7 +309,8 @@ typedef struct {
     uint32_t flags; /* 0 or DFLV_FLAG_EARLY_PREFETCH */
 } dflv_attn_desc;
 
-/* One attention layer's cache, structure-of-arrays planes:
+/* One attention layer's cache, structure-of-arrays planes (each plane in its
+ * own format for the asymmetric types):
  *   kq, vq : q8_0: int8 [B][Hkv][cap][D]; q4_0: uint8 [B][Hkv][cap][D/2]
  *            (element j < 16 of a 32-block in the low nibble of byte j,
  *            element j+16 in its high nibble); f32: float [B][Hkv][cap][D]

@@ -42,6 +42,10 @@ dflv_status check_attn_desc(const dflv_attn_desc* d) {
         case DFLV_KV_F32:
             if (d->D % 4 != 0 || d->D > 256) return DFLV_ERR_UNSUPPORTED;
             break;
+        case DFLV_KV_Q8_0_Q4_0:
+        case DFLV_KV_Q4_0_Q8_0:
+            if (d->D != 128 && d->D != 256) return DFLV_ERR_UNSUPPORTED;
+            break;
         default:
             return DFLV_ERR_UNSUPPORTED;
     }

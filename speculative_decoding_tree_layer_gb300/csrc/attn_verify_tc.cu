@@ -59,36 +59,46 @@ constexpr int kStageThreads = kStageWarps * 32;
 constexpr int kStageBarrier = 2;                     // named barrier of the stage warps
 constexpr int kTreeCost = 3;                         // a tree tile (quantise + attend) in cache tiles
 
-template <int D, int TYPE>
-struct TcLayout {
+// One raw plane (codes + scales of kTK keys) in the format T.
+template <int D, int T>
+struct PlaneFmt {
     static constexpr int NB = D / 32;
-    static constexpr int KB = (TYPE == DFLV_KV_Q8_0) ? D : D / 2;  // code bytes per key row
-    static constexpr int RSK = KB + 16;                               // padded raw row stride
+    static constexpr int KB = (T == DFLV_KV_Q8_0) ? D : D / 2;  // code bytes per key row
+    static constexpr int RSK = KB + 16;                            // padded raw row stride
+    static constexpr size_t kRawCodes = (size_t)kTK * RSK;
+    static constexpr size_t kRawScales = (size_t)kTK * NB * 2 + 16;  // + room for a misaligned start
+    static constexpr size_t kRaw = kRawCodes + kRawScales;           // one plane of one tile
+    static_assert(kRawCodes % 16 == 0 && kRaw % 16 == 0, "copy destinations stay 16-byte aligned");
+};
+
+// Keys in format KT, values in format VT (equal unless the cache is
+// asymmetric).
+template <int D, int KT, int VT>
+struct TcLayout {
+    using FK = PlaneFmt<D, KT>;
+    using FV = PlaneFmt<D, VT>;
+    static constexpr int NB = D / 32;
     static constexpr int OS = D + 4;                                  // merge row stride (floats)
     static constexpr size_t kHeader = 2048;   // tree arrays, barriers, flags
     static constexpr size_t kQ = (size_t)kRows * D * 2;
     static constexpr size_t kK = (size_t)2 * kTK * D * 2;    // K_hi rows 0-31, K_lo rows 32-63
     static constexpr size_t kV = (size_t)kTK * D * 2;        // one of V_hi, V_lo
     static constexpr size_t kP = (size_t)kRows * kTK * 2;    // one of P_hi, P_lo
-    static constexpr size_t kRawCodes = (size_t)kTK * RSK;
-    static constexpr size_t kRawScales = (size_t)kTK * NB * 2 + 16;  // + room for a misaligned start
-    static constexpr size_t kRaw = kRawCodes + kRawScales;           // one plane (K or V) of one tile
     static constexpr size_t off_Q = kHeader;
     static constexpr size_t off_K = off_Q + kQ;              // two buffers
     static constexpr size_t off_Vhi = off_K + 2 * kK;
     static constexpr size_t off_Vlo = off_Vhi + kV;
     static constexpr size_t off_Phi = off_Vlo + kV;
     static constexpr size_t off_Plo = off_Phi + kP;
-    static constexpr size_t off_rawK = off_Plo + kP;         // two buffers
-    static constexpr size_t off_rawV = off_rawK + 2 * kRaw;  // two buffers
-    static constexpr size_t loop_total = off_rawV + 2 * kRaw;
+    static constexpr size_t off_rawK = off_Plo + kP;             // two buffers
+    static constexpr size_t off_rawV = off_rawK + 2 * FK::kRaw;  // two buffers
+    static constexpr size_t loop_total = off_rawV + 2 * FV::kRaw;
     static constexpr size_t off_Om = kHeader;
     static constexpr size_t off_Mm = off_Om + (size_t)kRows * OS * 4;
     static constexpr size_t off_Lm = off_Mm + (size_t)kRows * 4;
     static constexpr size_t merge_total = off_Lm + (size_t)kRows * 4;
     static constexpr size_t total = loop_total > merge_total ? loop_total : merge_total;
     static constexpr uint32_t kTmemCols = (D + 4 * kTK <= 256) ? 256 : 512;  // O, then two S buffers
-    static_assert(kRawCodes % 16 == 0 && kRaw % 16 == 0, "bulk-copy destinations stay 16-byte aligned");
 };
 
 // header offsets
@@ -113,7 +123,7 @@ DFLV_DEVINL bool wait_phase(uint64_t* bar, uint32_t parity) {
 template <int D, int TYPE>
 DFLV_DEVINL void stage_hilo(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scales, int count,
                             uint8_t* __restrict__ hi, uint8_t* __restrict__ lo, int st) {
-    using L = TcLayout<D, TYPE>;
+    using L = PlaneFmt<D, TYPE>;
     constexpr int C8 = D / 8;
     constexpr int PER = kTK * C8 / kStageThreads;  // items per thread
     static_assert(PER * kStageThreads == kTK * C8, "items split evenly over the stage threads");
@@ -183,14 +193,14 @@ DFLV_DEVINL void stage_hilo(const uint8_t* __restrict__ codes, const uint16_t* _
 // (their byte offset in the buffer is returned by scale_shift).
 template <int D, int TYPE>
 DFLV_DEVINL int scale_shift(const uint16_t* plane_scales, size_t row0, int start) {
-    using L = TcLayout<D, TYPE>;
+    using L = PlaneFmt<D, TYPE>;
     return (int)(reinterpret_cast<uintptr_t>(plane_scales + (row0 + start) * L::NB) & 15);
 }
 
 template <int D, int TYPE>
 DFLV_DEVINL void issue_raw(const uint8_t* plane_codes, const uint16_t* plane_scales, size_t row0, int start,
                            int count, uint8_t* raw, uint64_t* bar, int st) {
-    using L = TcLayout<D, TYPE>;
+    using L = PlaneFmt<D, TYPE>;
     constexpr int CPR = L::KB / 16;  // 16-byte chunks per key row
     for (int idx = st; idx < count * CPR; idx += 32) {
         const int c = idx / CPR, ch = idx % CPR;
@@ -221,9 +231,11 @@ struct TileInfo {
     bool tree;
 };
 
-template <int D, int TYPE>
+template <int D, int KT, int VT>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, int RT, int CS) {
-    using L = TcLayout<D, TYPE>;
+    using L = TcLayout<D, KT, VT>;
+    using FK = typename L::FK;
+    using FV = typename L::FV;
     constexpr int NB = L::NB, OS = L::OS;
     extern __shared__ __align__(1024) unsigned char smem[];
     int32_t* par_s = reinterpret_cast<int32_t*>(smem);
@@ -307,10 +319,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
     auto issue_tile_raw = [&](int u, bool k_plane, bool v_plane) {
         const TileInfo ti = tile(u);
         if (k_plane)
-            issue_raw<D, TYPE>(kq, a.ks, plane_row0, ti.start, ti.count, rawK + (u & 1) * L::kRaw,
+            issue_raw<D, KT>(kq, a.ks, plane_row0, ti.start, ti.count, rawK + (u & 1) * FK::kRaw,
                                bars + kRawK0 + (u & 1), lane);
         if (v_plane)
-            issue_raw<D, TYPE>(vq, a.vs, plane_row0, ti.start, ti.count, rawV + (u & 1) * L::kRaw,
+            issue_raw<D, VT>(vq, a.vs, plane_row0, ti.start, ti.count, rawV + (u & 1) * FV::kRaw,
                                bars + kRawV0 + (u & 1), lane);
     };
     // the first two tiles' raw planes are requested at once
@@ -367,8 +379,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
             const int kk = vplane ? k - nblk : k, row = r_lo + kk / NB, blk = kk % NB;
             const uint16_t* src = (vplane ? a.v_new : a.k_new) + (((size_t)b * N + row) * a.Hkv + kvh) * D + blk * 32;
             const size_t slot = plane_row0 + P + row;
-            quantize_block<TYPE>(src, (vplane ? vq : kq) + slot * L::KB + blk * (L::KB / NB),
-                                 (vplane ? a.vs : a.ks) + slot * NB + blk);
+            if (vplane)
+                quantize_block<VT>(src, vq + slot * FV::KB + blk * (FV::KB / NB), a.vs + slot * NB + blk);
+            else
+                quantize_block<KT>(src, kq + slot * FK::KB + blk * (FK::KB / NB), a.ks + slot * NB + blk);
         }
         __threadfence();
     }
@@ -511,12 +525,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
             bool ok = true;
             if (t < T) {
                 const TileInfo ti = tile(t);
-                uint8_t* rk = rawK + (t & 1) * L::kRaw;
+                uint8_t* rk = rawK + (t & 1) * FK::kRaw;
                 ok = ok && wait_phase(bars + kRawK0 + (t & 1), (t >> 1) & 1);
-                const int shift = scale_shift<D, TYPE>(a.ks, plane_row0, ti.start);
+                const int shift = scale_shift<D, KT>(a.ks, plane_row0, ti.start);
                 if (t >= 2) ok = ok && wait_phase(bars + kSFull0 + (t & 1), ((t - 2) >> 1) & 1);
                 if (ok)
-                    stage_hilo<D, TYPE>(rk, reinterpret_cast<const uint16_t*>(rk + L::kRawCodes + shift), ti.count,
+                    stage_hilo<D, KT>(rk, reinterpret_cast<const uint16_t*>(rk + FK::kRawCodes + shift), ti.count,
                                         smem + L::off_K + (t & 1) * L::kK,
                                         smem + L::off_K + (t & 1) * L::kK + L::kK / 2, st);
                 mbar_arrive(bars + kKFree0 + (t & 1));  // raw K buffer of this parity released
@@ -526,12 +540,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
             if (t >= 1 && ok) {
                 const int u = t - 1;
                 const TileInfo tu = tile(u);
-                uint8_t* rv = rawV + (u & 1) * L::kRaw;
+                uint8_t* rv = rawV + (u & 1) * FV::kRaw;
                 ok = ok && wait_phase(bars + kRawV0 + (u & 1), (u >> 1) & 1);
-                const int shift = scale_shift<D, TYPE>(a.vs, plane_row0, tu.start);
+                const int shift = scale_shift<D, VT>(a.vs, plane_row0, tu.start);
                 if (u >= 1) ok = ok && wait_phase(bars + kODone, (u - 1) & 1);
                 if (ok)
-                    stage_hilo<D, TYPE>(rv, reinterpret_cast<const uint16_t*>(rv + L::kRawCodes + shift), tu.count,
+                    stage_hilo<D, VT>(rv, reinterpret_cast<const uint16_t*>(rv + FV::kRawCodes + shift), tu.count,
                                         smem + L::off_Vhi, smem + L::off_Vlo, st);
                 mbar_arrive(bars + kVFree0 + (u & 1));  // raw V buffer of this parity released
                 fence_proxy_async_smem();
@@ -733,10 +747,10 @@ int active_clusters(Kernel kern, size_t smem, int cs) {
     return cache[cs] > 0 ? cache[cs] : 0;
 }
 
-template <int D, int TYPE>
+template <int D, int KT, int VT>
 cudaError_t launch_tc(const AttnVerifyArgs& a, cudaStream_t stream) {
-    using L = TcLayout<D, TYPE>;
-    auto kern = attn_tc_kernel<D, TYPE>;
+    using L = TcLayout<D, KT, VT>;
+    auto kern = attn_tc_kernel<D, KT, VT>;
     cudaError_t e = ensure_smem(kern, L::total);
     if (e != cudaSuccess) return e;
     const int rows = (a.Hq / a.Hkv) * a.N_max;
@@ -773,11 +787,22 @@ cudaError_t launch_tc(const AttnVerifyArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
+template <int D>
+cudaError_t launch_tc_d(const AttnVerifyArgs& a, cudaStream_t stream) {
+    constexpr int Q8 = DFLV_KV_Q8_0, Q4 = DFLV_KV_Q4_0;
+    switch (a.type) {
+        case DFLV_KV_Q8_0: return launch_tc<D, Q8, Q8>(a, stream);
+        case DFLV_KV_Q4_0: return launch_tc<D, Q4, Q4>(a, stream);
+        case DFLV_KV_Q8_0_Q4_0: return launch_tc<D, Q8, Q4>(a, stream);
+        case DFLV_KV_Q4_0_Q8_0: return launch_tc<D, Q4, Q8>(a, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 cudaError_t launch_attn_tree_verify_tc(const AttnVerifyArgs& a, cudaStream_t stream) {
-    const bool q8 = a.type == DFLV_KV_Q8_0;
     switch (a.D) {
-        case 128: return q8 ? launch_tc<128, DFLV_KV_Q8_0>(a, stream) : launch_tc<128, DFLV_KV_Q4_0>(a, stream);
-        case 256: return q8 ? launch_tc<256, DFLV_KV_Q8_0>(a, stream) : launch_tc<256, DFLV_KV_Q4_0>(a, stream);
+        case 128: return launch_tc_d<128>(a, stream);
+        case 256: return launch_tc_d<256>(a, stream);
         default: return cudaErrorInvalidValue;
     }
 }

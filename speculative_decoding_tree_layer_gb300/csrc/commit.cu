@@ -133,14 +133,13 @@ __device__ void commit_kv_head(const CommitArgs& a, int layer, int b, int kvh, u
     const CommitAttnLayer ly = a.attn[layer];
     const size_t row0 = ((size_t)b * a.Hkv + kvh) * a.cap;
     const int nb = a.D / 32;
-    const int code_bytes = a.type == DFLV_KV_Q8_0 ? a.D : a.type == DFLV_KV_Q4_0 ? a.D / 2 : a.D * 4;
     // four planes: K codes, V codes, K scales, V scales (no scales for f32)
     for (int plane = 0; plane < 4; ++plane) {
         uint8_t* base;
         int rb;
         if (plane < 2) {
             base = plane == 0 ? ly.kq : ly.vq;
-            rb = code_bytes;
+            rb = kv_code_bytes(a.type, plane, a.D);
         } else {
             if (a.type == DFLV_KV_F32) break;
             base = reinterpret_cast<uint8_t*>(plane == 2 ? ly.ks : ly.vs);
@@ -193,7 +192,7 @@ cudaError_t launch_commit_rollback(const CommitArgs& a, cudaStream_t stream) {
         size_t smem = 0;
         if (a.n_gdn > 0) smem = (size_t)a.N_max * (a.dv + a.dk) * 4;
         if (a.n_attn > 0) {
-            const int code_bytes = a.type == DFLV_KV_Q8_0 ? a.D : a.type == DFLV_KV_Q4_0 ? a.D / 2 : a.D * 4;
+            const int code_bytes = max(kv_code_bytes(a.type, 0, a.D), kv_code_bytes(a.type, 1, a.D));
             const size_t kv = (size_t)a.N_max * code_bytes;
             if (kv > smem) smem = kv;
         }

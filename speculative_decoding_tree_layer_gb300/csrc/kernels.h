@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/dflv.h"
+
 namespace dflv {
 
 struct GdnVerifyArgs {
@@ -57,6 +59,15 @@ struct AttnVerifyArgs {
 
 cudaError_t launch_attn_tree_verify(const AttnVerifyArgs& a, cudaStream_t stream);
 cudaError_t launch_attn_tree_verify_tc(const AttnVerifyArgs& a, cudaStream_t stream);
+
+// Code bytes of one cache row of plane `plane` (0: keys, 1: values) for a
+// dflv_kv_type (the asymmetric types differ between the planes).
+__host__ __device__ inline int kv_code_bytes(int type, int plane, int D) {
+    int t = type;
+    if (type == DFLV_KV_Q8_0_Q4_0) t = plane ? DFLV_KV_Q4_0 : DFLV_KV_Q8_0;
+    else if (type == DFLV_KV_Q4_0_Q8_0) t = plane ? DFLV_KV_Q8_0 : DFLV_KV_Q4_0;
+    return t == DFLV_KV_Q8_0 ? D : t == DFLV_KV_Q4_0 ? D / 2 : D * 4;
+}
 
 struct AcceptArgs {
     int B, N_max, vocab;

@@ -71,6 +71,9 @@ def test_attn_host_validation(lib):
     assert call(d(Hq=25)) == dflv.DFLV_ERR_INVALID_ARG
     assert call(d(cap=10)) == dflv.DFLV_ERR_CAPACITY
     assert call(d(kv_type=7)) == dflv.DFLV_ERR_UNSUPPORTED
+    # asymmetric caches run on the tensor-core kernel only (head sizes 128, 256)
+    assert call(d(kv_type=dflv.DFLV_KV_Q8_0_Q4_0, D=64)) == dflv.DFLV_ERR_UNSUPPORTED
+    assert call(d(kv_type=dflv.DFLV_KV_Q4_0_Q8_0, D=64)) == dflv.DFLV_ERR_UNSUPPORTED
     assert call(d(scale=float("nan"))) == dflv.DFLV_ERR_INVALID_ARG
     assert call(d(), cache=dflv.dflv_kv_layer(16, 16, None, 16)) == dflv.DFLV_ERR_INVALID_ARG
     assert call(d(), cache=dflv.dflv_kv_layer(16, 16, 18, 16)) == dflv.DFLV_ERR_INVALID_ARG  # scale rows

@@ -114,11 +114,12 @@ def gpu_commit(dflv, gdn_layers, attn_layers, path, path_len, n_past, dims, expe
     return host(keep["n_past"])
 
 
-@pytest.mark.parametrize("kv_type", [synth.KV_Q8_0, synth.KV_Q4_0, synth.KV_F32])
+@pytest.mark.parametrize("kv_type", [synth.KV_Q8_0, synth.KV_Q4_0, synth.KV_F32, synth.KV_Q8_0_Q4_0,
+                                     synth.KV_Q4_0_Q8_0])
 def test_commit_gdn_and_kv(dflv, orc, kv_type):
     rng = np.random.default_rng(40 + kv_type)
     Hk, Hv, dk, dv = 2, 6, 128, 64
-    Hq, Hkv, D = 4, 2, 64 if kv_type != synth.KV_F32 else 16
+    Hq, Hkv, D = 4, 2, {synth.KV_F32: 16, synth.KV_Q8_0_Q4_0: 128, synth.KV_Q4_0_Q8_0: 128}.get(kv_type, 64)
     B, N = 3, 9
     parents = [np.array([-1, 0, 0, 2, 3, 1, 4, 6, 6], np.int32),  # accepted path 0, 2, 3 aliases
                synth.chain_tree(9), np.array([-1, 0, 1, 1], np.int32)]
@@ -153,11 +154,10 @@ def test_commit_gdn_and_kv(dflv, orc, kv_type):
                                ginp["state"])
     assert_close(host(keep["state"]), ref_state, what="committed state")
     orc.kv_commit(before, kv_type, path, path_len, P)
-    dt = {synth.KV_Q8_0: np.int8, synth.KV_Q4_0: np.uint8, synth.KV_F32: np.float32}[kv_type]
     for key in ("kq", "vq", "ks", "vs"):
         if before[key] is None:
             continue
-        got = host(dc[key], np.uint16 if key in ("ks", "vs") else dt)
+        got = host(dc[key], before[key].dtype)
         for b in range(B):
             # slots below P + L are fully specified; [P + L, P + N) are not
             hi = P[b] + path_len[b]

@@ -27,6 +27,10 @@ def dflv():
 def _plane_np_dtype(key, kv_type):
     if key in ("ks", "vs"):
         return np.uint16
+    if kv_type == synth.KV_Q8_0_Q4_0:
+        kv_type = synth.KV_Q8_0 if key == "kq" else synth.KV_Q4_0
+    elif kv_type == synth.KV_Q4_0_Q8_0:
+        kv_type = synth.KV_Q4_0 if key == "kq" else synth.KV_Q8_0
     return {synth.KV_Q8_0: np.int8, synth.KV_Q4_0: np.uint8, synth.KV_F32: np.float32}[kv_type]
 
 
@@ -92,6 +96,11 @@ SMALL = [
     (synth.KV_Q8_0, [64], 513, 600, 6, 1, 256, 20, "chain"),       # window shorter than the chain
     (synth.KV_Q4_0, [64, 3], [1000, 5], 1100, 12, 2, 128, 0, "ddtree"),
     (synth.KV_Q8_0, [1], 77, 80, 24, 4, 256, 2048, "uniform"),     # window covering everything
+    # asymmetric caches: keys and values in different formats
+    (synth.KV_Q8_0_Q4_0, [22, 9], [300, 57], 400, 6, 1, 256, 64, "ddtree"),
+    (synth.KV_Q4_0_Q8_0, [22, 9], [300, 57], 400, 6, 1, 256, 64, "ddtree"),
+    (synth.KV_Q8_0_Q4_0, [64, 3], [1000, 5], 1100, 12, 2, 128, 0, "ddtree"),
+    (synth.KV_Q4_0_Q8_0, [22], 4096, 4200, 24, 4, 256, 2048, "ddtree"),
 ]
 
 
