@@ -37,6 +37,14 @@ constexpr int kTopkThreads = 512;
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr float kLog2e = 1.4426950408889634f;
 
+// 2^x by the hardware's approximate base-2 exponential (PTX ex2.approx; a
+// few ulp, far inside what a log-sum-exp over the vocabulary needs).
+DFLV_DEVINL float ex2(float x) {
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // (v, i) beats (bv, bi): larger value, or equal value and lower index.
 DFLV_DEVINL bool beats(float v, int i, float bv, int bi) { return v > bv || (v == bv && i < bi); }
 
@@ -49,7 +57,7 @@ DFLV_DEVINL void lse_merge(float& m, float& s, float m2, float s2) {
         return;
     }
     const float mn = fmaxf(m, m2);
-    s = s * exp2f((m - mn) * kLog2e) + s2 * exp2f((m2 - mn) * kLog2e);
+    s = s * ex2((m - mn) * kLog2e) + s2 * ex2((m2 - mn) * kLog2e);
     m = mn;
 }
 
@@ -157,22 +165,30 @@ __global__ void __launch_bounds__(kTopkThreads) draft_topk_kernel(const DdtreeAr
 #pragma unroll
         for (int u = 0; u < 8; ++u) cm = fmaxf(cm, fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w)));
         if (cm > m) {  // the chunk's first value is always in range, so cm is finite
-            s *= exp2f((m - cm) * kLog2e);
+            s *= ex2((m - cm) * kLog2e);
             m = cm;
         }
         const float mb = m * kLog2e;
-        float cs = 0.f;
+        float cs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-            cs += exp2f(fmaf(x[u].x, kLog2e, -mb)) + exp2f(fmaf(x[u].y, kLog2e, -mb)) +
-                  exp2f(fmaf(x[u].z, kLog2e, -mb)) + exp2f(fmaf(x[u].w, kLog2e, -mb));
-            const int c = (q + u * kTopkThreads) * 4;
-            topk_insert<K>(v, ix, x[u].x, c);
-            topk_insert<K>(v, ix, x[u].y, c + 1);
-            topk_insert<K>(v, ix, x[u].z, c + 2);
-            topk_insert<K>(v, ix, x[u].w, c + 3);
+            cs[0] += ex2(fmaf(x[u].x, kLog2e, -mb));
+            cs[1] += ex2(fmaf(x[u].y, kLog2e, -mb));
+            cs[2] += ex2(fmaf(x[u].z, kLog2e, -mb));
+            cs[3] += ex2(fmaf(x[u].w, kLog2e, -mb));
         }
-        s += cs;
+        s += (cs[0] + cs[1]) + (cs[2] + cs[3]);
+        // the top-K list only looks at a chunk whose maximum could enter it
+        if (cm > v[K - 1]) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int c = (q + u * kTopkThreads) * 4;
+                topk_insert<K>(v, ix, x[u].x, c);
+                topk_insert<K>(v, ix, x[u].y, c + 1);
+                topk_insert<K>(v, ix, x[u].z, c + 2);
+                topk_insert<K>(v, ix, x[u].w, c + 3);
+            }
+        }
     }
 
     // warp, then block
