@@ -16,6 +16,7 @@
 // matching index.
 #include <climits>
 
+#include "cluster.cuh"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -24,21 +25,6 @@ namespace dflv {
 namespace {
 
 constexpr int kArgmaxThreads = 512;
-
-DFLV_DEVINL uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
-    return r;
-}
-DFLV_DEVINL void cluster_barrier() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::
-                     : "memory");
-}
-DFLV_DEVINL uint32_t dsmem_addr(const void* p, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-    return r;
-}
 
 // (v, i) beats (bv, bi): larger value, or equal value and lower index.
 DFLV_DEVINL void better(float v, int i, float& bv, int& bi) {
@@ -51,7 +37,7 @@ DFLV_DEVINL void better(float v, int i, float& bv, int& bi) {
 __global__ void __launch_bounds__(kArgmaxThreads) accept_argmax_kernel(AcceptArgs a, int CS) {
     __shared__ float red_v[kArgmaxThreads / 32];
     __shared__ int red_i[kArgmaxThreads / 32];
-    const int rank = (int)cluster_rank();
+    const int rank = (int)cluster_ctarank();
     const int i = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     grid_dependency_wait();
@@ -111,18 +97,16 @@ __global__ void __launch_bounds__(kArgmaxThreads) accept_argmax_kernel(AcceptArg
         red_v[0] = bv;
         red_i[0] = bi;
     }
-    cluster_barrier();
+    cluster_sync_all();
     if (rank == 0 && tid == 0) {
         for (int q = 1; q < CS; ++q) {
-            float ov;
-            int oi;
-            asm volatile("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(ov) : "r"(dsmem_addr(&red_v[0], q)) : "memory");
-            asm volatile("ld.shared::cluster.s32 %0, [%1];\n" : "=r"(oi) : "r"(dsmem_addr(&red_i[0], q)) : "memory");
+            const float ov = ld_dsmem_f32(map_to_rank(smem_u32(&red_v[0]), q));
+            const int oi = ld_dsmem_s32(map_to_rank(smem_u32(&red_i[0]), q));
             better(ov, oi, bv, bi);
         }
         a.best[(size_t)b * a.N_max + i] = bi;
     }
-    cluster_barrier();  // keep this CTA's shared memory alive for rank 0
+    cluster_sync_all();  // keep this CTA's shared memory alive for rank 0
 }
 
 __global__ void accept_walk_kernel(AcceptArgs a) {
