@@ -57,6 +57,8 @@ constexpr int kThreads = (kLoadWarp + 2) * 32;
 constexpr int kStage0 = kSoftWarps * 32;             // first stage thread
 constexpr int kStageThreads = kStageWarps * 32;
 constexpr int kStageBarrier = 2;                     // named barrier of the stage warps
+constexpr int kPrepBarrier = 3;                      // named barrier of the other warps (Q, tree rows)
+constexpr int kPrepThreads = kThreads - kStageThreads;
 constexpr int kTreeCost = 3;                         // a tree tile (quantise + attend) in cache tiles
 
 // One raw plane (codes + scales of kTK keys) in the format T.
@@ -214,6 +216,11 @@ DFLV_DEVINL void issue_raw(const uint8_t* plane_codes, const uint16_t* plane_sca
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// barrier over `count` threads (whole warps) under id
+DFLV_DEVINL void named_barrier_sync_n(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // barrier over `count` threads (whole warps) under id; returns the OR of
 // pred over them, the same value in every participating thread
 DFLV_DEVINL bool named_barrier_or(int id, int count, bool pred) {
@@ -330,17 +337,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
         for (int u = 0; u < min(T, 2); ++u)
             if (!tile(u).tree) issue_tile_raw(u, warp == kLoadWarp, warp != kLoadWarp);
 
-    if (early) grid_dependency_wait();
+    // The stage warps go straight to their loop: they read only the raw
+    // tiles (cached slots below P, or tree slots that the other warps
+    // quantise and the load warps request after this block), so with early
+    // prefetch they stage the first cached tiles before the dependency wait.
+    // The other warps wait, prepare Q and quantise the tree rows, and meet at
+    // their own barrier.
+    const bool stage_warp = warp >= kSoftWarps && warp < kMmaWarp;
+    const int pt = warp < kSoftWarps ? tid : tid - kStageThreads;  // index among the other warps
+    if (early && !stage_warp) grid_dependency_wait();
 
     // ---- Q rows -> fp16, core-matrix layout (rows past the tile are zero);
     //      every load of a thread is issued before the first is used
-    {
+    if (!stage_warp) {
         constexpr int C8 = D / 8;
-        constexpr int PER = (kRows * C8 + kThreads - 1) / kThreads;
+        constexpr int PER = (kRows * C8 + kPrepThreads - 1) / kPrepThreads;
         uint4 inq[PER];
 #pragma unroll
         for (int j = 0; j < PER; ++j) {
-            const int idx = tid + j * kThreads;
+            const int idx = pt + j * kPrepThreads;
             const int r = (idx & 7) + (idx / (8 * C8)) * 8;
             const int d8 = (idx >> 3) % C8;
             const int rho = row0 + r;
@@ -353,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
         }
 #pragma unroll
         for (int j = 0; j < PER; ++j) {
-            const int idx = tid + j * kThreads;
+            const int idx = pt + j * kPrepThreads;
             if (idx >= kRows * C8) break;
             const int r = (idx & 7) + (idx / (8 * C8)) * 8;
             const int d8 = (idx >> 3) % C8;
@@ -370,11 +385,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
     //      tile quantises that tile's rows into the cache itself (every row
     //      tile's CTA writes the same bytes) and copies them back like a
     //      cached tile once this block's writes are visible
-    {
+    if (!stage_warp) {
         const int r_lo = max(0, g0 - n_cache_tiles) * kTK;
         const int r_hi = min(n, (g0 + T - n_cache_tiles) * kTK);
         const int nblk = (r_hi > r_lo) ? (r_hi - r_lo) * NB : 0;
-        for (int k = tid; k < 2 * nblk; k += kThreads) {
+        for (int k = pt; k < 2 * nblk; k += kPrepThreads) {
             const bool vplane = k >= nblk;
             const int kk = vplane ? k - nblk : k, row = r_lo + kk / NB, blk = kk % NB;
             const uint16_t* src = (vplane ? a.v_new : a.k_new) + (((size_t)b * N + row) * a.Hkv + kvh) * D + blk * 32;
@@ -385,9 +400,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
                 quantize_block<KT>(src, kq + slot * FK::KB + blk * (FK::KB / NB), a.ks + slot * NB + blk);
         }
         __threadfence();
+        fence_proxy_async_smem();
+        named_barrier_sync_n(kPrepBarrier, kPrepThreads);
     }
-    fence_proxy_async_smem();
-    __syncthreads();
 
     const uint32_t tmem_O = tmem;  // columns [0, D); S buffers at D and D + 64
     float m_run = -INFINITY, l_run = 0.f;
