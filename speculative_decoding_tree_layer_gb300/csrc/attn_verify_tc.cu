@@ -735,19 +735,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
 }
 
 // How many clusters of cs CTAs of this kernel can be resident at once at
-// this shared-memory size (queried once per kernel and cluster size; 16 uses
-// the non-portable cluster size).
-template <typename Kernel>
-int active_clusters(Kernel kern, size_t smem, int cs) {
-    static int cache[17] = {0};
+// this shared-memory size (queried once per kernel instantiation and
+// cluster size; sizes above 8 are the non-portable ones, allowed here for
+// the kernel before the query and so before any launch that uses them).
+template <int D, int KT, int VT>
+int active_clusters(int cs) {
+    static int cache[17] = {0};  // one table per instantiation
     if (cs < 1 || cs > 16) return 0;
     if (cache[cs] == 0) {
+        auto kern = attn_tc_kernel<D, KT, VT>;
         int n = 0;
         if (cs > 8) cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(cs, 1, 1);
         cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = smem;
+        cfg.dynamicSmemBytes = TcLayout<D, KT, VT>::total;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = cs;
@@ -772,15 +774,16 @@ cudaError_t launch_tc(const AttnVerifyArgs& a, cudaStream_t stream) {
     const long range = (a.window > 0) ? (long)a.window - 1 : (long)a.cap;
     const long tiles = (range + kTK - 1) / kTK + 3;
     const int sms = sm_count_cached();
-    // the largest cluster (<= 16) that still lets every cluster be resident
-    // at once and that the key range can feed
+    // the largest cluster (<= 16, any size: the key tiles split by cost, so
+    // a size between powers of two still shortens the longest CTA) that
+    // still lets every cluster be resident at once and that the key range
+    // can feed
     auto choose_cs = [&](int n_rt) {
         const long clusters = (long)n_rt * a.Hkv * a.B;
-        int cs = 1;
-        while (cs < 16 && clusters * cs * 2 <= sms && cs * 2 <= tiles &&
-               active_clusters(kern, L::total, cs * 2) >= clusters)
-            cs *= 2;
-        return cs;
+        for (int cs = 16; cs > 1; --cs)
+            if (clusters * cs <= sms && cs * 2 <= tiles && active_clusters<D, KT, VT>(cs) >= clusters)
+                return cs;
+        return 1;
     };
     // row tiles: as few as the 128-row MMA allows; when the key range is
     // short (latency-bound: a few tiles per CTA) one more row tile is taken
@@ -791,7 +794,7 @@ cudaError_t launch_tc(const AttnVerifyArgs& a, cudaStream_t stream) {
         const int n2 = n_rt + 1, cs2 = choose_cs(n2);
         const long ctas = (long)n_rt * a.Hkv * a.B * cs, ctas2 = (long)n2 * a.Hkv * a.B * cs2;
         if ((rows + n2 - 1) / n2 >= 32 && tiles <= 16L * cs2 && ctas2 * 4 > ctas * 5 &&
-            active_clusters(kern, L::total, cs2) >= (long)n2 * a.Hkv * a.B) {
+            active_clusters<D, KT, VT>(cs2) >= (long)n2 * a.Hkv * a.B) {
             n_rt = n2;
             cs = cs2;
         }
