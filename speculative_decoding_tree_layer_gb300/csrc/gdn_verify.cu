@@ -252,7 +252,7 @@ DFLV_DEVINL void gdn_apply_pending(const GdnVerifyArgs& a, float* S_s, const uin
 }
 
 template <int DK, int RB, int NPT>
-__global__ void __launch_bounds__(kGdnThreads, NPT == 32 ? 3 : 2)
+__global__ void __launch_bounds__(kGdnThreads, (NPT == 32 && RB <= 32) ? 3 : 2)
     gdn_tree_verify_kernel(GdnVerifyArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     const GdnSmemLayout L(NPT, DK, RB);
@@ -518,6 +518,11 @@ cudaError_t launch_dk_rb(const GdnVerifyArgs& a, cudaStream_t stream) {
 template <int DK>
 cudaError_t launch_dk(const GdnVerifyArgs& a, cudaStream_t stream) {
     const bool small = a.N_max <= 32;
+    // Trees of up to 32 nodes: 64 state rows per CTA when dv allows it, so
+    // that a head takes dv/64 CTAs and the launch stays within one CTA per SM
+    // at the common shapes (its slowest CTAs then share no SM with another
+    // CTA of the same launch); larger trees keep 32 rows (registers).
+    if (small && a.dv % 64 == 0) return launch_dk_rb<DK, 64, 32>(a, stream);
     if (a.dv % 32 == 0)
         return small ? launch_dk_rb<DK, 32, 32>(a, stream) : launch_dk_rb<DK, 32, 64>(a, stream);
     return small ? launch_dk_rb<DK, 16, 32>(a, stream) : launch_dk_rb<DK, 16, 64>(a, stream);
@@ -526,7 +531,8 @@ cudaError_t launch_dk(const GdnVerifyArgs& a, cudaStream_t stream) {
 }  // namespace
 
 size_t gdn_verify_smem_bytes(int N_max, int dk, int dv) {
-    return GdnSmemLayout(N_max <= 32 ? 32 : 64, dk, dv % 32 == 0 ? 32 : 16).total;
+    const bool small = N_max <= 32;
+    return GdnSmemLayout(small ? 32 : 64, dk, (small && dv % 64 == 0) ? 64 : dv % 32 == 0 ? 32 : 16).total;
 }
 
 cudaError_t launch_gdn_tree_verify(const GdnVerifyArgs& a, cudaStream_t stream) {

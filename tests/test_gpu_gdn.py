@@ -62,6 +62,8 @@ CASES = [
     (1, [64], 4, 8, 128, 64, "ddtree"),
     (1, [64], 1, 2, 128, 128, "chain"),        # depth 63
     (3, [13, 64, 40], 2, 4, 128, 128, "uniform"),
+    (2, [22, 31], 2, 4, 128, 128, "ddtree"),    # up to 32 nodes: 64-row blocks
+    (1, [32], 1, 2, 64, 64, "chain"),           # one 64-row block per head
 ]
 
 
