@@ -14,7 +14,7 @@ What it computes, from the pages:
     options table; README server parameters: a confidence margin, off by
     default, 6 with SpecLA).
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
   * log-probabilities are the log-softmax of the draft's logits per
     position; a node's score is the sum of the log-probabilities of the
     tokens on its root path (the root scores 0);
