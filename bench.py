@@ -459,6 +459,128 @@ def kernel_chain_ms(S, torch, stream, steps, warmup):
     return out
 
 
+# ---------------------------------------------------------------------------- at scale
+# The long-context, wide-tree stress shapes: 8 sequences with 64-node trees,
+# one attention layer over a 131,072-token q4_0 cache with full attention
+# (24 query / 4 KV heads, D = 256) and one GDN layer of the 27B shape.
+SCALE_B, SCALE_N, SCALE_CTX = 8, 64, 131072
+
+
+def scale_bytes_attn():
+    Hq, Hkv, D, B, N, P = ATT["Hq"], ATT["Hkv"], ATT["D"], SCALE_B, SCALE_N, SCALE_CTX
+    row = D // 2 + D // 32 * 2                 # q4_0: codes + fp16 scales per (token, head)
+    kv = B * 2 * P * Hkv * row
+    return kv + B * N * (Hq * D * 2 + Hq * D * 4 + 2 * Hkv * D * 2) + B * 2 * 2 * N * Hkv * row
+
+
+def scale_flops_attn():
+    """Q K^T and P V over every (node, query head, visible key): 2 * 2 * D
+    flops each (the kernel's hi/lo operand split adds passes, not counted)."""
+    Hq, D, B, N, P = ATT["Hq"], ATT["D"], SCALE_B, SCALE_N, SCALE_CTX
+    return 2 * 2 * D * B * N * Hq * (P + N)
+
+
+def bf16_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops_sustained"]), "measured sustained"
+    except (OSError, KeyError, ValueError):
+        return 1700.0, "fallback sustained"
+
+
+def scale_bytes_gdn():
+    Hk, Hv, dk, dv, B, N = GDN["Hk"], GDN["Hv"], GDN["dk"], GDN["dv"], SCALE_B, SCALE_N
+    return B * (Hv * dv * dk * 4 + 2 * N * Hk * dk * 2 + N * Hv * dv * 2 + 2 * N * Hv * 4 + 2 * N * Hv * dv * 4 +
+                N * Hv * 4 + N * Hk * dk * 2)
+
+
+def scale_measure(torch, dflv, reps=8, rounds=10):
+    """Per-launch time of the attention and GDN verify at the stress shapes,
+    launched back to back (same buffers, early prefetch after the first);
+    inputs drawn on the device from a seeded generator."""
+    dev = "cuda"
+    g = torch.Generator(device=dev)
+    g.manual_seed(SEED + 31)
+    B, N, P = SCALE_B, SCALE_N, SCALE_CTX
+    Hq, Hkv, D = ATT["Hq"], ATT["Hkv"], ATT["D"]
+    cap = P + N
+    out = {}
+    rng = np.random.default_rng(SEED + 37)
+    pars = [synth.ddtree(rng, N, VOCAB)[0] for _ in range(B)]
+    parent, n_nodes = synth.batch_trees(pars, N)
+    par_d, nn_d = torch.from_numpy(parent).to(dev), torch.from_numpy(n_nodes).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream()
+
+    def bf16(*shape, unit=False):
+        x = torch.randn(*shape, generator=g, device=dev)
+        if unit:  # q and k of a GDN layer are L2-normalised per head
+            x = x / x.norm(dim=-1, keepdim=True)
+        return x.to(torch.bfloat16).view(torch.int16)
+
+    def timed(fn):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            fn(0)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph, stream=stream):
+            for r in range(reps):
+                fn(r)
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record()
+            for _ in range(rounds):
+                graph.replay()
+            e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / (rounds * reps)
+
+    # attention: q4_0 cache, full attention
+    kq = torch.randint(0, 256, (B, Hkv, cap, D // 2), generator=g, device=dev, dtype=torch.uint8)
+    vq = torch.randint(0, 256, (B, Hkv, cap, D // 2), generator=g, device=dev, dtype=torch.uint8)
+    ks = (torch.rand(B, Hkv, cap, D // 32, generator=g, device=dev) * 0.02).to(torch.float16).view(torch.int16)
+    vs = (torch.rand(B, Hkv, cap, D // 32, generator=g, device=dev) * 0.02).to(torch.float16).view(torch.int16)
+    q, kn, vn = bf16(B, N, Hq, D), bf16(B, N, Hkv, D), bf16(B, N, Hkv, D)
+    n_past = torch.full((B,), P, dtype=torch.int32, device=dev)
+    o = torch.empty((B, N, Hq, D), device=dev)
+    kv = dflv.kv_layer(kq, vq, ks, vs)
+    descs = [dflv.attn_desc(B, N, Hq, Hkv, D, cap, 0, dflv.DFLV_KV_Q4_0, 1.0 / np.sqrt(D), f)
+             for f in (0, dflv.DFLV_FLAG_EARLY_PREFETCH)]
+    ms = timed(lambda r: dflv.check(dflv.dflv_tree_attn_verify(descs[r > 0], par_d, nn_d, n_past, q, kn, vn, kv, o,
+                                                             status)))
+    byt, flops = scale_bytes_attn(), scale_flops_attn()
+    tpk, tkind = bf16_peak()
+    tf = flops / (ms * 1e-3) / 1e12
+    out["attn_q4_131k_b8_n64"] = {"ms_per_launch": ms, "algorithmic_bytes_per_launch": byt,
+                                  "achieved": byt / (ms * 1e-3) / 1e9, "unit": "GB/s",
+                                  "algorithmic_flops_per_launch": flops, "tflops": tf,
+                                  "tensor_peak_tflops": tpk, "tensor_frac": tf / tpk,
+                                  "tensor_peak_source": tkind + " bf16_tflops"}
+    del kq, vq, ks, vs
+    # GDN: 27B shape, batch 8, 64-node trees
+    Hk, Hv, dk, dv = GDN["Hk"], GDN["Hv"], GDN["dk"], GDN["dv"]
+    st = torch.randn(B, Hv, dv, dk, generator=g, device=dev) * 0.02
+    gq, gk, gv = bf16(B, N, Hk, dk, unit=True), bf16(B, N, Hk, dk, unit=True), bf16(B, N, Hv, dv)
+    beta = torch.sigmoid(torch.randn(B, N, Hv, generator=g, device=dev))
+    la = -torch.nn.functional.softplus(torch.randn(B, N, Hv, generator=g, device=dev))
+    go = torch.empty(B, N, Hv, dv, device=dev)
+    fac = dflv.gdn_factors(torch.empty(B, N, Hv, dv, device=dev), torch.empty(B, N, Hv, device=dev),
+                           torch.empty(B, N, Hk, dk, dtype=torch.int16, device=dev))
+    gdescs = [dflv.gdn_desc(B, N, Hk, Hv, dk, dv, f) for f in (0, dflv.DFLV_FLAG_EARLY_PREFETCH)]
+    ms = timed(lambda r: dflv.check(dflv.dflv_tree_gdn_verify(gdescs[r > 0], par_d, nn_d, gq, gk, gv, beta, la, st,
+                                                            go, fac, status)))
+    byt = scale_bytes_gdn()
+    out["gdn_b8_n64"] = {"ms_per_launch": ms, "algorithmic_bytes_per_launch": byt,
+                         "achieved": byt / (ms * 1e-3) / 1e9, "unit": "GB/s"}
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    return out
+
+
 def run_gpu(args, rank, world):
     import torch
 
@@ -524,6 +646,7 @@ def run_gpu(args, rank, world):
     #      overlap), one CUDA graph per kind, timed with events on the
     #      launching stream; per launch = chain time / launches
     per = kernel_chain_ms(S, torch, stream, args.steps, args.warmup)
+    scale = scale_measure(torch, dflv) if not args.no_scale else {}
     # ---- end to end: pinned host inputs -> device, step, result -> host, every step
     S.reset()
     count[0] = 0
@@ -548,7 +671,7 @@ def run_gpu(args, rank, world):
     torch.cuda.synchronize()
     e2e_ms = reduce_max(world, e0.elapsed_time(e1))
     d2h = (BUDGET + 2) * 4
-    return dict(ms=ms_max, per=per, clocks=clk, L=L, e2e_ms=e2e_ms, h2d=S.in_bytes, d2h=d2h,
+    return dict(ms=ms_max, per=per, scale=scale, clocks=clk, L=L, e2e_ms=e2e_ms, h2d=S.in_bytes, d2h=d2h,
                 launches=S.launches_per_step, dev_name=torch.cuda.get_device_name(), host=host)
 
 
@@ -673,6 +796,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-scale", action="store_true", help="skip the at-scale kernel measurements")
     ap.add_argument("--kernel", choices=["gdn", "attn", "accept", "commit", "conv", "conv_commit", "ddtree"],
                     default=None,
                     help="profiling mode: launch one kernel of the step --launches times on its "
@@ -755,6 +879,10 @@ def main():
                                       "launching stream",
                      "traffic": profiled_traffic(dom)},
         "kernels_ms_per_launch": per,
+        "at_scale": {"what": "the stress shapes beside the step: 8 sequences with 64-node trees; attention over a "
+                             "131,072-token q4_0 cache, full attention; GDN of the 27B shape; 8 launches back to "
+                             "back per CUDA graph, CUDA events",
+                     **{k: dict(v, peak=peak, frac=v["achieved"] / peak) for k, v in r["scale"].items()}},
         "beside_the_step": {"what": "the short convolution in front of each GDN layer (48 tree-conv launches "
                                     "back to back, C=10240, K=4), the commit of its window (one launch, 48 "
                                     "layers) and the construction of the next draft tree from the draft's "
