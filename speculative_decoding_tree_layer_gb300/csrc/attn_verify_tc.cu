@@ -773,30 +773,47 @@ cudaError_t launch_tc(const AttnVerifyArgs& a, cudaStream_t stream) {
     const int rows = (a.Hq / a.Hkv) * a.N_max;
     const long range = (a.window > 0) ? (long)a.window - 1 : (long)a.cap;
     const long tiles = (range + kTK - 1) / kTK + 3;
-    const int sms = sm_count_cached();
-    // the largest cluster (<= 16, any size: the key tiles split by cost, so
-    // a size between powers of two still shortens the longest CTA) that
-    // still lets every cluster be resident at once and that the key range
-    // can feed
-    auto choose_cs = [&](int n_rt) {
+    // Cluster size and row tiles by a small cost model: a CTA costs its share
+    // of the key tiles plus a fixed prologue-and-merge overhead (in tile
+    // units), and the launch costs that times the number of waves of
+    // clusters the GPU can hold at once (the occupancy query).  Any size up
+    // to 16 is allowed (the key tiles split by cost, so sizes between powers
+    // of two also shorten the longest CTA).  Short key ranges end up with one
+    // wave of the largest resident clusters; long ranges with several waves
+    // of smaller ones, which keeps every SM busy.
+    constexpr double kOverheadTiles = 3.0;
+    auto est = [&](int n_rt, int cs) {
         const long clusters = (long)n_rt * a.Hkv * a.B;
-        for (int cs = 16; cs > 1; --cs)
-            if (clusters * cs <= sms && cs * 2 <= tiles && active_clusters<D, KT, VT>(cs) >= clusters)
-                return cs;
-        return 1;
+        const int act = active_clusters<D, KT, VT>(cs);
+        if (act <= 0) return 1e30;
+        const long waves = (clusters + act - 1) / act;
+        return (double)waves * ((double)tiles / cs + kOverheadTiles);
     };
-    // row tiles: as few as the 128-row MMA allows; when the key range is
-    // short (latency-bound: a few tiles per CTA) one more row tile is taken
-    // if it buys clearly more CTAs with every cluster still resident
+    auto choose_cs = [&](int n_rt, double& best) {
+        int bcs = 1;
+        best = est(n_rt, 1);
+        for (int cs = 2; cs <= 16 && cs * 2 <= tiles; ++cs) {
+            const double e = est(n_rt, cs);
+            if (e < best) {
+                best = e;
+                bcs = cs;
+            }
+        }
+        return bcs;
+    };
+    // row tiles: as few as the 128-row MMA allows, or one more (rows of at
+    // least 32 each) when that is cheaper by the same model
     int n_rt = (rows + kRows - 1) / kRows;
-    int cs = choose_cs(n_rt);
+    double e1, e2;
+    int cs = choose_cs(n_rt, e1);
     {
-        const int n2 = n_rt + 1, cs2 = choose_cs(n2);
-        const long ctas = (long)n_rt * a.Hkv * a.B * cs, ctas2 = (long)n2 * a.Hkv * a.B * cs2;
-        if ((rows + n2 - 1) / n2 >= 32 && tiles <= 16L * cs2 && ctas2 * 4 > ctas * 5 &&
-            active_clusters<D, KT, VT>(cs2) >= (long)n2 * a.Hkv * a.B) {
-            n_rt = n2;
-            cs = cs2;
+        const int n2 = n_rt + 1;
+        if ((rows + n2 - 1) / n2 >= 32) {
+            const int cs2 = choose_cs(n2, e2);
+            if (e2 < e1) {
+                n_rt = n2;
+                cs = cs2;
+            }
         }
     }
     const int RT = (rows + n_rt - 1) / n_rt;
