@@ -843,6 +843,7 @@ def main():
     ab = dict(gdn=gdn_bytes(L), attn=attn_bytes(), accept=accept_bytes(), commit=commit_bytes(L),
               conv=conv_bytes(), conv_commit=conv_commit_bytes(L), ddtree=ddtree_bytes())
     launches = dict(gdn=N_GDN, attn=N_ATTN, accept=1, commit=1)
+    step_mb = sum(ab[k] * launches[k] for k in launches) / 1e6
     # dominant kernel: the largest share of the step
     shares = {k: per[k] * launches[k] for k in per if k in launches} if per else {}
     beside = {}
@@ -866,7 +867,7 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16/f32 (q8_0 KV)", "data": "synthetic",
         "config": {"workload": WORKLOAD, "batch": 1, "budget": BUDGET, "ctx": CTX, "window": WINDOW,
                    "kv": "q8_0", "vocab": VOCAB, "accepted_len": L,
-                   "l2": "inputs larger than L2 (~630 MB touched per step); no flush",
+                   "l2": f"inputs larger than L2 (~{step_mb:.0f} MB touched per step); no flush",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "device": r["dev_name"]},
         "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
