@@ -4,6 +4,9 @@
  * computes, where each part comes from on the pages, its layouts and its
  * precision.  No blocking, fusion or reordering beyond the definitions.
  */
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 #include "oracle.h"
 
 #include <math.h>
@@ -135,22 +138,25 @@ int orc_tree_gdn_verify(int B, int N, int Hk, int Hv, int dk, int dv,
                         const float* beta, const float* log_alpha, const float* state,
                         float* out, double* node_states) {
     if (!gdn_dims_ok(B, N, Hk, Hv, dk, dv)) return ORC_ERR_ARG;
-    gdn_inputs in = {B, N, Hk, Hv, dk, dv, q, k, v, beta, log_alpha};
-    size_t SS = (size_t)dv * dk;
-    double* S0 = malloc(SS * sizeof(double));
-    double* states = malloc((size_t)N * SS * sizeof(double));
-    double *qd = malloc(dk * sizeof(double)), *kd = malloc(dk * sizeof(double));
-    double *vd = malloc(dv * sizeof(double)), *od = malloc(dv * sizeof(double));
-    int rc = ORC_OK;
-    for (int b = 0; b < B && rc == ORC_OK; ++b) {
-        int n = n_nodes[b];
+    for (int b = 0; b < B; ++b) {
         int32_t depth[64];
         uint64_t anc[64];
-        if (n > N || orc_tree_topology(n, parent + (size_t)b * N, depth, anc) != ORC_OK) {
-            rc = ORC_ERR_TOPOLOGY;
-            break;
-        }
-        for (int h = 0; h < Hv; ++h) {
+        if (n_nodes[b] > N || orc_tree_topology(n_nodes[b], parent + (size_t)b * N, depth, anc) != ORC_OK)
+            return ORC_ERR_TOPOLOGY;
+    }
+    gdn_inputs in = {B, N, Hk, Hv, dk, dv, q, k, v, beta, log_alpha};
+    const size_t SS = (size_t)dv * dk;
+    /* every (sequence, head) is independent: the same steps in the same
+     * order whichever thread takes it */
+#pragma omp parallel
+    {
+        double* S0 = malloc(SS * sizeof(double));
+        double* states = malloc((size_t)N * SS * sizeof(double));
+        double *qd = malloc(dk * sizeof(double)), *kd = malloc(dk * sizeof(double));
+        double *vd = malloc(dv * sizeof(double)), *od = malloc(dv * sizeof(double));
+#pragma omp for schedule(dynamic)
+        for (int bh = 0; bh < B * Hv; ++bh) {
+            const int b = bh / Hv, h = bh % Hv, n = n_nodes[b];
             const float* Sf = state + ((size_t)b * Hv + h) * SS;
             for (size_t e = 0; e < SS; ++e) S0[e] = (double)Sf[e];
             for (int i = 0; i < n; ++i) {
@@ -166,9 +172,9 @@ int orc_tree_gdn_verify(int B, int N, int Hk, int Hv, int dk, int dv,
                            states + (size_t)i * SS, SS * sizeof(double));
             }
         }
+        free(S0); free(states); free(qd); free(kd); free(vd); free(od);
     }
-    free(S0); free(states); free(qd); free(kd); free(vd); free(od);
-    return rc;
+    return ORC_OK;
 }
 
 int orc_tree_gdn_verify_bruteforce(int B, int N, int Hk, int Hv, int dk, int dv,
@@ -220,16 +226,18 @@ int orc_gdn_commit(int B, int N, int Hk, int Hv, int dk, int dv,
                    const int32_t* path, const int32_t* path_len, float* state) {
     if (!gdn_dims_ok(B, N, Hk, Hv, dk, dv)) return ORC_ERR_ARG;
     gdn_inputs in = {B, N, Hk, Hv, dk, dv, q, k, v, beta, log_alpha};
-    size_t SS = (size_t)dv * dk;
-    double* Sa = malloc(SS * sizeof(double));
-    double* Sb = malloc(SS * sizeof(double));
-    double *qd = malloc(dk * sizeof(double)), *kd = malloc(dk * sizeof(double));
-    double *vd = malloc(dv * sizeof(double)), *od = malloc(dv * sizeof(double));
-    int rc = ORC_OK;
-    for (int b = 0; b < B; ++b) {
-        int L = path_len[b];
-        if (L < 1 || L > N) { rc = ORC_ERR_ARG; break; }
-        for (int h = 0; h < Hv; ++h) {
+    const size_t SS = (size_t)dv * dk;
+    for (int b = 0; b < B; ++b)
+        if (path_len[b] < 1 || path_len[b] > N) return ORC_ERR_ARG;
+#pragma omp parallel
+    {
+        double* Sa = malloc(SS * sizeof(double));
+        double* Sb = malloc(SS * sizeof(double));
+        double *qd = malloc(dk * sizeof(double)), *kd = malloc(dk * sizeof(double));
+        double *vd = malloc(dv * sizeof(double)), *od = malloc(dv * sizeof(double));
+#pragma omp for schedule(dynamic)
+        for (int bh = 0; bh < B * Hv; ++bh) {
+            const int b = bh / Hv, h = bh % Hv, L = path_len[b];
             float* Sf = state + ((size_t)b * Hv + h) * SS;
             for (size_t e = 0; e < SS; ++e) Sa[e] = (double)Sf[e];
             /* decode exactly the accepted tokens, in path order */
@@ -241,9 +249,9 @@ int orc_gdn_commit(int B, int N, int Hk, int Hv, int dk, int dv,
             }
             for (size_t e = 0; e < SS; ++e) Sf[e] = (float)Sa[e];
         }
+        free(Sa); free(Sb); free(qd); free(kd); free(vd); free(od);
     }
-    free(Sa); free(Sb); free(qd); free(kd); free(vd); free(od);
-    return rc;
+    return ORC_OK;
 }
 
 /* ------------------------------------------------------------------------ */
@@ -448,10 +456,6 @@ int orc_tree_attn_verify(int B, int N, int Hq, int Hkv, int D, int cap, int wind
     kv_cache c = {B, Hkv, D, cap, kv_type, kq, vq, ks, vs};
     int32_t* depth = malloc((size_t)B * 64 * sizeof(int32_t));
     uint64_t* anc = malloc((size_t)B * 64 * sizeof(uint64_t));
-    double* qd = malloc(D * sizeof(double));
-    double* key = malloc(D * sizeof(double));
-    double* val = malloc(D * sizeof(double));
-    double* acc = malloc(D * sizeof(double));
     int rc = ORC_OK;
     for (int b = 0; b < B && rc == ORC_OK; ++b) {
         int n = n_nodes[b], P = n_past[b];
@@ -469,24 +473,48 @@ int orc_tree_attn_verify(int B, int N, int Hq, int Hkv, int D, int cap, int wind
                 kv_write_row(&c, 0, b, h, n_past[b] + i, k_new + off);
                 kv_write_row(&c, 1, b, h, n_past[b] + i, v_new + off);
             }
-    /* (ii) every requested (sequence, node, query head) output */
+    /* (ii) every requested (sequence, node, query head) output; the rows
+     * are independent, whichever thread computes them */
     if (rc == ORC_OK) {
+        long n_out = 0;
         if (rows == NULL) {
-            for (int b = 0; b < B; ++b)
-                for (int i = 0; i < n_nodes[b]; ++i)
-                    for (int h = 0; h < Hq; ++h)
-                        attn_one(&c, N, Hq, window, scale, b, i, h, n_past[b], n_nodes[b],
-                                 depth + 64 * b, anc + 64 * b, q, qd, key, val, acc, out);
+            for (int b = 0; b < B; ++b) n_out += (long)n_nodes[b] * Hq;
         } else {
             for (int r = 0; r < n_rows; ++r) {
-                int h = rows[r] % Hq, i = (rows[r] / Hq) % N, b = rows[r] / Hq / N;
-                if (b < 0 || b >= B || i >= n_nodes[b]) { rc = ORC_ERR_ARG; break; }
-                attn_one(&c, N, Hq, window, scale, b, i, h, n_past[b], n_nodes[b],
-                         depth + 64 * b, anc + 64 * b, q, qd, key, val, acc, out);
+                int i = (rows[r] / Hq) % N, b = rows[r] / Hq / N;
+                if (b < 0 || b >= B || i >= n_nodes[b]) rc = ORC_ERR_ARG;
+            }
+            n_out = n_rows;
+        }
+        if (rc == ORC_OK) {
+#pragma omp parallel
+            {
+                double* qd = malloc(D * sizeof(double));
+                double* key = malloc(D * sizeof(double));
+                double* val = malloc(D * sizeof(double));
+                double* acc = malloc(D * sizeof(double));
+#pragma omp for schedule(dynamic)
+                for (long r = 0; r < n_out; ++r) {
+                    int b, i, h;
+                    if (rows == NULL) {
+                        long t = r;
+                        b = 0;
+                        while (t >= (long)n_nodes[b] * Hq) t -= (long)n_nodes[b++] * Hq;
+                        i = (int)(t / Hq);
+                        h = (int)(t % Hq);
+                    } else {
+                        h = rows[r] % Hq;
+                        i = (rows[r] / Hq) % N;
+                        b = rows[r] / Hq / N;
+                    }
+                    attn_one(&c, N, Hq, window, scale, b, i, h, n_past[b], n_nodes[b],
+                             depth + 64 * b, anc + 64 * b, q, qd, key, val, acc, out);
+                }
+                free(qd); free(key); free(val); free(acc);
             }
         }
     }
-    free(depth); free(anc); free(qd); free(key); free(val); free(acc);
+    free(depth); free(anc);
     return rc;
 }
 
@@ -634,4 +662,18 @@ int orc_conv_commit(int B, int N, int C, int K, const uint16_t* x, const int32_t
     }
     free(seq);
     return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* threads                                                                   */
+/* ------------------------------------------------------------------------ */
+
+int orc_set_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+    return omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
 }

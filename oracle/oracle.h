@@ -155,6 +155,11 @@ int orc_tree_conv_verify(int B, int N, int C, int K, const int32_t* parent, cons
 int orc_conv_commit(int B, int N, int C, int K, const uint16_t* x, const int32_t* path,
                     const int32_t* path_len, uint16_t* state);
 
+/* Threads used by the functions that loop over independent (sequence, head)
+ * or output rows (OpenMP when compiled with it): sets n (> 0) and returns
+ * the count in force.  Results do not depend on it. */
+int orc_set_threads(int n);
+
 /* ---- KV commit: move slot P+path[m] to P+m for m < L (all reads first) ---- */
 int orc_kv_commit(int B, int N, int Hkv, int D, int cap, int kv_type,
                   const int32_t* path, const int32_t* path_len, const int32_t* n_past,
