@@ -22,6 +22,7 @@ path has no exchange step); rank 0 prints one JSON line.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -43,6 +44,7 @@ UNIT = "nodes/s/layer"
 N_LAYERS, N_GDN, N_ATTN = 64, 48, 16
 BUDGET, VOCAB, CTX, WINDOW, PLANT = 22, 151936, 32768, 2048, 8
 DRAFT_BLOCK, TOPK, TAU = 16, 4, 6.0   # draft positions per tree, expansion width, pruning margin
+CLOCK_LOAD_S = 0.5                     # untimed replays of the step on each side of the timed steps, for the clock samples
 GDN = synth.GDN_27B
 ATT = synth.ATTN_27B
 CONV = synth.CONV_27B
@@ -148,16 +150,22 @@ def commit_bytes(L):
 
 # ---------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi samples during the timed region (200 ms period)."""
+    """nvidia-smi samples (200 ms period); only those stamped between
+    mark() and stop() count, i.e. the samples taken while the GPU ran the
+    timed steps and the same steps around them."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,timestamp")
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
+        self.t_mark = None
+
+    def mark(self):
+        self.t_mark = time.time()
 
     def start(self):
         try:
@@ -174,6 +182,7 @@ class ClockSampler:
             self.lines.append(line.strip())
 
     def stop(self):
+        t_stop = time.time()
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -186,7 +195,13 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(f[9], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                ts = None
+            if ts is not None and self.t_mark is not None and not (self.t_mark <= ts <= t_stop):
                 continue
             try:
                 sm.append(float(f[1]))
@@ -627,6 +642,18 @@ def run_gpu(args, rank, world):
     clocks = ClockSampler(int(ids[local]) if local < len(ids) else local)
     clocks.start()
     time.sleep(0.3)
+
+    def load_for(seconds):
+        # the same step, replayed untimed, so that the clock samples around
+        # the short timed region are taken under its load
+        t = time.perf_counter()
+        while time.perf_counter() - t < seconds:
+            for _ in range(32):
+                replay()
+            torch.cuda.synchronize()
+
+    clocks.mark()
+    load_for(CLOCK_LOAD_S)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record()
     for _ in range(args.steps):
@@ -634,6 +661,7 @@ def run_gpu(args, rank, world):
     t1.record()
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
+    load_for(CLOCK_LOAD_S)
     clk = clocks.stop()
     barrier(world)
     status = int(S.status.item())
