@@ -409,8 +409,48 @@ class GpuStep:
                                           [c["x"] for c in self.conv], self.path, self.path_len, self.status)
 
 
-def kernel_chain_ms(S, torch, stream, steps, warmup):
-    """Average launch duration of each kernel kind inside its own chain."""
+L2_FLUSH_BYTES = 2 * 129 * 2**20   # twice the L2
+
+
+class L2Flush:
+    """Writes a buffer twice the size of the L2 on the current stream, so
+    that the next replay starts with none of its inputs cached."""
+
+    def __init__(self, torch):
+        self.buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
+        self.i = 0
+
+    def __call__(self):
+        self.i += 1
+        self.buf.fill_(self.i)
+
+
+def cold_replays(torch, graph, count, flush, stream):
+    """Replays `graph` `count` times on `stream`, each after an L2 flush and
+    between its own pair of CUDA events; returns the replay times in ms.
+    The flush is still running when the events and the replay are submitted,
+    so the host's submission stays off the measured interval."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(count)]
+    with torch.cuda.stream(stream):
+        for a, b in evs:
+            flush()
+            a.record()
+            graph.replay()
+            b.record()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def pct(xs):
+    """p10 / p50 / p90 of a list of times."""
+    return [float(np.percentile(xs, q)) for q in (10, 50, 90)]
+
+
+def kernel_chain_ms(S, torch, stream, steps, warmup, flush):
+    """Launch duration of each kernel kind inside its own chain, from cold
+    L2: every replay follows an L2 flush.  A kind with one launch per step is
+    replayed as a graph of that one launch.  Returns (mean per launch,
+    p10/p50/p90 per launch over the replays)."""
     dflv, chk = S.dflv, S.dflv.check
 
     def gdn_chain():
@@ -442,36 +482,27 @@ def kernel_chain_ms(S, torch, stream, steps, warmup):
     def ddtree():
         chk(S.ddtree_build(), "ddtree build")
 
-    # A kind with a single launch per step is captured REPS times per graph,
-    # so that the host's graph submission stays off the measured interval.
-    REPS = 16
-    out = {}
-    for name, fn, n, reps in (("gdn", gdn_chain, N_GDN, 1), ("attn", attn_chain, N_ATTN, 1),
-                              ("accept", accept, 1, REPS), ("commit", commit, 1, REPS),
-                              ("conv", conv_chain, N_GDN, 1), ("conv_commit", conv_commit, 1, REPS),
-                              ("ddtree", ddtree, 1, REPS)):
+    out, dist = {}, {}
+    for name, fn, n in (("gdn", gdn_chain, N_GDN), ("attn", attn_chain, N_ATTN), ("accept", accept, 1),
+                        ("commit", commit, 1), ("conv", conv_chain, N_GDN), ("conv_commit", conv_commit, 1),
+                        ("ddtree", ddtree, 1)):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            for _ in range(reps):
-                fn()
+            fn()
         S.reset()
         with torch.cuda.stream(stream):
             accept()  # an accepted path: the GDN verifies apply it as their pending commit
         torch.cuda.synchronize()
-        for _ in range(warmup):
-            g.replay()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
-            e0.record()
-            for _ in range(steps):
+            for _ in range(warmup):
                 g.replay()
-            e1.record()
         torch.cuda.synchronize()
-        out[name] = e0.elapsed_time(e1) / (steps * n * reps)
+        ts = cold_replays(torch, g, steps, flush, stream)
+        out[name] = float(np.sum(ts)) / (steps * n)
+        dist[name] = [x / n for x in pct(ts)]
         S.reset()
         torch.cuda.synchronize()
-    return out
+    return out, dist
 
 
 # ---------------------------------------------------------------------------- at scale
@@ -510,10 +541,13 @@ def scale_bytes_gdn():
                 N * Hv * 4 + N * Hk * dk * 2)
 
 
-def scale_measure(torch, dflv, reps=8, rounds=10):
+def scale_measure(torch, dflv, flush, reps=8, rounds=10):
     """Per-launch time of the attention and GDN verify at the stress shapes,
-    launched back to back (same buffers, early prefetch after the first);
-    inputs drawn on the device from a seeded generator."""
+    `reps` launches back to back per graph (early prefetch after the first),
+    each replay after an L2 flush.  Attention reads 1.2 GB per launch, so its
+    launches share one set of buffers; the GDN launches rotate over `reps`
+    input sets so that none reads what the one before left in the L2.  Inputs
+    are drawn on the device from a seeded generator."""
     dev = "cuda"
     g = torch.Generator(device=dev)
     g.manual_seed(SEED + 31)
@@ -542,17 +576,11 @@ def scale_measure(torch, dflv, reps=8, rounds=10):
         with torch.cuda.graph(graph, stream=stream):
             for r in range(reps):
                 fn(r)
-        for _ in range(3):
-            graph.replay()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
-            e0.record()
-            for _ in range(rounds):
+            for _ in range(3):
                 graph.replay()
-            e1.record()
         torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / (rounds * reps)
+        return float(np.sum(cold_replays(torch, graph, rounds, flush, stream))) / (rounds * reps)
 
     # attention: q4_0 cache, full attention
     kq = torch.randint(0, 256, (B, Hkv, cap, D // 2), generator=g, device=dev, dtype=torch.uint8)
@@ -578,16 +606,24 @@ def scale_measure(torch, dflv, reps=8, rounds=10):
     del kq, vq, ks, vs
     # GDN: 27B shape, batch 8, 64-node trees
     Hk, Hv, dk, dv = GDN["Hk"], GDN["Hv"], GDN["dk"], GDN["dv"]
-    st = torch.randn(B, Hv, dv, dk, generator=g, device=dev) * 0.02
-    gq, gk, gv = bf16(B, N, Hk, dk, unit=True), bf16(B, N, Hk, dk, unit=True), bf16(B, N, Hv, dv)
-    beta = torch.sigmoid(torch.randn(B, N, Hv, generator=g, device=dev))
-    la = -torch.nn.functional.softplus(torch.randn(B, N, Hv, generator=g, device=dev))
-    go = torch.empty(B, N, Hv, dv, device=dev)
-    fac = dflv.gdn_factors(torch.empty(B, N, Hv, dv, device=dev), torch.empty(B, N, Hv, device=dev),
-                           torch.empty(B, N, Hk, dk, dtype=torch.int16, device=dev))
+    sets = []
+    for _ in range(reps):
+        sets.append(dict(
+            st=torch.randn(B, Hv, dv, dk, generator=g, device=dev) * 0.02,
+            q=bf16(B, N, Hk, dk, unit=True), k=bf16(B, N, Hk, dk, unit=True), v=bf16(B, N, Hv, dv),
+            beta=torch.sigmoid(torch.randn(B, N, Hv, generator=g, device=dev)),
+            la=-torch.nn.functional.softplus(torch.randn(B, N, Hv, generator=g, device=dev)),
+            o=torch.empty(B, N, Hv, dv, device=dev),
+            fac=dflv.gdn_factors(torch.empty(B, N, Hv, dv, device=dev), torch.empty(B, N, Hv, device=dev),
+                                 torch.empty(B, N, Hk, dk, dtype=torch.int16, device=dev))))
     gdescs = [dflv.gdn_desc(B, N, Hk, Hv, dk, dv, f) for f in (0, dflv.DFLV_FLAG_EARLY_PREFETCH)]
-    ms = timed(lambda r: dflv.check(dflv.dflv_tree_gdn_verify(gdescs[r > 0], par_d, nn_d, gq, gk, gv, beta, la, st,
-                                                            go, fac, status)))
+
+    def gdn(r):
+        d = sets[r]
+        dflv.check(dflv.dflv_tree_gdn_verify(gdescs[r > 0], par_d, nn_d, d["q"], d["k"], d["v"], d["beta"], d["la"],
+                                             d["st"], d["o"], d["fac"], status))
+
+    ms = timed(gdn)
     byt = scale_bytes_gdn()
     out["gdn_b8_n64"] = {"ms_per_launch": ms, "algorithmic_bytes_per_launch": byt,
                          "achieved": byt / (ms * 1e-3) / 1e9, "unit": "GB/s"}
@@ -669,12 +705,24 @@ def run_gpu(args, rank, world):
     assert status == 0, f"device status {status}"
     ms_max = reduce_max(world, ms)
 
+    # ---- the spread over steps: the same replays, each between its own events
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in evs:
+        a.record()
+        replay()
+        b.record()
+    torch.cuda.synchronize()
+    step_pct = pct([a.elapsed_time(b) for a, b in evs])
+
     # ---- per-kernel durations: every kernel kind of the step launched back
     #      to back as in the step (all its layers, same buffers, same launch
-    #      overlap), one CUDA graph per kind, timed with events on the
-    #      launching stream; per launch = chain time / launches
-    per = kernel_chain_ms(S, torch, stream, args.steps, args.warmup)
-    scale = scale_measure(torch, dflv) if not args.no_scale else {}
+    #      overlap), one CUDA graph per kind, each replay after an L2 flush and
+    #      between its own events on the launching stream; per launch =
+    #      chain time / launches
+    flush = L2Flush(torch)
+    per, dist = kernel_chain_ms(S, torch, stream, args.steps, args.warmup, flush)
+    scale = scale_measure(torch, dflv, flush) if not args.no_scale else {}
+    del flush
     # ---- end to end: pinned host inputs -> device, step, result -> host, every step
     S.reset()
     count[0] = 0
@@ -699,7 +747,7 @@ def run_gpu(args, rank, world):
     torch.cuda.synchronize()
     e2e_ms = reduce_max(world, e0.elapsed_time(e1))
     d2h = (BUDGET + 2) * 4
-    return dict(ms=ms_max, per=per, scale=scale, clocks=clk, L=L, e2e_ms=e2e_ms, h2d=S.in_bytes, d2h=d2h,
+    return dict(ms=ms_max, per=per, dist=dist, step_pct=step_pct, scale=scale, clocks=clk, L=L, e2e_ms=e2e_ms, h2d=S.in_bytes, d2h=d2h,
                 launches=S.launches_per_step, dev_name=torch.cuda.get_device_name(), host=host)
 
 
@@ -914,14 +962,20 @@ def main():
                      "peak_source": f"{peak_kind} hbm_gbs",
                      "algorithmic_bytes_per_launch": ab[dom],
                      "avg_launch_ms": dur_ms,
-                     "launch_timing": "chain of all launches of this kernel in the step, back to back (a kernel "
-                                      "launched once per step: 16 launches per graph), CUDA events on the "
-                                      "launching stream",
+                     "launch_timing": "one replay = the chain of all launches of this kernel in the step, "
+                                      "back to back (one launch for a kernel launched once per step); each "
+                                      "replay after an L2 flush (a buffer twice the L2 written) and between "
+                                      "its own CUDA events on the launching stream; mean over the replays",
                      "traffic": profiled_traffic(dom)},
         "kernels_ms_per_launch": per,
+        "kernels_ms_per_launch_p10_p50_p90": r["dist"],
+        "step_ms_p10_p50_p90": r["step_pct"],
+        "nodes_per_s_per_layer": {"step": value / world,
+                                  **{k: BUDGET / (per[k] * 1e-3) for k in ("gdn", "attn") if per.get(k)}},
         "at_scale": {"what": "the stress shapes beside the step: 8 sequences with 64-node trees; attention over a "
                              "131,072-token q4_0 cache, full attention; GDN of the 27B shape; 8 launches back to "
-                             "back per CUDA graph, CUDA events",
+                             "back per CUDA graph (the GDN launches on 8 distinct input sets), an L2 flush before "
+                             "each replay, CUDA events",
                      **{k: dict(v, peak=peak, frac=v["achieved"] / peak) for k, v in r["scale"].items()}},
         "beside_the_step": {"what": "the short convolution in front of each GDN layer (48 tree-conv launches "
                                     "back to back, C=10240, K=4), the commit of its window (one launch, 48 "
