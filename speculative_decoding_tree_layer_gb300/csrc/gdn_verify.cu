@@ -518,11 +518,14 @@ cudaError_t launch_dk_rb(const GdnVerifyArgs& a, cudaStream_t stream) {
 template <int DK>
 cudaError_t launch_dk(const GdnVerifyArgs& a, cudaStream_t stream) {
     const bool small = a.N_max <= 32;
-    // Trees of up to 32 nodes: 64 state rows per CTA when dv allows it, so
-    // that a head takes dv/64 CTAs and the launch stays within one CTA per SM
-    // at the common shapes (its slowest CTAs then share no SM with another
-    // CTA of the same launch); larger trees keep 32 rows (registers).
-    if (small && a.dv % 64 == 0) return launch_dk_rb<DK, 64, 32>(a, stream);
+    // 64 state rows per CTA when dv allows it, so that a head takes dv/64
+    // CTAs.  Trees of up to 32 nodes: the launch then stays within one CTA
+    // per SM at the common shapes (its slowest CTAs share no SM with another
+    // CTA of the same launch).  Larger trees: the CTA's shared memory admits
+    // one CTA per SM at 32 rows already, so 64 rows halve the waves and the
+    // Gram tiles each CTA repeats for its head.
+    if (a.dv % 64 == 0)
+        return small ? launch_dk_rb<DK, 64, 32>(a, stream) : launch_dk_rb<DK, 64, 64>(a, stream);
     if (a.dv % 32 == 0)
         return small ? launch_dk_rb<DK, 32, 32>(a, stream) : launch_dk_rb<DK, 32, 64>(a, stream);
     return small ? launch_dk_rb<DK, 16, 32>(a, stream) : launch_dk_rb<DK, 16, 64>(a, stream);
@@ -532,7 +535,7 @@ cudaError_t launch_dk(const GdnVerifyArgs& a, cudaStream_t stream) {
 
 size_t gdn_verify_smem_bytes(int N_max, int dk, int dv) {
     const bool small = N_max <= 32;
-    return GdnSmemLayout(small ? 32 : 64, dk, (small && dv % 64 == 0) ? 64 : dv % 32 == 0 ? 32 : 16).total;
+    return GdnSmemLayout(small ? 32 : 64, dk, dv % 64 == 0 ? 64 : dv % 32 == 0 ? 32 : 16).total;
 }
 
 cudaError_t launch_gdn_tree_verify(const GdnVerifyArgs& a, cudaStream_t stream) {

@@ -259,13 +259,15 @@ def test_tiny_case_full_step_twice(dflv, orc):
         assert np.array_equal(hc[:, :, :ref_P], ref_cache["kq"][:, :, :ref_P])
 
 
-def test_deferred_commit_matches_eager(dflv, orc):
+@pytest.mark.parametrize("N", [22, 48])
+def test_deferred_commit_matches_eager(dflv, orc, N):
     """Deferred commit: each verify applies the previous step's accepted path
     to the state it streams (and writes it back), so a step commits only the
     KV caches.  Three steps on two sequences (one with an empty pending
-    path), outputs and states against the oracle's eager commit."""
-    rng = np.random.default_rng(77)
-    Hk, Hv, dk, dv, B, N = 2, 6, 128, 64, 2, 22
+    path), outputs and states against the oracle's eager commit; trees of up
+    to 32 nodes and over 32 take different launch forms."""
+    rng = np.random.default_rng(77 + N)
+    Hk, Hv, dk, dv, B = 2, 6, 128, 64, 2
     state0 = (rng.standard_normal((B, Hv, dv, dk)) * 0.3).astype(np.float32)
     state = dev(state0)
     ref_state = state0.copy()

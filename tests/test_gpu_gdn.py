@@ -64,6 +64,8 @@ CASES = [
     (3, [13, 64, 40], 2, 4, 128, 128, "uniform"),
     (2, [22, 31], 2, 4, 128, 128, "ddtree"),    # up to 32 nodes: 64-row blocks
     (1, [32], 1, 2, 64, 64, "chain"),           # one 64-row block per head
+    (2, [40, 33], 2, 4, 64, 96, "uniform"),     # over 32 nodes, dv 96: 32-row blocks
+    (1, [48], 1, 2, 32, 48, "ddtree"),          # over 32 nodes, dv 48: 16-row blocks
 ]
 
 
