@@ -541,6 +541,40 @@ def scale_bytes_gdn():
                 N * Hv * 4 + N * Hk * dk * 2)
 
 
+def scale_trees(torch):
+    """The stress shapes' trees: SCALE_B DDTree-shaped trees of SCALE_N nodes."""
+    rng = np.random.default_rng(SEED + 37)
+    pars = [synth.ddtree(rng, SCALE_N, VOCAB)[0] for _ in range(SCALE_B)]
+    parent, n_nodes = synth.batch_trees(pars, SCALE_N)
+    return torch.from_numpy(parent).to("cuda"), torch.from_numpy(n_nodes).to("cuda")
+
+
+def dev_bf16(torch, g, *shape, unit=False):
+    """N(0, 1) bf16 bits on the device (L2-normalised over the last axis if
+    `unit`, as q and k of a GDN layer are)."""
+    x = torch.randn(*shape, generator=g, device="cuda")
+    if unit:
+        x = x / x.norm(dim=-1, keepdim=True)
+    return x.to(torch.bfloat16).view(torch.int16)
+
+
+def scale_gdn_set(torch, dflv, g):
+    """One GDN layer's inputs, state and outputs at the stress shape."""
+    B, N, dev = SCALE_B, SCALE_N, "cuda"
+    Hk, Hv, dk, dv = GDN["Hk"], GDN["Hv"], GDN["dk"], GDN["dv"]
+    u, gg = torch.empty(B, N, Hv, dv, device=dev), torch.empty(B, N, Hv, device=dev)
+    kc = torch.empty(B, N, Hk, dk, dtype=torch.int16, device=dev)
+    return dict(
+        u=u, g=gg, kc=kc,
+        st=torch.randn(B, Hv, dv, dk, generator=g, device=dev) * 0.02,
+        q=dev_bf16(torch, g, B, N, Hk, dk, unit=True), k=dev_bf16(torch, g, B, N, Hk, dk, unit=True),
+        v=dev_bf16(torch, g, B, N, Hv, dv),
+        beta=torch.sigmoid(torch.randn(B, N, Hv, generator=g, device=dev)),
+        la=-torch.nn.functional.softplus(torch.randn(B, N, Hv, generator=g, device=dev)),
+        o=torch.empty(B, N, Hv, dv, device=dev),
+        fac=dflv.gdn_factors(u, gg, kc))
+
+
 def scale_measure(torch, dflv, flush, reps=8, rounds=10):
     """Per-launch time of the attention and GDN verify at the stress shapes,
     `reps` launches back to back per graph (early prefetch after the first),
@@ -555,18 +589,12 @@ def scale_measure(torch, dflv, flush, reps=8, rounds=10):
     Hq, Hkv, D = ATT["Hq"], ATT["Hkv"], ATT["D"]
     cap = P + N
     out = {}
-    rng = np.random.default_rng(SEED + 37)
-    pars = [synth.ddtree(rng, N, VOCAB)[0] for _ in range(B)]
-    parent, n_nodes = synth.batch_trees(pars, N)
-    par_d, nn_d = torch.from_numpy(parent).to(dev), torch.from_numpy(n_nodes).to(dev)
+    par_d, nn_d = scale_trees(torch)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream()
 
     def bf16(*shape, unit=False):
-        x = torch.randn(*shape, generator=g, device=dev)
-        if unit:  # q and k of a GDN layer are L2-normalised per head
-            x = x / x.norm(dim=-1, keepdim=True)
-        return x.to(torch.bfloat16).view(torch.int16)
+        return dev_bf16(torch, g, *shape, unit=unit)
 
     def timed(fn):
         graph = torch.cuda.CUDAGraph()
@@ -606,16 +634,7 @@ def scale_measure(torch, dflv, flush, reps=8, rounds=10):
     del kq, vq, ks, vs
     # GDN: 27B shape, batch 8, 64-node trees
     Hk, Hv, dk, dv = GDN["Hk"], GDN["Hv"], GDN["dk"], GDN["dv"]
-    sets = []
-    for _ in range(reps):
-        sets.append(dict(
-            st=torch.randn(B, Hv, dv, dk, generator=g, device=dev) * 0.02,
-            q=bf16(B, N, Hk, dk, unit=True), k=bf16(B, N, Hk, dk, unit=True), v=bf16(B, N, Hv, dv),
-            beta=torch.sigmoid(torch.randn(B, N, Hv, generator=g, device=dev)),
-            la=-torch.nn.functional.softplus(torch.randn(B, N, Hv, generator=g, device=dev)),
-            o=torch.empty(B, N, Hv, dv, device=dev),
-            fac=dflv.gdn_factors(torch.empty(B, N, Hv, dv, device=dev), torch.empty(B, N, Hv, device=dev),
-                                 torch.empty(B, N, Hk, dk, dtype=torch.int16, device=dev))))
+    sets = [scale_gdn_set(torch, dflv, g) for _ in range(reps)]
     gdescs = [dflv.gdn_desc(B, N, Hk, Hv, dk, dv, f) for f in (0, dflv.DFLV_FLAG_EARLY_PREFETCH)]
 
     def gdn(r):
@@ -841,6 +860,20 @@ def profile_one(kind, launches):
 
     dflv.load()
     torch.cuda.set_device(0)
+    if kind == "gdn_scale":
+        # the GDN verify at the stress shape (8 sequences, 64-node trees)
+        g = torch.Generator(device="cuda")
+        g.manual_seed(SEED + 31)
+        par_d, nn_d = scale_trees(torch)
+        d = scale_gdn_set(torch, dflv, g)
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        desc = dflv.gdn_desc(SCALE_B, SCALE_N, GDN["Hk"], GDN["Hv"], GDN["dk"], GDN["dv"])
+        for _ in range(launches):
+            dflv.check(dflv.dflv_tree_gdn_verify(desc, par_d, nn_d, d["q"], d["k"], d["v"], d["beta"], d["la"],
+                                                 d["st"], d["o"], d["fac"], status))
+        torch.cuda.synchronize()
+        print(json.dumps({"kernel": kind, "launches": launches, "status": int(status.item())}))
+        return
     rng = np.random.default_rng(SEED)
     host = make_host_inputs(rng, n_layers=4)
     S = GpuStep(host, torch, dflv)
@@ -882,7 +915,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-scale", action="store_true", help="skip the at-scale kernel measurements")
-    ap.add_argument("--kernel", choices=["gdn", "attn", "accept", "commit", "conv", "conv_commit", "ddtree"],
+    ap.add_argument("--kernel", choices=["gdn", "attn", "accept", "commit", "conv", "conv_commit", "ddtree",
+                                         "gdn_scale"],
                     default=None,
                     help="profiling mode: launch one kernel of the step --launches times on its "
                          "single-layer workload and exit (for ncu captures)")

@@ -143,7 +143,12 @@ def gdn_desc(B, N_max, Hk, Hv, dk, dv, flags=0):
 
 
 def gdn_factors(u, g, kcopy):
-    return dflv_gdn_factors(_ptr(u), _ptr(g), _ptr(kcopy))
+    """The factor buffers' pointers.  The struct holds references to the
+    tensors it was made from, so that buffers passed as temporaries stay
+    allocated for as long as the struct is in use."""
+    f = dflv_gdn_factors(_ptr(u), _ptr(g), _ptr(kcopy))
+    f._tensors = (u, g, kcopy)
+    return f
 
 
 def attn_desc(B, N_max, Hq, Hkv, D, cap, window, kv_type, scale, flags=0):
@@ -151,7 +156,11 @@ def attn_desc(B, N_max, Hq, Hkv, D, cap, window, kv_type, scale, flags=0):
 
 
 def kv_layer(kq, vq, ks=None, vs=None):
-    return dflv_kv_layer(_ptr(kq), _ptr(vq), _ptr(ks), _ptr(vs))
+    """One layer's cache planes; holds references to the tensors, as
+    gdn_factors does."""
+    c = dflv_kv_layer(_ptr(kq), _ptr(vq), _ptr(ks), _ptr(vs))
+    c._tensors = (kq, vq, ks, vs)
+    return c
 
 
 # ---------------------------------------------------------------- the C ABI

@@ -142,3 +142,30 @@ def test_ddtree_host_validation(lib):
     assert call(ok, draft_logits=None) == dflv.DFLV_ERR_INVALID_ARG
     assert call(ok, draft_logits=24) == dflv.DFLV_ERR_INVALID_ARG                        # misaligned
     assert call(ok, parent=18) == dflv.DFLV_ERR_INVALID_ARG
+
+
+def test_structs_keep_the_tensors_they_point_to():
+    # A factor or cache struct made from temporaries must keep them alive:
+    # the library stores only their addresses, and a freed tensor's memory
+    # would be handed to the next allocation while kernels still write it.
+    import gc
+    import weakref
+
+    import torch
+
+    u = torch.empty(8)
+    ref = weakref.ref(u)
+    f = dflv.gdn_factors(u, torch.empty(4), torch.empty(4, dtype=torch.int16))
+    addr = u.data_ptr()
+    del u
+    gc.collect()
+    assert ref() is not None and f.u == addr
+    kq = torch.empty(16, dtype=torch.uint8)
+    kref = weakref.ref(kq)
+    c = dflv.kv_layer(kq, torch.empty(16, dtype=torch.uint8))
+    del kq
+    gc.collect()
+    assert kref() is not None and c.kq == kref().data_ptr()
+    del f, c
+    gc.collect()
+    assert ref() is None and kref() is None
