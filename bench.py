@@ -792,9 +792,10 @@ def oracle_block_sample(host):
     return time.perf_counter() - t
 
 
-def cpu_baseline(host, reps=1):
+def cpu_baseline(host, min_seconds=3.0, min_reps=3):
     """The oracle on all host cores (its loops over independent (sequence,
-    head) and output rows run in parallel), and on one thread."""
+    head) and output rows run in parallel), and on one thread: samples
+    repeated for at least `min_seconds` and `min_reps`, median reported."""
     import oracle
 
     oracle.build()
@@ -802,15 +803,19 @@ def cpu_baseline(host, reps=1):
     res = {}
     for threads in (cores, 1):
         used = oracle.set_threads(threads)
-        ts = [oracle_block_sample(host) for _ in range(reps)]
-        res[threads] = (used, float(np.median(ts)))
-    used, t = res[cores]
+        ts, t0 = [], time.perf_counter()
+        while len(ts) < min_reps or time.perf_counter() - t0 < min_seconds:
+            ts.append(oracle_block_sample(host))
+        res[threads] = (used, float(np.median(ts)), len(ts))
+    oracle.set_threads(cores)
+    used, t, n = res[cores]
     return {"value": BUDGET * 4 / t, "unit": UNIT, "cores": used, "kind": "oracle",
-            "sample": "one [GDN, GDN, GDN, attention] block of the step (4 of 64 layers) + accept over the "
-                      "full vocab + commit of that block; C oracle, fp64, parallel over (sequence, head) and "
-                      "output rows",
-            "seconds_per_sample": t,
-            "single_thread": {"value": BUDGET * 4 / res[1][1], "cores": 1, "seconds_per_sample": res[1][1]}}
+            "sample": f"one [GDN, GDN, GDN, attention] block of the step (4 of 64 layers) + accept over the "
+                      f"full vocab + commit of that block; C oracle, fp64, parallel over (sequence, head) and "
+                      f"output rows; median of {n} samples",
+            "seconds_per_sample": t, "samples": n,
+            "single_thread": {"value": BUDGET * 4 / res[1][1], "cores": 1, "seconds_per_sample": res[1][1],
+                              "samples": res[1][2]}}
 
 
 # ---------------------------------------------------------------------------- distributed plumbing
