@@ -626,7 +626,8 @@ def scale_measure(torch, dflv, flush, reps=8, rounds=10):
     byt, flops = scale_bytes_attn(), scale_flops_attn()
     tpk, tkind = bf16_peak()
     tf = flops / (ms * 1e-3) / 1e12
-    out["attn_q4_131k_b8_n64"] = {"ms_per_launch": ms, "algorithmic_bytes_per_launch": byt,
+    out["attn_q4_131k_b8_n64"] = {"ms_per_launch": ms, "nodes_per_s_per_layer": B * N / (ms * 1e-3),
+                                  "algorithmic_bytes_per_launch": byt,
                                   "achieved": byt / (ms * 1e-3) / 1e9, "unit": "GB/s",
                                   "algorithmic_flops_per_launch": flops, "tflops": tf,
                                   "tensor_peak_tflops": tpk, "tensor_frac": tf / tpk,
@@ -644,7 +645,8 @@ def scale_measure(torch, dflv, flush, reps=8, rounds=10):
 
     ms = timed(gdn)
     byt = scale_bytes_gdn()
-    out["gdn_b8_n64"] = {"ms_per_launch": ms, "algorithmic_bytes_per_launch": byt,
+    out["gdn_b8_n64"] = {"ms_per_launch": ms, "nodes_per_s_per_layer": B * N / (ms * 1e-3),
+                         "algorithmic_bytes_per_launch": byt,
                          "achieved": byt / (ms * 1e-3) / 1e9, "unit": "GB/s"}
     torch.cuda.synchronize()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
