@@ -30,8 +30,10 @@
 // NPT (32 or 64) so every loop has a fixed trip count and the tensor-core
 // fragments of a step are loaded together.  With early prefetch the state
 // rows and the tree are fetched before the kernel waits for its predecessor.
-// It writes u, g and a copy of k as the factors commit needs, and never
-// writes S_0 (rollback is free).
+// It writes u, g and a copy of k as the factors commit needs.  A plain
+// verify never writes S_0 (rollback is free); with a pending path (deferred
+// commit) a CTA first applies the previous step's accepted path to its rows
+// and writes those rows back, so the state is the committed one again.
 #include "common.cuh"
 #include "kernels.h"
 #include "tree.cuh"
