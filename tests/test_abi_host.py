@@ -169,3 +169,14 @@ def test_structs_keep_the_tensors_they_point_to():
     del f, c
     gc.collect()
     assert ref() is None and kref() is None
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    # The product path has no fallback: without libdflv.so every entry point
+    # raises instead of computing anything.
+    monkeypatch.setattr(dflv, "_lib", None)
+    monkeypatch.setattr(dflv, "LIB_PATH", str(tmp_path / "libdflv.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        dflv.load()
+    with pytest.raises(RuntimeError, match="not built"):
+        dflv.dflv_accept_greedy(1, 2, 4, 16, 16, 16, 16, 16, 16, 16, 16, 16)
