@@ -773,25 +773,52 @@ def run_gpu(args, rank, world):
 
 
 # ---------------------------------------------------------------------------- CPU oracle
-def oracle_block_sample(host):
+def oracle_block_sample(host, parts=None):
     """The oracle on one [GDN, GDN, GDN, attention] block of the step plus
-    accept and commit of that block: returns seconds."""
+    accept and commit of that block: returns seconds.  With a list `parts`,
+    appends the seconds of each part (GDN verify of the three layers,
+    attention verify, accept, commit)."""
     import oracle
 
     parent, n_nodes = host["parent"], host["n_nodes"]
-    t = time.perf_counter()
     gdn_layers = [d for kind, d in host["layers"][:4] if kind == "gdn"]
+    a = host["layers"][3][1]
+    cache = synth.copy_cache(a["cache"])   # the sample's own cache, outside the timed parts
+    t0 = time.perf_counter()
     for d in gdn_layers:
         oracle.tree_gdn_verify(parent, n_nodes, d["q"], d["k"], d["v"], d["beta"], d["log_alpha"], d["state"])
-    a = host["layers"][3][1]
-    cache = synth.copy_cache(a["cache"])
+    t1 = time.perf_counter()
     oracle.tree_attn_verify(parent, n_nodes, np.array([CTX], np.int32), a["q"], a["k_new"], a["v_new"], cache,
                             WINDOW, oracle.KV_Q8_0)
+    t2 = time.perf_counter()
     path, plen, _, _ = oracle.accept_greedy(host["logits"], host["tokens"], parent, n_nodes)
+    t3 = time.perf_counter()
     for d in gdn_layers:
         oracle.gdn_commit(d["q"], d["k"], d["v"], d["beta"], d["log_alpha"], path, plen, d["state"])
     oracle.kv_commit(cache, oracle.KV_Q8_0, path, plen, np.array([CTX], np.int32))
-    return time.perf_counter() - t
+    t4 = time.perf_counter()
+    if parts is not None:
+        parts.append((t1 - t0, t2 - t1, t3 - t2, t4 - t3))
+    return t4 - t0
+
+
+def oracle_c4_sequence():
+    """The oracle on one sequence of the long-context stress shape at 22
+    nodes: attention over a 131,072-token q4_0 cache with full attention,
+    and one GDN layer; returns (attention seconds, GDN seconds)."""
+    import oracle
+
+    rng = np.random.default_rng(SEED + 41)
+    parent, n_nodes = synth.batch_trees([synth.ddtree(rng, BUDGET, VOCAB)[0]], BUDGET)
+    inp = synth.attn_inputs(rng, 1, BUDGET, ATT["Hq"], ATT["Hkv"], ATT["D"])
+    cache = synth.kv_cache(rng, 1, ATT["Hkv"], SCALE_CTX + BUDGET, ATT["D"], synth.KV_Q4_0)
+    g = synth.gdn_inputs(rng, 1, BUDGET, **GDN)
+    t0 = time.perf_counter()
+    oracle.tree_attn_verify(parent, n_nodes, np.array([SCALE_CTX], np.int32), inp["q"], inp["k_new"],
+                            inp["v_new"], cache, 0, oracle.KV_Q4_0)
+    t1 = time.perf_counter()
+    oracle.tree_gdn_verify(parent, n_nodes, g["q"], g["k"], g["v"], g["beta"], g["log_alpha"], g["state"])
+    return t1 - t0, time.perf_counter() - t1
 
 
 def cpu_baseline(host, min_seconds=3.0, min_reps=3):
@@ -803,21 +830,37 @@ def cpu_baseline(host, min_seconds=3.0, min_reps=3):
     oracle.build()
     cores = os.cpu_count() or 1
     res = {}
+    parts = []
     for threads in (cores, 1):
         used = oracle.set_threads(threads)
         ts, t0 = [], time.perf_counter()
         while len(ts) < min_reps or time.perf_counter() - t0 < min_seconds:
-            ts.append(oracle_block_sample(host))
+            ts.append(oracle_block_sample(host, parts if threads == cores else None))
         res[threads] = (used, float(np.median(ts)), len(ts))
     oracle.set_threads(cores)
     used, t, n = res[cores]
+    gdn_s, attn_s, acc_s, com_s = (float(np.median([p[j] for p in parts])) for j in range(4))
+    per_layer = {"gdn": BUDGET / (gdn_s / 3), "attn": BUDGET / attn_s, "unit": "nodes/s per layer",
+                 "accept_seconds": acc_s, "commit_seconds": com_s,
+                 "what": "the parts of the all-core sample: one GDN layer (3 per block) and one attention layer "
+                         "at the step's shapes"}
+    try:
+        c4_attn, c4_gdn = oracle_c4_sequence()
+        c4 = {"attn_seconds": c4_attn, "gdn_seconds": c4_gdn, "attn_nodes_per_s": BUDGET / c4_attn,
+              "gdn_nodes_per_s": BUDGET / c4_gdn, "cores": used,
+              "what": "one sequence at 22 nodes of the long-context stress shape (131,072-token q4_0 cache, "
+                      "full attention) on all cores; the stress shape has 8 sequences: x8 the time is an "
+                      "extrapolation, not a measurement"}
+    except Exception as e:  # a baseline that cannot run is reported, not fatal
+        c4 = {"error": f"{type(e).__name__}: {e}"}
     return {"value": BUDGET * 4 / t, "unit": UNIT, "cores": used, "kind": "oracle",
             "sample": f"one [GDN, GDN, GDN, attention] block of the step (4 of 64 layers) + accept over the "
                       f"full vocab + commit of that block; C oracle, fp64, parallel over (sequence, head) and "
                       f"output rows; median of {n} samples",
             "seconds_per_sample": t, "samples": n,
             "single_thread": {"value": BUDGET * 4 / res[1][1], "cores": 1, "seconds_per_sample": res[1][1],
-                              "samples": res[1][2]}}
+                              "samples": res[1][2]},
+            "per_layer": per_layer, "long_context_one_sequence": c4}
 
 
 # ---------------------------------------------------------------------------- distributed plumbing
