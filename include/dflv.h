@@ -81,7 +81,8 @@ typedef enum {
 enum {
     DFLV_DEV_TOPOLOGY = 1, /* parent[0] != -1, parent[i] outside [0, i), n outside [1, N_max] */
     DFLV_DEV_CAPACITY = 2, /* P < 0 or P + n > cap in an attention layer */
-    DFLV_DEV_PATH = 4,     /* commit got path_len outside [1, N_max] or a node outside [0, N_max) */
+    DFLV_DEV_PATH = 4,     /* an accepted path with a length outside the call's range (each call
+                              states it) or a node outside [0, N_max) */
     DFLV_DEV_TIMEOUT = 8   /* a bounded wait for an asynchronous copy gave up */
 };
 
@@ -382,7 +383,10 @@ dflv_status dflv_accept_greedy(int32_t B, int32_t N_max, int32_t vocab, const fl
  * write).  Slots [P + L, P + N_max) are left unspecified.  Rejected nodes
  * need no work: verify never wrote the committed state or slots < P.
  * The path must be a root-to-node path of the verified tree (as accept
- * produces); N_max must equal the verify calls' N_max. */
+ * produces); N_max must equal the verify calls' N_max.  path_len[b] must lie
+ * in [1, N_max] and every path node in [0, N_max): otherwise DFLV_DEV_PATH is
+ * raised, sequence b's states and cache slots are left as they were, and its
+ * n_past is unspecified. */
 dflv_status dflv_commit_rollback(const dflv_gdn_desc* gdn, int32_t n_gdn, float* const* states,
                                  const dflv_gdn_factors* factors, const dflv_attn_desc* attn,
                                  int32_t n_attn, const dflv_kv_layer* caches,
