@@ -28,7 +28,7 @@ _SOURCES = [os.path.join(_HERE, "oracle.c"), os.path.join(_HERE, "oracle.h")]
 _lock = threading.Lock()
 _lib = None
 
-KV_Q8_0, KV_Q4_0, KV_F32, KV_Q8_0_Q4_0, KV_Q4_0_Q8_0 = 0, 1, 2, 3, 4
+KV_Q8_0, KV_Q4_0, KV_F32, KV_Q8_0_Q4_0, KV_Q4_0_Q8_0, KV_TQ3_0 = 0, 1, 2, 3, 4, 5
 OK, ERR_ARG, ERR_TOPOLOGY, ERR_CAPACITY = 0, 1, 2, 4
 
 
@@ -70,12 +70,14 @@ def _load():
             lib.orc_tree_gdn_verify.argtypes = [I] * 6 + [P] * 10
             lib.orc_tree_gdn_verify_bruteforce.argtypes = [I] * 6 + [P] * 9
             lib.orc_gdn_commit.argtypes = [I] * 6 + [P] * 8
-            for f in ("orc_quantize_q8_0", "orc_quantize_q4_0"):
+            for f in ("orc_quantize_q8_0", "orc_quantize_q4_0", "orc_quantize_tq3_0"):
                 getattr(lib, f).argtypes = [P, P, P]
                 getattr(lib, f).restype = None
-            for f in ("orc_dequantize_q8_0", "orc_dequantize_q4_0"):
+            for f in ("orc_dequantize_q8_0", "orc_dequantize_q4_0", "orc_dequantize_tq3_0"):
                 getattr(lib, f).argtypes = [P, ctypes.c_uint16, P]
                 getattr(lib, f).restype = None
+            lib.orc_fwht_f32.argtypes = [I, P]
+            lib.orc_fwht_f32.restype = None
             lib.orc_tree_attn_verify.argtypes = [I] * 8 + [ctypes.c_double] + [P] * 11 + [P, I]
             lib.orc_accept_greedy.argtypes = [I, I, I] + [P] * 8
             lib.orc_kv_commit.argtypes = [I] * 6 + [P] * 7
@@ -225,6 +227,34 @@ def dequantize_q4_0(nib, d16):
     return x
 
 
+def quantize_tq3_0(x):
+    """32 fp32 values -> (12 code bytes, fp16 scale bits)."""
+    x = _c(x, np.float32)
+    assert x.shape == (32,)
+    codes = np.zeros(12, np.uint8)
+    d = np.zeros(1, np.uint16)
+    _load().orc_quantize_tq3_0(_p(x), _p(codes), _p(d))
+    return codes, int(d[0])
+
+
+def dequantize_tq3_0(codes, d16):
+    codes = _c(codes, np.uint8)
+    assert codes.shape == (12,)
+    x = np.zeros(32, np.float64)
+    _load().orc_dequantize_tq3_0(_p(codes), int(d16), _p(x))
+    return x
+
+
+def fwht(x):
+    """The TQ3_0 rotation of each row of x (fp32, last axis a power of two),
+    as the oracle's cache writes apply it."""
+    y = np.array(x, dtype=np.float32, order="C", copy=True)
+    n = y.shape[-1]
+    for row in y.reshape(-1, n):
+        _load().orc_fwht_f32(n, row.ctypes.data_as(ctypes.c_void_p))
+    return y
+
+
 # ---------------------------------------------------------------- attention
 def tree_attn_verify(parent, n_nodes, n_past, q, k_new, v_new, cache, window, kv_type,
                      scale=None, rows=None):
@@ -278,7 +308,8 @@ def kv_commit(cache, kv_type, path, path_len, n_past):
     B, N = path.shape
     kq = cache["kq"]
     Hkv, cap = kq.shape[1], kq.shape[2]
-    D = kq.shape[3] * (2 if kv_type in (KV_Q4_0, KV_Q4_0_Q8_0) else 1)
+    D = (kq.shape[3] * 8 // 3 if kv_type == KV_TQ3_0
+         else kq.shape[3] * (2 if kv_type in (KV_Q4_0, KV_Q4_0_Q8_0) else 1))
     rc = _load().orc_kv_commit(B, N, Hkv, D, cap, int(kv_type), _p(path), _p(path_len),
                                _p(n_past), _p(cache["kq"]), _p(cache["vq"]),
                                _p(cache.get("ks")), _p(cache.get("vs")))

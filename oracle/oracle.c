@@ -306,6 +306,63 @@ void orc_dequantize_q4_0(const uint8_t* nib, uint16_t d16, double* x) {
     }
 }
 
+/* TQ3_0 (readings in oracle.h): d = amax / 3, three-bit codes packed as a
+ * little-endian bit stream, the same rounding as q8_0 / q4_0. */
+void orc_quantize_tq3_0(const float* x, uint8_t* codes, uint16_t* d16) {
+    float amax = 0.0f;
+    for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(x[j]));
+    float d = amax / 3.0f;
+    float id = (d != 0.0f) ? 1.0f / d : 0.0f;
+    *d16 = orc_float_to_half_rn(d);
+    for (int j = 0; j < 12; ++j) codes[j] = 0;
+    for (int j = 0; j < 32; ++j) {
+        float r = roundf(x[j] * id);
+        if (r > 3.0f) r = 3.0f;
+        if (r < -4.0f) r = -4.0f;
+        unsigned c = (unsigned)((int)r + 4);
+        int bit = 3 * j;
+        codes[bit / 8] |= (uint8_t)(c << (bit % 8));
+        if (bit % 8 > 5) codes[bit / 8 + 1] |= (uint8_t)(c >> (8 - bit % 8));
+    }
+}
+
+void orc_dequantize_tq3_0(const uint8_t* codes, uint16_t d16, double* x) {
+    double d = (double)orc_half_to_float(d16);
+    for (int j = 0; j < 32; ++j) {
+        int bit = 3 * j;
+        unsigned v = codes[bit / 8];
+        if (bit / 8 + 1 < 12) v |= (unsigned)codes[bit / 8 + 1] << 8;
+        int c = (int)((v >> (bit % 8)) & 7u);
+        x[j] = d * (double)(c - 4);
+    }
+}
+
+void orc_fwht_f32(int n, float* x) {
+    for (int h = 1; h < n; h *= 2)
+        for (int i = 0; i < n; i += 2 * h)
+            for (int j = i; j < i + h; ++j) {
+                float a = x[j], b = x[j + h];
+                x[j] = a + b;
+                x[j + h] = a - b;
+            }
+    const float s = (float)(1.0 / sqrt((double)n));
+    for (int j = 0; j < n; ++j) x[j] *= s;
+}
+
+/* The same transform in fp64, for the query and the output (no integer
+ * depends on them). */
+static void fwht_f64(int n, double* x) {
+    for (int h = 1; h < n; h *= 2)
+        for (int i = 0; i < n; i += 2 * h)
+            for (int j = i; j < i + h; ++j) {
+                double a = x[j], b = x[j + h];
+                x[j] = a + b;
+                x[j + h] = a - b;
+            }
+    const double s = 1.0 / sqrt((double)n);
+    for (int j = 0; j < n; ++j) x[j] *= s;
+}
+
 /* ------------------------------------------------------------------------ */
 /* attention tree verify                                                     */
 /* ------------------------------------------------------------------------ */
@@ -326,8 +383,12 @@ static int plane_type(int type, int which) {
 }
 
 static size_t kv_row_bytes(int type, int D) {
-    return type == ORC_KV_Q8_0 ? (size_t)D : type == ORC_KV_Q4_0 ? (size_t)D / 2 : (size_t)D * 4;
+    return type == ORC_KV_Q8_0 ? (size_t)D : type == ORC_KV_Q4_0 ? (size_t)D / 2
+           : type == ORC_KV_TQ3_0 ? (size_t)D / 32 * 12 : (size_t)D * 4;
 }
+
+/* Keys stored as TQ3_0 put the whole attention in the rotated basis. */
+static int kv_rotated(int type) { return type == ORC_KV_TQ3_0; }
 
 static size_t kv_row_index(const kv_cache* c, int b, int h, int pos) {
     return ((size_t)b * c->Hkv + h) * c->cap + pos;
@@ -349,6 +410,8 @@ static void kv_read_row(const kv_cache* c, int which, int b, int h, int pos, dou
     for (int blk = 0; blk < c->D / 32; ++blk) {
         if (type == ORC_KV_Q8_0)
             orc_dequantize_q8_0((const int8_t*)qrow + 32 * blk, srow[blk], x + 32 * blk);
+        else if (type == ORC_KV_TQ3_0)
+            orc_dequantize_tq3_0(qrow + 12 * blk, srow[blk], x + 32 * blk);
         else
             orc_dequantize_q4_0(qrow + 16 * blk, srow[blk], x + 32 * blk);
     }
@@ -361,27 +424,32 @@ static void kv_write_row(kv_cache* c, int which, int b, int h, int pos, const ui
     uint16_t* sc = which ? c->vs : c->ks;
     const int type = plane_type(c->type, which);
     uint8_t* qrow = plane + row * kv_row_bytes(type, c->D);
-    float x[32];
     if (type == ORC_KV_F32) {
         float* f = (float*)qrow;
         for (int d = 0; d < c->D; ++d) f[d] = (float)orc_bf16_to_double(src[d]);
         return;
     }
+    float* x = malloc((size_t)c->D * sizeof(float));
+    for (int d = 0; d < c->D; ++d) x[d] = (float)orc_bf16_to_double(src[d]);
+    if (kv_rotated(c->type)) orc_fwht_f32(c->D, x);   /* keys and values alike */
     uint16_t* srow = sc + row * (c->D / 32);
     for (int blk = 0; blk < c->D / 32; ++blk) {
-        for (int j = 0; j < 32; ++j) x[j] = (float)orc_bf16_to_double(src[32 * blk + j]);
         if (type == ORC_KV_Q8_0)
-            orc_quantize_q8_0(x, (int8_t*)qrow + 32 * blk, &srow[blk]);
+            orc_quantize_q8_0(x + 32 * blk, (int8_t*)qrow + 32 * blk, &srow[blk]);
+        else if (type == ORC_KV_TQ3_0)
+            orc_quantize_tq3_0(x + 32 * blk, qrow + 12 * blk, &srow[blk]);
         else
-            orc_quantize_q4_0(x, qrow + 16 * blk, &srow[blk]);
+            orc_quantize_q4_0(x + 32 * blk, qrow + 16 * blk, &srow[blk]);
     }
+    free(x);
 }
 
 static int attn_dims_ok(int B, int N, int Hq, int Hkv, int D, int cap, int window, int type) {
     if (B < 1 || N < 1 || N > 64 || Hkv < 1 || Hq < Hkv || Hq % Hkv != 0) return 0;
     if (D < 1 || cap < 1 || window < 0) return 0;
-    if (type < ORC_KV_Q8_0 || type > ORC_KV_Q4_0_Q8_0) return 0;
+    if (type < ORC_KV_Q8_0 || type > ORC_KV_TQ3_0) return 0;
     if (type != ORC_KV_F32 && D % 32 != 0) return 0;
+    if (kv_rotated(type) && (D & (D - 1)) != 0) return 0;   /* the rotation needs a power of two */
     return 1;
 }
 
@@ -404,6 +472,7 @@ static void attn_one(const kv_cache* c, int N, int Hq, int window, double scale,
     int ipos = P + depth[i];
     const uint16_t* qrow = q + (((size_t)b * N + i) * Hq + h) * D;
     for (int d = 0; d < D; ++d) qd[d] = orc_bf16_to_double(qrow[d]);
+    if (kv_rotated(c->type)) fwht_f64(D, qd);   /* the query into the keys' basis */
     /* pass 1: the maximum score */
     double mx = -INFINITY;
     for (int slot = 0; slot < P + n; ++slot) {
@@ -443,7 +512,9 @@ static void attn_one(const kv_cache* c, int N, int Hq, int window, double scale,
         for (int d = 0; d < D; ++d) acc[d] += p * val[d];
     }
     float* o = out + (((size_t)b * N + i) * Hq + h) * D;
-    for (int d = 0; d < D; ++d) o[d] = (float)(acc[d] / den);
+    for (int d = 0; d < D; ++d) acc[d] /= den;
+    if (kv_rotated(c->type)) fwht_f64(D, acc);  /* back from the values' basis */
+    for (int d = 0; d < D; ++d) o[d] = (float)acc[d];
 }
 
 int orc_tree_attn_verify(int B, int N, int Hq, int Hkv, int D, int cap, int window,
@@ -573,7 +644,7 @@ int orc_kv_commit(int B, int N, int Hkv, int D, int cap, int kv_type,
      * source rows are read before any is written, because a destination can
      * be another accepted node's source (path [0, 2, 3]: 2 -> 1, 3 -> 2). */
     if (B < 1 || N < 1 || N > 64 || Hkv < 1 || D < 1 || cap < 1) return ORC_ERR_ARG;
-    if (kv_type < ORC_KV_Q8_0 || kv_type > ORC_KV_Q4_0_Q8_0) return ORC_ERR_ARG;
+    if (kv_type < ORC_KV_Q8_0 || kv_type > ORC_KV_TQ3_0) return ORC_ERR_ARG;
     kv_cache c = {B, Hkv, D, cap, kv_type, kq, vq, ks, vs};
     size_t sb = (kv_type == ORC_KV_F32) ? 0 : (size_t)(D / 32) * sizeof(uint16_t);
     uint8_t* tmp = malloc((size_t)N * ((size_t)D * 4 + sb));

@@ -52,7 +52,8 @@
  *   GDN out  [B][N][Hv][dv] f32
  *   attention q [B][N][Hq][D] bf16; k_new, v_new [B][N][Hkv][D] bf16
  *   cache planes per layer: quants [B][Hkv][cap][D] (int8, q8_0),
- *       [B][Hkv][cap][D/2] (uint8 nibbles, q4_0) or [B][Hkv][cap][D] f32;
+ *       [B][Hkv][cap][D/2] (uint8 nibbles, q4_0), [B][Hkv][cap][3D/8] (uint8
+ *       three-bit codes, TQ3_0) or [B][Hkv][cap][D] f32;
  *       scales [B][Hkv][cap][D/32] fp16 bits (unused for f32)
  *   attention out [B][N][Hq][D] f32
  *   logits [B][N][V] f32; tokens [B][N] int32
@@ -70,7 +71,8 @@ enum { ORC_OK = 0, ORC_ERR_ARG = 1, ORC_ERR_TOPOLOGY = 2, ORC_ERR_CAPACITY = 4 }
 /* Cache types; the last two quantise keys and values differently ("Luce
  * DFlash" README, "Asymmetric K/V quantization"): K q8_0 with V q4_0, and
  * K q4_0 with V q8_0. */
-enum { ORC_KV_Q8_0 = 0, ORC_KV_Q4_0 = 1, ORC_KV_F32 = 2, ORC_KV_Q8_0_Q4_0 = 3, ORC_KV_Q4_0_Q8_0 = 4 };
+enum { ORC_KV_Q8_0 = 0, ORC_KV_Q4_0 = 1, ORC_KV_F32 = 2, ORC_KV_Q8_0_Q4_0 = 3, ORC_KV_Q4_0_Q8_0 = 4,
+       ORC_KV_TQ3_0 = 5 };
 
 /* ---- scalar conversions (the oracle's own) ---- */
 double orc_bf16_to_double(uint16_t h);
@@ -118,6 +120,25 @@ void orc_quantize_q8_0(const float* x, int8_t* qs, uint16_t* d16);
 void orc_quantize_q4_0(const float* x, uint8_t* nib, uint16_t* d16);
 void orc_dequantize_q8_0(const int8_t* qs, uint16_t d16, double* x);
 void orc_dequantize_q4_0(const uint8_t* nib, uint16_t d16, double* x);
+
+/* TQ3_0 ("Luce DFlash" README, "Asymmetric K/V quantization": 3.5 bits per
+ * value, an FWHT rotation applied to the query and undone on the attention
+ * output when the keys are TQ3_0).  The pages give neither the block layout,
+ * the codebook nor the rotation size; the readings here: a block of 32
+ * values holds one fp16 scale d = amax / 3 and 32 three-bit codes
+ * c = clamp(round_half_away(x * (1/d)), -4, 3) + 4 (12 bytes, code j in bits
+ * 3j .. 3j+2 of the little-endian 96-bit block), x = d * (c - 4); the
+ * rotation is the orthonormal Walsh-Hadamard transform over the whole head
+ * dimension (a power of two), applied to keys AND values before they are
+ * quantised (the output can only be rotated back if the values were rotated
+ * too), to the query, and again to the output (the orthonormal transform is
+ * its own inverse). */
+void orc_quantize_tq3_0(const float* x, uint8_t* codes, uint16_t* d16);
+void orc_dequantize_tq3_0(const uint8_t* codes, uint16_t d16, double* x);
+/* The rotation in fp32, in place (it decides the stored codes): butterflies
+ * of stride 1, 2, 4, ..., n/2 in that order, each (a, b) -> (a + b, a - b),
+ * then one multiplication by the fp32 value of 1/sqrt(n). */
+void orc_fwht_f32(int n, float* x);
 
 /* ---- attention tree verify ---- */
 /* Writes the quantised tree keys/values into cache slots [P, P+n) and then

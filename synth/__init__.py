@@ -25,7 +25,7 @@ import heapq
 
 import numpy as np
 
-KV_Q8_0, KV_Q4_0, KV_F32, KV_Q8_0_Q4_0, KV_Q4_0_Q8_0 = 0, 1, 2, 3, 4
+KV_Q8_0, KV_Q4_0, KV_F32, KV_Q8_0_Q4_0, KV_Q4_0_Q8_0, KV_TQ3_0 = 0, 1, 2, 3, 4, 5
 
 GDN_27B = dict(Hk=16, Hv=48, dk=128, dv=128)
 ATTN_27B = dict(Hq=24, Hkv=4, D=256)
@@ -225,6 +225,8 @@ def kv_cache(rng, B, Hkv, cap, D, kv_type, scale_std=0.02):
 
     q8_0: int8 codes ~ U[-127, 127], fp16 scales ~ |N(0, scale_std)|;
     q4_0: 4-bit codes ~ U[0, 15] (two per byte), same scales;
+    TQ3_0: 3-bit codes ~ U[0, 7] (any byte pattern is 32 valid codes per 12
+          bytes), same scales;
     f32:  values ~ N(0, 1), no scale planes;
     the asymmetric types draw each plane in its own format."""
     if kv_type == KV_F32:
@@ -238,10 +240,12 @@ def kv_cache(rng, B, Hkv, cap, D, kv_type, scale_std=0.02):
     def plane(t):
         if t == KV_Q8_0:
             return rng.integers(-127, 128, size=(B, Hkv, cap, D), dtype=np.int8)
+        if t == KV_TQ3_0:
+            return rng.integers(0, 256, size=(B, Hkv, cap, D // 32 * 12), dtype=np.uint8)
         return rng.integers(0, 256, size=(B, Hkv, cap, D // 2), dtype=np.uint8)
 
     planes = {KV_Q8_0: (KV_Q8_0, KV_Q8_0), KV_Q4_0: (KV_Q4_0, KV_Q4_0), KV_Q8_0_Q4_0: (KV_Q8_0, KV_Q4_0),
-              KV_Q4_0_Q8_0: (KV_Q4_0, KV_Q8_0)}
+              KV_Q4_0_Q8_0: (KV_Q4_0, KV_Q8_0), KV_TQ3_0: (KV_TQ3_0, KV_TQ3_0)}
     if kv_type not in planes:
         raise ValueError(kv_type)
     kt, vt = planes[kv_type]
