@@ -76,13 +76,14 @@ def test_gdn_inputs_recipe():
     assert 0.015 < float(g["state"].std()) < 0.025
 
 
-@pytest.mark.parametrize("kv_type", [synth.KV_Q8_0, synth.KV_Q4_0, synth.KV_Q8_0_Q4_0, synth.KV_Q4_0_Q8_0])
+@pytest.mark.parametrize("kv_type", [synth.KV_Q8_0, synth.KV_Q4_0, synth.KV_Q8_0_Q4_0, synth.KV_Q4_0_Q8_0,
+                                     synth.KV_TQ3_0])
 def test_kv_cache_recipe(kv_type):
     rng = np.random.default_rng(5)
     D = 128
     c = synth.kv_cache(rng, 2, 3, 40, D, kv_type)
     widths = {synth.KV_Q8_0: (D, D), synth.KV_Q4_0: (D // 2, D // 2), synth.KV_Q8_0_Q4_0: (D, D // 2),
-              synth.KV_Q4_0_Q8_0: (D // 2, D)}[kv_type]
+              synth.KV_Q4_0_Q8_0: (D // 2, D), synth.KV_TQ3_0: (D // 32 * 12, D // 32 * 12)}[kv_type]
     for plane, w in zip(("kq", "vq"), widths):
         a = c[plane]
         assert a.shape == (2, 3, 40, w)
