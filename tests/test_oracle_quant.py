@@ -113,3 +113,42 @@ def test_zero_block_gives_zero_scale_and_codes(orc):
     assert d16 == 0 and not qs.any()
     nib, d16 = orc.quantize_q4_0(np.zeros(32, np.float32))
     assert d16 == 0 and (nib == 0x88).all()
+
+
+def test_divisor_examples_separate_the_two_readings(golden):
+    # The quantiser could divide by the stored fp16 scale or multiply by the
+    # fp32 reciprocal of the fp32 scale; both are plausible readings of the
+    # format.  The examples marked with a "divided by d16" variant must give
+    # different codes under the two, or they would not pin the choice.  The
+    # variant is recomputed here in exact rationals (round half away).
+    from fractions import Fraction
+
+    def half_away(fr):
+        return int(fr + Fraction(1, 2)) if fr >= 0 else -int(-fr + Fraction(1, 2))
+
+    seen = 0
+    for ex in golden["quantize"]:
+        alt = ex.get("codes_if_divided_by_d16") or ex.get("bytes_if_divided_by_d16")
+        if alt is None:
+            continue
+        seen += 1
+        d16 = Fraction(float(np.uint16(int(ex["d16"], 16)).view(np.float16)))
+        qmin, qmax = (-127, 127) if ex["type"] == "q8_0" else (-8, 7)
+        codes = np.zeros(32, np.int64)
+        for j, val in ex["x_nonzero"].items():
+            codes[int(j)] = min(qmax, max(qmin, half_away(Fraction(val) / d16)))
+        if ex["type"] == "q8_0":
+            want_alt = np.zeros(32, np.int64)
+            for j, c in ex["codes_if_divided_by_d16"].items():
+                want_alt[int(j)] = c
+            np.testing.assert_array_equal(codes, want_alt)
+            want = np.zeros(32, np.int64)
+            for j, c in ex["codes_nonzero"].items():
+                want[int(j)] = c
+            assert not np.array_equal(codes, want)
+        else:
+            c8 = codes + 8
+            alt_bytes = (c8[:16] | (c8[16:] << 4)).astype(np.uint8)
+            np.testing.assert_array_equal(alt_bytes, [int(b, 16) for b in ex["bytes_if_divided_by_d16"]])
+            assert not np.array_equal(alt_bytes, [int(b, 16) for b in ex["bytes"]])
+    assert seen == 2
