@@ -62,15 +62,16 @@ def is_attn(layer):
 MAX_REPLAYS = 512          # replays between resets that the cache capacity allows
 
 
-def make_host_inputs(rng, n_layers=N_LAYERS):
-    """Host-side inputs of the step (numpy), seeded; the first n_layers layers."""
+def make_host_inputs(rng, n_layers=N_LAYERS, ctx=CTX):
+    """Host-side inputs of the step (numpy), seeded; the first n_layers layers
+    over a cache of ctx committed tokens."""
     par, tok = synth.ddtree(rng, BUDGET, VOCAB)
     parent, n_nodes = synth.batch_trees([par], BUDGET)
     tokens = tok[None].astype(np.int32)
     planted = synth.deepest_path(par)[:PLANT]
     logits = synth.random_logits(rng, 1, BUDGET, VOCAB)
     synth.plant_path(logits, tokens, planted)
-    cap = CTX + BUDGET * MAX_REPLAYS + 64
+    cap = ctx + BUDGET * MAX_REPLAYS + 64
     layers = []
     for layer in range(n_layers):
         if is_attn(layer):
@@ -86,8 +87,19 @@ def make_host_inputs(rng, n_layers=N_LAYERS):
     conv = [synth.conv_inputs(crng, 1, BUDGET, CONV["C"], CONV["K"]) for kind, _ in layers if kind == "gdn"]
     # the draft's logits for the next tree (its construction is measured beside the step)
     draft = synth.draft_logits(np.random.default_rng(SEED + 104729), 1, DRAFT_BLOCK, VOCAB)
-    return dict(parent=parent, n_nodes=n_nodes, tokens=tokens, logits=logits, layers=layers, cap=cap,
+    return dict(parent=parent, n_nodes=n_nodes, tokens=tokens, logits=logits, layers=layers, cap=cap, ctx=ctx,
                 planted=planted, conv=conv, draft=draft)
+
+
+def step_inputs(host):
+    """The per-step inputs of a host input set, in the order the step's input
+    buffer packs them: (name, array)."""
+    out = [("parent", host["parent"]), ("n_nodes", host["n_nodes"]), ("tokens", host["tokens"]),
+           ("logits", host["logits"])]
+    for li, (kind, d) in enumerate(host["layers"]):
+        keys = ("q", "k_new", "v_new") if kind == "attn" else ("q", "k", "v", "beta", "log_alpha")
+        out += [(f"{li}.{k}", d[k]) for k in keys]
+    return [(name, np.ascontiguousarray(a)) for name, a in out]
 
 
 # ---------------------------------------------------------------------------- algorithmic bytes
@@ -263,32 +275,18 @@ class GpuStep:
         self.host = host
         cap = host["cap"]
         N = BUDGET
+        self.ctx = host["ctx"]
         # ---- per-step inputs: one packed pinned host buffer and its device twin
-        entries = []
-
-        def add(name, arr):
-            entries.append((name, np.ascontiguousarray(arr)))
-
-        add("parent", host["parent"])
-        add("n_nodes", host["n_nodes"])
-        add("tokens", host["tokens"])
-        add("logits", host["logits"])
-        for li, (kind, d) in enumerate(host["layers"]):
-            keys = ("q", "k_new", "v_new") if kind == "attn" else ("q", "k", "v", "beta", "log_alpha")
-            for k in keys:
-                add(f"{li}.{k}", d[k])
         offs, total = {}, 0
-        for name, a in entries:
+        for name, a in step_inputs(host):
             total = (total + 255) // 256 * 256
             offs[name] = (total, a)
             total += a.nbytes
+        self.offs = offs
         self.in_bytes = total
         self.h_in = t.empty(total, dtype=t.uint8, pin_memory=True)
-        hv = self.h_in.numpy()
-        for name, (o, a) in offs.items():
-            hv[o:o + a.nbytes] = a.view(np.uint8).reshape(-1)
         self.d_in = t.empty(total, dtype=t.uint8, device=dev)
-        self.d_in.copy_(self.h_in)
+        self.load_inputs(host)
 
         def view(name):
             o, a = offs[name]
@@ -300,8 +298,7 @@ class GpuStep:
                                                                view("logits"))
         # ---- persistent state and outputs
         self.status = t.zeros(1, dtype=t.int32, device=dev)
-        self.n_past0 = CTX
-        self.n_past = t.full((1,), CTX, dtype=t.int32, device=dev)
+        self.n_past = t.full((1,), self.ctx, dtype=t.int32, device=dev)
         self.path = t.zeros((1, N), dtype=t.int32, device=dev)
         self.path_len = t.zeros(1, dtype=t.int32, device=dev)
         self.next_token = t.zeros(1, dtype=t.int32, device=dev)
@@ -360,6 +357,16 @@ class GpuStep:
                          n_nodes=t.empty(1, dtype=t.int32, device=dev), score=t.empty((1, N), device=dev))
         self.ddtree_desc = dflv.ddtree_desc(1, DRAFT_BLOCK, VOCAB, TOPK, N, TAU)
 
+    def load_inputs(self, host):
+        """Packs a host input set of the same shapes into the pinned buffer
+        and copies it to the device buffer the captured step reads."""
+        hv = self.h_in.numpy()
+        for name, a in step_inputs(host):
+            o, a0 = self.offs[name]
+            assert a.shape == a0.shape and a.dtype == a0.dtype, name
+            hv[o:o + a.nbytes] = a.view(np.uint8).reshape(-1)
+        self.d_in.copy_(self.h_in)
+
     # one pass of the hot path: every layer's verify (the GDN layers first
     # commit the previous step's accepted path into their state: deferred
     # commit), acceptance, commit of the KV caches.  Step `par` writes
@@ -388,7 +395,7 @@ class GpuStep:
         """Committed state back to its initial value (between passes)."""
         for s, s0 in zip(self.states, self.state0):
             s.copy_(s0)
-        self.n_past.fill_(CTX)
+        self.n_past.fill_(self.ctx)
         self.path_len.zero_()  # nothing pending
         for c in self.conv:
             c["state"].copy_(c["state0"])
@@ -653,6 +660,26 @@ def scale_measure(torch, dflv, flush, reps=8, rounds=10):
     return out
 
 
+def capture_step(S, torch, stream):
+    """Eager warm-up of the step on the capture stream (sets kernel
+    attributes once), reset, then one CUDA graph per step parity (the factor
+    sets alternate between steps).  Returns the two graphs; the state is
+    reset, so the first replay has nothing pending."""
+    with torch.cuda.stream(stream):
+        S.step(0)
+        S.step(1)
+    torch.cuda.synchronize()
+    S.reset()
+    torch.cuda.synchronize()
+    graphs = [torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()]
+    for par in range(2):
+        with torch.cuda.graph(graphs[par], stream=stream):
+            S.step(par)
+    torch.cuda.synchronize()
+    assert int(S.status.item()) == 0, f"device status {int(S.status.item())}"
+    return graphs
+
+
 def run_gpu(args, rank, world):
     import torch
 
@@ -666,20 +693,7 @@ def run_gpu(args, rank, world):
     S = GpuStep(host, torch, dflv)
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
-    # eager warm-up on the capture stream (sets kernel attributes once), then
-    # capture the two step parities (factor sets alternate between steps)
-    with torch.cuda.stream(stream):
-        S.step(0)
-        S.step(1)
-    torch.cuda.synchronize()
-    S.reset()
-    torch.cuda.synchronize()
-    graphs = [torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()]
-    for par in range(2):
-        with torch.cuda.graph(graphs[par], stream=stream):
-            S.step(par)
-    torch.cuda.synchronize()
-    assert int(S.status.item()) == 0, f"device status {int(S.status.item())}"
+    graphs = capture_step(S, torch, stream)
     count = [0]
 
     def replay():
@@ -715,7 +729,7 @@ def run_gpu(args, rank, world):
         # every replay commits its accepted path and so advances the cache
         # position; the phases below start again at the context length (the
         # window keeps each step's work the same at any position)
-        S.n_past.fill_(CTX)
+        S.n_past.fill_(S.ctx)
 
     clocks.mark()
     load_for(CLOCK_LOAD_S, MAX_REPLAYS - args.warmup - 1)
@@ -755,6 +769,8 @@ def run_gpu(args, rank, world):
     #      chain time / launches
     flush = L2Flush(torch)
     per, dist = kernel_chain_ms(S, torch, stream, args.steps, args.warmup, flush)
+    status = int(S.status.item())
+    assert status == 0, f"device status {status} after the per-kernel chains"
     scale = scale_measure(torch, dflv, flush) if not args.no_scale else {}
     del flush
     # ---- end to end: pinned host inputs -> device, step, result -> host, every step
@@ -779,6 +795,8 @@ def run_gpu(args, rank, world):
         _ = int(S.h_out[BUDGET])
     e1.record()
     torch.cuda.synchronize()
+    status = int(S.status.item())
+    assert status == 0, f"device status {status} after the end-to-end steps"
     e2e_ms = reduce_max(world, e0.elapsed_time(e1))
     d2h = (BUDGET + 2) * 4
     return dict(ms=ms_max, per=per, dist=dist, step_pct=step_pct, scale=scale, clocks=clk, L=L, e2e_ms=e2e_ms, h2d=S.in_bytes, d2h=d2h,
@@ -974,7 +992,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-scale", action="store_true", help="skip the at-scale kernel measurements")

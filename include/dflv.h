@@ -351,12 +351,13 @@ size_t dflv_attn_workspace_size(const dflv_attn_desc* desc);
 /* Greedy acceptance                                                         */
 /* ------------------------------------------------------------------------ */
 
-/* best[b][i] = argmax_v logits[b][i][v] (ties: lowest v).  Then from the
+/* best[b][i] = argmax_v logits[b][i][v] (ties: lowest v; a NaN logit counts
+ * as -infinity, so a row of NaN or -infinity gives 0).  Then from the
  * root: while a child c of the current node has tokens[b][c] == best of the
  * current node, move to the lowest-index such c.  path[b][0..L) = visited
  * nodes (path[b][0] = 0), path_len[b] = L >= 1 = tokens committed this
  * step, next_token[b] = best of the last visited node.
- *   logits [B][N_max][vocab] f32 (finite); tokens, parent [B][N_max] int32
+ *   logits [B][N_max][vocab] f32; tokens, parent [B][N_max] int32
  *   path, best [B][N_max] int32; path_len, next_token [B] int32
  * Everything stays on the device, so accept -> commit needs no host sync. */
 dflv_status dflv_accept_greedy(int32_t B, int32_t N_max, int32_t vocab, const float* logits,

@@ -603,12 +603,19 @@ int orc_accept_greedy(int B, int N, int V, const float* logits, const int32_t* t
         uint64_t anc[64];
         const int32_t* par = parent + (size_t)b * N;
         if (n > N || orc_tree_topology(n, par, depth, anc) != ORC_OK) return ORC_ERR_TOPOLOGY;
-        /* target argmax of every node; ties go to the lowest vocab index */
+        /* target argmax of every node; ties go to the lowest vocab index, and
+         * a NaN logit counts as -infinity (an all-NaN row gives index 0) */
         for (int i = 0; i < n; ++i) {
             const float* row = logits + ((size_t)b * N + i) * V;
             int arg = 0;
-            for (int t = 1; t < V; ++t)
-                if (row[t] > row[arg]) arg = t;
+            float top = isnan(row[0]) ? -INFINITY : row[0];
+            for (int t = 1; t < V; ++t) {
+                const float x = isnan(row[t]) ? -INFINITY : row[t];
+                if (x > top) {
+                    top = x;
+                    arg = t;
+                }
+            }
             best[(size_t)b * N + i] = arg;
         }
         /* walk from the root while a child carries the target's argmax token;

@@ -26,8 +26,10 @@ namespace {
 
 constexpr int kArgmaxThreads = 512;
 
-// (v, i) beats (bv, bi): larger value, or equal value and lower index.
+// (v, i) beats (bv, bi): larger value, or equal value and lower index.  A
+// NaN counts as -infinity, so an all-NaN row gives its lowest index.
 DFLV_DEVINL void better(float v, int i, float& bv, int& bi) {
+    v = (v != v) ? -INFINITY : v;
     if (v > bv || (v == bv && i < bi)) {
         bv = v;
         bi = i;

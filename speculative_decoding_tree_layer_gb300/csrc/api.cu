@@ -251,7 +251,7 @@ dflv_status dflv_commit_rollback(const dflv_gdn_desc* gdn, int32_t n_gdn, float*
     if (n_gdn < 0 || n_attn < 0) return DFLV_ERR_INVALID_ARG;
     if (n_gdn > DFLV_MAX_COMMIT_GDN_LAYERS || n_attn > DFLV_MAX_COMMIT_ATTN_LAYERS)
         return DFLV_ERR_UNSUPPORTED;
-    if (!path || !path_len || !status_dev || !aligned4(path) || !aligned4(path_len))
+    if (!path || !path_len || !status_dev || !aligned4(path) || !aligned4(path_len) || !aligned4(status_dev))
         return DFLV_ERR_INVALID_ARG;
     dflv::CommitArgs a = {};
     a.n_gdn = n_gdn;

@@ -95,6 +95,29 @@ def test_accept_ties(dflv, orc):
     assert np.array_equal(best, rb) and nxt[0] == rn[0] == 7
 
 
+def test_accept_nan_logits(dflv, orc):
+    """A NaN logit counts as -inf on both sides: rows with NaN before, after
+    and instead of the maximum, an all-NaN row and a NaN/-inf row, at a
+    vocabulary that several CTAs of a row split."""
+    V = 151936
+    rng = np.random.default_rng(91)
+    parent = np.array([[-1, 0, 1, 2, 3, 4]], np.int32)
+    logits = synth.random_logits(rng, 1, 6, V)
+    logits[0, 0, rng.integers(0, V, 500)] = np.nan
+    logits[0, 0, 0] = np.nan
+    logits[0, 1] = np.nan
+    logits[0, 2] = -np.inf
+    logits[0, 2, ::3] = np.nan
+    logits[0, 3, : V // 2] = np.nan
+    logits[0, 4, V // 2:] = np.nan
+    tokens = np.zeros((1, 6), np.int32)
+    path, plen, nxt, best = gpu_accept(dflv, logits, tokens, parent, np.array([6], np.int32))
+    rp, rl, rn, rb = orc.accept_greedy(logits, tokens, parent, np.array([6], np.int32))
+    assert np.array_equal(best, rb) and plen[0] == rl[0] and nxt[0] == rn[0]
+    assert np.array_equal(path[0, : rl[0]], rp[0, : rl[0]])
+    assert rb[0, 1] == 0 and rb[0, 2] == 0
+
+
 def gpu_commit(dflv, gdn_layers, attn_layers, path, path_len, n_past, dims, expect_status=0):
     """gdn_layers: list of dicts with device tensors state/u/g/kc; attn_layers:
     list of dicts with device planes."""

@@ -129,8 +129,9 @@ def test_attn_full_size_32k_q8_window(dflv, orc):
 
 
 @pytest.mark.parametrize("n", [8, 22, 64])
-def test_attn_long_context_q4_full_attention_sampled(dflv, orc, n):
-    # 8 sequences, 131,072-token q4_0 cache, full attention: sampled rows
+def test_attn_long_context_q4_full_attention(dflv, orc, n):
+    # 8 sequences, 131,072-token q4_0 cache, full attention: one whole
+    # sequence and sampled rows of others
     rng = np.random.default_rng(1239 + n)
     B, P, Hq, Hkv, D = 8, 131072, 24, 4, 256
     parents = [synth.ddtree(rng, n, 151936)[0] for _ in range(B)]
@@ -139,17 +140,24 @@ def test_attn_long_context_q4_full_attention_sampled(dflv, orc, n):
     cache = synth.kv_cache(rng, B, Hkv, P + 64, D, synth.KV_Q4_0)
     n_past = np.full(B, P, np.int32)
     out, planes = gpu_attn(dflv, parent, n_nodes, n_past, inp, cache, 0, synth.KV_Q4_0, Hq, Hkv, D)
-    rows = []
+    # every row of one whole sequence (all nodes x all query heads: every row
+    # tile, KV head and key split of that sequence's launch blocks), plus
+    # sampled rows of three other sequences
+    full_b = {8: 5, 22: 2, 64: 6}[n]
+    rows = list(range(full_b * n * Hq, (full_b + 1) * n * Hq))
+    sampled = []
     for b in (0, 3, 7):
         for i in (0, n - 1, int(rng.integers(0, n))):
-            rows.append((b * n + i) * Hq + int(rng.integers(0, Hq)))
-    rows = np.unique(np.asarray(rows, np.int32))
+            sampled.append((b * n + i) * Hq + int(rng.integers(0, Hq)))
+    sampled = np.unique(np.asarray(sampled, np.int32))
+    rows = np.unique(np.concatenate([np.asarray(rows, np.int32), sampled]))
     ref_cache = synth.copy_cache(cache)
     ref = orc.tree_attn_verify(parent, n_nodes, n_past, inp["q"], inp["k_new"], inp["v_new"], ref_cache, 0,
                                synth.KV_Q4_0, rows=rows)
     flat_o, flat_r = out.reshape(-1, D), ref.reshape(-1, D)
+    assert_close(out[full_b], ref[full_b], what=f"every row of sequence {full_b}")
     # the tolerance's rms is taken over the sampled rows
-    assert_close(flat_o[rows], flat_r[rows], what="sampled rows")
+    assert_close(flat_o[sampled], flat_r[sampled], what="sampled rows")
     for key in ("kq", "vq", "ks", "vs"):
         sl = np.s_[:, :, P:P + n]
         assert np.array_equal(planes[key][sl], ref_cache[key][sl]), key

@@ -63,6 +63,26 @@ def test_ties_go_to_lowest_vocab_index_and_lowest_node(orc):
     assert nxt[0] == 0
 
 
+def test_nan_logits_count_as_minus_infinity(orc):
+    # A NaN logit never wins unless nothing else can: row 0 has a NaN first
+    # and its maximum later, row 1 is all NaN (index 0), row 2 mixes NaN and
+    # -inf only (index 0, the lowest of the equal -inf values), row 3 has a
+    # NaN after its maximum.  Compared with numpy's argmax after the same
+    # substitution, which is an independent statement of the rule.
+    V = 9
+    par = np.array([-1, 0, 1, 2], np.int32)
+    tokens = np.array([[0, 99, 99, 99]], np.int32)
+    logits = np.zeros((1, 4, V), np.float32)
+    logits[0, 0] = [np.nan, 1.0, 3.0, np.nan, 2.0, 3.0, -1.0, 0.0, np.nan]
+    logits[0, 1] = np.nan
+    logits[0, 2] = [np.nan, -np.inf, np.nan, -np.inf, np.nan, np.nan, -np.inf, np.nan, np.nan]
+    logits[0, 3] = [0.5, 4.0, np.nan, 1.0, 2.0, np.nan, 0.0, 0.0, 0.0]
+    _, L, nxt, best = _accept(orc, logits, tokens, [par])
+    want = np.argmax(np.where(np.isnan(logits[0]), -np.inf, logits[0]), axis=1)
+    assert list(want) == [2, 0, 0, 1]
+    assert list(best[0]) == list(want) and L[0] == 1 and nxt[0] == 2
+
+
 @pytest.mark.parametrize("seed", range(6))
 def test_against_bruteforce_over_all_paths(orc, seed):
     # DDTree siblings carry distinct tokens, so at most one child can match
