@@ -95,10 +95,9 @@ struct TcLayout {
     static constexpr size_t off_rawK = off_Plo + kP;             // two buffers
     static constexpr size_t off_rawV = off_rawK + 2 * FK::kRaw;  // two buffers
     static constexpr size_t loop_total = off_rawV + 2 * FV::kRaw;
+    // merge: CS x ceil(RT / CS) <= kRows + 15 received partial rows
     static constexpr size_t off_Om = kHeader;
-    static constexpr size_t off_Mm = off_Om + (size_t)kRows * OS * 4;
-    static constexpr size_t off_Lm = off_Mm + (size_t)kRows * 4;
-    static constexpr size_t merge_total = off_Lm + (size_t)kRows * 4;
+    static constexpr size_t merge_total = off_Om + (size_t)(kRows + 16) * OS * 4;
     static constexpr size_t total = loop_total > merge_total ? loop_total : merge_total;
     static constexpr uint32_t kTmemCols = (D + 4 * kTK <= 256) ? 256 : 512;  // O, then two S buffers
 };
@@ -645,29 +644,38 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
     // the next kernel may be scheduled while the partials are merged
     grid_launch_dependents();
 
-    // ---- partial results -> shared memory (reusing the tile region)
-    float* Om = reinterpret_cast<float*>(smem + L::off_Om);
-    float* Mm = reinterpret_cast<float*>(smem + L::off_Mm);
-    float* Lm = reinterpret_cast<float*>(smem + L::off_Lm);
+    // ---- partial results to the CTA that finalises each row: rank q of the
+    //      cluster owns rows q, q + CS, ...  Every CTA first leaves its tile
+    //      loop (the receiving region reuses the tile buffers), then each
+    //      softmax thread stores its row's (O, max, sum) straight into the
+    //      owner's shared memory (posted stores: no round trip), and one more
+    //      cluster barrier publishes them.  Slot (s, q) of an owner holds the
+    //      partial of its s-th row from peer q: O in [0, D), max at D, sum at
+    //      D + 1.
+    float* Rcv = reinterpret_cast<float*>(smem + L::off_Om);
+    cluster_sync_all();
     if (warp < kSoftWarps) {
-        const int srow = tid;
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-        const bool have_o = T > 0 && !any_fail;
+        const int r = tid;
+        const bool valid = r < RT && row0 + r < rows_valid;
+        const int owner = valid ? r % CS : 0, slot = valid ? r / CS : 0;
+        const uint32_t dst = map_to_rank(smem_u32(Rcv + (size_t)(slot * CS + rank) * OS), (uint32_t)owner);
+        const bool have_o = T > 0 && !any_fail;  // uniform over the CTA
+        if (have_o) {
+            // the TMEM loads are warp-collective: every lane loads, only
+            // the lanes of valid rows store
+            const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
 #pragma unroll 1
-        for (int c0o = 0; c0o < D; c0o += 32) {
-            float o[32];
-            if (have_o) {
+            for (int c0o = 0; c0o < D; c0o += 32) {
+                float o[32];
                 tc::ld32(tmem_O + lane_off + c0o, o);
-            } else {
+                if (valid) {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) o[e] = 0.f;
+                    for (int e = 0; e < 32; e += 4)
+                        st_dsmem_f4(dst + (uint32_t)(c0o + e) * 4, o[e], o[e + 1], o[e + 2], o[e + 3]);
+                }
             }
-#pragma unroll
-            for (int e = 0; e < 32; e += 4)
-                *reinterpret_cast<float4*>(Om + srow * OS + c0o + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
         }
-        Mm[srow] = have_o ? m_run : -INFINITY;
-        Lm[srow] = have_o ? l_run : 0.f;
+        if (valid) st_dsmem_f2(dst + (uint32_t)D * 4, have_o ? m_run : -INFINITY, have_o ? l_run : 0.f);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -675,53 +683,34 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
         tc::fence_after_sync();
         tc::dealloc(tmem, L::kTmemCols);
     }
-    cluster_sync_all();
+    cluster_sync_all();  // every pushed partial is visible to its owner
 
-    // ---- merge: rank r finalises rows r, r + CS, ... (one warp per row); a
-    //      row's peer values are all requested before any is used
-    const uint32_t om_base = smem_u32(Om), mm_base = smem_u32(Mm), lm_base = smem_u32(Lm);
+    // ---- merge the owned rows from local shared memory, one warp per row
     constexpr int nwarps = kThreads / 32;
     constexpr int PL = D / 32;  // output floats per lane
-    for (int r = rank + CS * warp; r < RT; r += CS * nwarps) {
-        const int rho = row0 + r;
+    for (int slot = warp; rank + slot * CS < RT; slot += nwarps) {
+        const int r = rank + slot * CS, rho = row0 + r;
         if (rho >= rows_valid) continue;
-        // every peer's running max and sum, requested together (CS <= 16)
-        float mq16[16], lq16[16];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-            mq16[q] = q < CS ? ld_dsmem_f32(map_to_rank(mm_base + r * 4, q)) : -INFINITY;
-            lq16[q] = q < CS ? ld_dsmem_f32(map_to_rank(lm_base + r * 4, q)) : 0.f;
-        }
+        const float* base = Rcv + (size_t)slot * CS * OS;
         float M = -INFINITY;
-#pragma unroll
-        for (int q = 0; q < 16; ++q) M = fmaxf(M, mq16[q]);
+        for (int q = 0; q < CS; ++q) M = fmaxf(M, base[q * OS + D]);
         const float bse = (M == -INFINITY) ? 0.f : M;
         float Lt = 0.f, acc[PL];
 #pragma unroll
         for (int e = 0; e < PL; ++e) acc[e] = 0.f;
-        for (int q0 = 0; q0 < CS; q0 += 8) {  // peers in batches of eight
-            float v[8][PL], mq[8], lq[8];
+        for (int q = 0; q < CS; ++q) {
+            const float mq = base[q * OS + D];
+            if (mq == -INFINITY) continue;  // a peer without keys for this row sent no O
+            const float w = exp2f(mq - bse);
+            Lt = fmaf(w, base[q * OS + D + 1], Lt);
+            const float* oq = base + q * OS + lane * PL;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const bool on = q0 + q < CS;
-                mq[q] = q0 == 0 ? mq16[q] : mq16[8 + q];
-                lq[q] = q0 == 0 ? lq16[q] : lq16[8 + q];
-#pragma unroll
-                for (int e = 0; e < PL; e += 4) {
-                    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (on) x = ld_dsmem_f4(map_to_rank(om_base + (r * OS + lane * PL + e) * 4, q0 + q));
-                    v[q][e] = x.x;
-                    v[q][e + 1] = x.y;
-                    v[q][e + 2] = x.z;
-                    v[q][e + 3] = x.w;
-                }
-            }
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float w = exp2f(mq[q] - bse);  // 0 for absent peers (mq = -inf)
-                Lt = fmaf(w, lq[q], Lt);
-#pragma unroll
-                for (int e = 0; e < PL; ++e) acc[e] = fmaf(w, v[q][e], acc[e]);
+            for (int e = 0; e < PL; e += 4) {
+                const float4 x = *reinterpret_cast<const float4*>(oq + e);
+                acc[e] = fmaf(w, x.x, acc[e]);
+                acc[e + 1] = fmaf(w, x.y, acc[e + 1]);
+                acc[e + 2] = fmaf(w, x.z, acc[e + 2]);
+                acc[e + 3] = fmaf(w, x.w, acc[e + 3]);
             }
         }
         const float inv = 1.f / Lt;
@@ -731,7 +720,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
         for (int e = 0; e < PL; e += 4)
             *reinterpret_cast<float4*>(dst + e) = make_float4(acc[e] * inv, acc[e + 1] * inv, acc[e + 2] * inv, acc[e + 3] * inv);
     }
-    cluster_sync_all();  // peers may still be reading this CTA's shared memory
 }
 
 // How many clusters of cs CTAs of this kernel can be resident at once at

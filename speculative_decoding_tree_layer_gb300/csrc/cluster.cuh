@@ -57,5 +57,13 @@ DFLV_DEVINL float4 ld_dsmem_f4(uint32_t addr) {
 DFLV_DEVINL void st_dsmem_f2(uint32_t addr, float x, float y) {
     asm volatile("st.shared::cluster.v2.f32 [%0], {%1,%2};\n" ::"r"(addr), "f"(x), "f"(y) : "memory");
 }
+DFLV_DEVINL void st_dsmem_u4(uint32_t addr, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(addr), "r"(x), "r"(y), "r"(z), "r"(w)
+                 : "memory");
+}
+DFLV_DEVINL void st_dsmem_f4(uint32_t addr, float x, float y, float z, float w) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1,%2,%3,%4};\n" ::"r"(addr), "f"(x), "f"(y), "f"(z), "f"(w)
+                 : "memory");
+}
 
 }  // namespace dflv
