@@ -20,16 +20,18 @@
 //     to a tree tile first quantises the tree's rows into the cache;
 //   * stage warps (4): each raw tile is expanded into fp16 hi + lo tiles
 //     with the block scale folded in (d * code is exact in fp32; hi =
-//     fp16(x), lo = fp16(x - hi)).  K tiles are double-buffered;
+//     fp16(x), lo = fp16(x - hi)).  K and V tiles are double-buffered;
 //   * the MMA warp (1) issues tcgen05.mma: [S_hi | S_lo] = Q [K_hi ; K_lo]^T
 //     into one of two S buffers in tensor memory (M = 128, N = 64, K = head
-//     size), so the next tile's scores are formed while the softmax works on
-//     this one, and O += P_hi V_hi + P_hi V_lo + P_lo V_hi with O resident in
-//     tensor memory;
-//   * softmax warps (4): one thread per query row (its TMEM lane) reads the
-//     32 scores, applies the tree / window mask and an fp32 online softmax
-//     with a lazily updated running max (O is rescaled in tensor memory only
-//     when a row's max grows by more than 2^8), and writes P as fp16 hi + lo.
+//     size), and O += P_hi V_hi + P_hi V_lo + P_lo V_hi with O resident in
+//     tensor memory.  Q and P are read from tensor memory, so the tensor
+//     core's shared-memory reads are only the K and V tiles;
+//   * softmax warps (4): one thread per query row (its TMEM lane) writes the
+//     row's query into tensor memory once, then per tile reads the 32
+//     scores, applies the tree / window mask and an fp32 online softmax with
+//     a lazily updated running max (O is rescaled in tensor memory only when
+//     a row's max grows by more than 2^8), and writes P as fp16 hi + lo over
+//     the scores it has read.
 // Partial (max, sum, O) are merged across the cluster through distributed
 // shared memory.  Operands use the no-swizzle core-matrix layout described
 // in tcgen05.cuh.
@@ -82,30 +84,28 @@ struct TcLayout {
     static constexpr int NB = D / 32;
     static constexpr int OS = D + 4;                                  // merge row stride (floats)
     static constexpr size_t kHeader = 2048;   // tree arrays, barriers, flags
-    static constexpr size_t kQ = (size_t)kRows * D * 2;
     static constexpr size_t kK = (size_t)2 * kTK * D * 2;    // K_hi rows 0-31, K_lo rows 32-63
     static constexpr size_t kV = (size_t)kTK * D * 2;        // one of V_hi, V_lo
-    static constexpr size_t kP = (size_t)kRows * kTK * 2;    // one of P_hi, P_lo
-    static constexpr size_t off_Q = kHeader;
-    static constexpr size_t off_K = off_Q + kQ;              // two buffers
-    static constexpr size_t off_Vhi = off_K + 2 * kK;
-    static constexpr size_t off_Vlo = off_Vhi + kV;
-    static constexpr size_t off_Phi = off_Vlo + kV;
-    static constexpr size_t off_Plo = off_Phi + kP;
-    static constexpr size_t off_rawK = off_Plo + kP;             // two buffers
+    static constexpr size_t off_K = kHeader;                 // two buffers
+    static constexpr size_t off_V = off_K + 2 * kK;          // two buffers of V_hi then V_lo
+    static constexpr size_t off_rawK = off_V + 4 * kV;           // two buffers
     static constexpr size_t off_rawV = off_rawK + 2 * FK::kRaw;  // two buffers
     static constexpr size_t loop_total = off_rawV + 2 * FV::kRaw;
     // merge: CS x ceil(RT / CS) <= kRows + 15 received partial rows
     static constexpr size_t off_Om = kHeader;
     static constexpr size_t merge_total = off_Om + (size_t)(kRows + 16) * OS * 4;
     static constexpr size_t total = loop_total > merge_total ? loop_total : merge_total;
-    static constexpr uint32_t kTmemCols = (D + 4 * kTK <= 256) ? 256 : 512;  // O, then two S buffers
+    // tensor memory: O in columns [0, D), two S / P buffers of 2 kTK columns
+    // at kScol, Q (fp16 pairs) in D / 2 columns at kQcol
+    static constexpr uint32_t kScol = D, kQcol = D + 4 * kTK;
+    static constexpr uint32_t kTmemCols = (kQcol + D / 2 <= 256) ? 256 : 512;
+    static_assert(kQcol + D / 2 <= 512, "O, the S buffers and Q fit in tensor memory");
 };
 
 // header offsets
-constexpr int kHdrDepth = 256, kHdrMask = 512, kHdrBar = 1024, kHdrSlot = 1152, kHdrFail = 1156;
-enum Bar { kRawK0, kRawK1, kRawV0, kRawV1, kKFree0, kKFree1, kVFree0, kVFree1, kKReady0, kKReady1, kVReady,
-           kSFull0, kSFull1, kPReady, kODone, kMmaFin, kNumBars };
+constexpr int kHdrDepth = 256, kHdrMask = 512, kHdrBar = 1024, kHdrSlot = 1280, kHdrFail = 1284;
+enum Bar { kRawK0, kRawK1, kRawV0, kRawV1, kKFree0, kKFree1, kVFree0, kVFree1, kKReady0, kKReady1, kVReady0,
+           kVReady1, kSFull0, kSFull1, kPReady0, kPReady1, kODone0, kODone1, kMmaFin, kNumBars };
 static_assert(kHdrBar + kNumBars * 8 <= kHdrSlot, "barriers fit below the TMEM slot");
 
 DFLV_DEVINL bool wait_phase(uint64_t* bar, uint32_t parity) {
@@ -251,7 +251,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kHdrSlot);
     int32_t* fail_s = reinterpret_cast<int32_t*>(smem + kHdrFail);
     auto failed = [&]() { return *reinterpret_cast<volatile int32_t*>(fail_s) != 0; };
-    unsigned char* Q_s = smem + L::off_Q;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rank = (int)cluster_ctarank();
@@ -306,8 +305,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
 
     if (tid == 0) {
         for (int i = 0; i < kNumBars; ++i) {
-            const bool by_stagers = (i >= kKFree0 && i <= kVFree1) || i == kKReady0 || i == kKReady1 || i == kVReady;
-            const int count = i <= kRawV1 ? 32 : by_stagers ? kStageThreads : (i == kPReady ? kSoftWarps * 32 : 1);
+            const bool by_stagers = i >= kKFree0 && i <= kVReady1;
+            const bool by_softmax = i == kPReady0 || i == kPReady1;
+            const int count = i <= kRawV1 ? 32 : by_stagers ? kStageThreads : by_softmax ? kSoftWarps * 32 : 1;
             mbar_init(bars + i, count);
         }
         fence_mbar_init();
@@ -346,39 +346,33 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
     const int pt = warp < kSoftWarps ? tid : tid - kStageThreads;  // index among the other warps
     if (early && !stage_warp) grid_dependency_wait();
 
-    // ---- Q rows -> fp16, core-matrix layout (rows past the tile are zero);
-    //      every load of a thread is issued before the first is used
-    if (!stage_warp) {
-        constexpr int C8 = D / 8;
-        constexpr int PER = (kRows * C8 + kPrepThreads - 1) / kPrepThreads;
-        uint4 inq[PER];
+    // ---- Q rows -> fp16 pairs in tensor memory: softmax thread r writes row
+    //      r into its own lane (rows past the tile are zero); every load of a
+    //      thread is issued before the first is used
+    if (warp < kSoftWarps) {
+        const int r = tid, rho = row0 + r;
+        const bool on = r < RT && rho < rows_valid;
+        const uint4* src = on ? reinterpret_cast<const uint4*>(a.q + (((size_t)b * N + rho / G) * a.Hq + kvh * G + rho % G) * D)
+                              : nullptr;
+        constexpr int C8 = D / 8;  // 16-byte chunks of a row
+        uint4 w[C8];
 #pragma unroll
-        for (int j = 0; j < PER; ++j) {
-            const int idx = pt + j * kPrepThreads;
-            const int r = (idx & 7) + (idx / (8 * C8)) * 8;
-            const int d8 = (idx >> 3) % C8;
-            const int rho = row0 + r;
-            inq[j] = make_uint4(0, 0, 0, 0);
-            if (idx < kRows * C8 && r < RT && rho < rows_valid) {
-                const int i = rho / G, gh = rho % G;
-                inq[j] = __ldg(reinterpret_cast<const uint4*>(a.q + (((size_t)b * N + i) * a.Hq + kvh * G + gh) * D +
-                                                             d8 * 8));
+        for (int j = 0; j < C8; ++j) w[j] = on ? __ldg(src + j) : make_uint4(0, 0, 0, 0);
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+#pragma unroll
+        for (int c = 0; c < C8; c += 8) {  // 64 dims = 32 columns per store
+            uint32_t v[32];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t x[4] = {w[c + j].x, w[c + j].y, w[c + j].z, w[c + j].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    v[4 * j + e] = pack_f16x2(bf16_bits_to_float((uint16_t)(x[e] & 0xffff)),
+                                              bf16_bits_to_float((uint16_t)(x[e] >> 16)));
             }
+            tc::st32u(tmem + lane_off + L::kQcol + (uint32_t)(c * 4), v);
         }
-#pragma unroll
-        for (int j = 0; j < PER; ++j) {
-            const int idx = pt + j * kPrepThreads;
-            if (idx >= kRows * C8) break;
-            const int r = (idx & 7) + (idx / (8 * C8)) * 8;
-            const int d8 = (idx >> 3) % C8;
-            const uint32_t w[4] = {inq[j].x, inq[j].y, inq[j].z, inq[j].w};
-            uint32_t o[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                o[e] = pack_f16x2(bf16_bits_to_float((uint16_t)(w[e] & 0xffff)),
-                                  bf16_bits_to_float((uint16_t)(w[e] >> 16)));
-            *reinterpret_cast<uint4*>(Q_s + tc::cm_offset(r, d8 * 8, D)) = make_uint4(o[0], o[1], o[2], o[3]);
-        }
+        tc::fence_before_sync();
     }
     // ---- the tree's own keys and values: the CTA that attends to a tree
     //      tile quantises that tile's rows into the cache itself (every row
@@ -403,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
         named_barrier_sync_n(kPrepBarrier, kPrepThreads);
     }
 
-    const uint32_t tmem_O = tmem;  // columns [0, D); S buffers at D and D + 64
+    const uint32_t tmem_O = tmem;  // columns [0, D)
     float m_run = -INFINITY, l_run = 0.f;
 
     if (warp < kSoftWarps) {
@@ -422,20 +416,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
         }
         const float sl2 = a.scale * kLog2e;
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-        unsigned char* Phi = smem + L::off_Phi;
-        unsigned char* Plo = smem + L::off_Plo;
         // a warp whose rows are all padding only keeps the barrier phases
         // in step (its P rows and O rows are never read back)
         const bool warp_active = 32 * warp < min(RT, rows_valid - row0);
         for (int t = 0; t < T && !warp_active; ++t) {
-            if (t > 0) {
-                const bool ok = __all_sync(0xffffffffu, wait_phase(bars + kODone, (t - 1) & 1));
-                if (!ok) {
-                    if (lane == 0) atomicOr(fail_s, 1);
-                    break;
-                }
+            const bool ok = __all_sync(0xffffffffu, wait_phase(bars + kSFull0 + (t & 1), (t >> 1) & 1));
+            if (!ok) {
+                if (lane == 0) atomicOr(fail_s, 1);
+                break;
             }
-            mbar_arrive(bars + kPReady);
+            mbar_arrive(bars + kPReady0 + (t & 1));
         }
         for (int t = 0; t < T && warp_active; ++t) {
             const TileInfo ti = tile(t);
@@ -447,9 +437,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
             }
             tc::fence_after_sync();
             float s[kTK];
+            const uint32_t ts = tmem + L::kScol + (uint32_t)((t & 1) * 2 * kTK);  // this tile's S / P buffer
             {
                 float sh[32], sl[32];
-                const uint32_t ts = tmem + D + (uint32_t)((t & 1) * 2 * kTK);
                 tc::ld32(ts + lane_off, sh);
                 tc::ld32(ts + lane_off + kTK, sl);
 #pragma unroll
@@ -482,17 +472,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
                 l_run *= alpha;
                 rescale = t > 0;
             }
-            // P and O are free once the previous tile's PV has completed
-            if (t > 0) {
-                bool ok2 = wait_phase(bars + kODone, (t - 1) & 1);
-                ok2 = __all_sync(0xffffffffu, ok2);
+            if (__any_sync(0xffffffffu, rescale)) {
+                // every product into O so far has completed before O is rescaled
+                bool ok2 = __all_sync(0xffffffffu, wait_phase(bars + kODone0 + ((t - 1) & 1), ((t - 1) >> 1) & 1));
                 if (!ok2) {
                     if (lane == 0) atomicOr(fail_s, 1);
                     break;
                 }
                 tc::fence_after_sync();
-            }
-            if (__any_sync(0xffffffffu, rescale)) {
                 const float al = rescale ? alpha : 1.f;
 #pragma unroll 1
                 for (int c0o = 0; c0o < D; c0o += 32) {
@@ -517,19 +504,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
                 pl[j / 2] = *reinterpret_cast<const uint32_t*>(&l2);
             }
             l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-#pragma unroll
-            for (int k8 = 0; k8 < kTK / 8; ++k8) {
-                const uint32_t off = tc::cm_offset(srow, k8 * 8, kTK);
-                *reinterpret_cast<uint4*>(Phi + off) = make_uint4(ph[4 * k8], ph[4 * k8 + 1], ph[4 * k8 + 2], ph[4 * k8 + 3]);
-                *reinterpret_cast<uint4*>(Plo + off) = make_uint4(pl[4 * k8], pl[4 * k8 + 1], pl[4 * k8 + 2], pl[4 * k8 + 3]);
-            }
-            fence_proxy_async_smem();
+            // P over the scores just read: P_hi in the buffer's columns
+            // [0, kTK/2), P_lo in [kTK/2, kTK)
+            tc::st16u(ts + lane_off, ph);
+            tc::st16u(ts + lane_off + kTK / 2, pl);
             tc::fence_before_sync();
-            mbar_arrive(bars + kPReady);
+            mbar_arrive(bars + kPReady0 + (t & 1));
         }
         // the last PV
         if (__all_sync(0xffffffffu, T > 0 && !failed())) {
-            bool ok = __all_sync(0xffffffffu, wait_phase(bars + kODone, (T - 1) & 1));
+            bool ok = __all_sync(0xffffffffu, wait_phase(bars + kODone0 + ((T - 1) & 1), ((T - 1) >> 1) & 1));
             if (!ok && lane == 0) atomicOr(fail_s, 1);
             tc::fence_after_sync();
         }
@@ -557,13 +541,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
                 uint8_t* rv = rawV + (u & 1) * FV::kRaw;
                 ok = ok && wait_phase(bars + kRawV0 + (u & 1), (u >> 1) & 1);
                 const int shift = scale_shift<D, VT>(a.vs, plane_row0, tu.start);
-                if (u >= 1) ok = ok && wait_phase(bars + kODone, (u - 1) & 1);
+                // the products of tile u - 2 that read this V buffer have completed
+                if (u >= 2) ok = ok && wait_phase(bars + kODone0 + (u & 1), ((u - 2) >> 1) & 1);
+                unsigned char* vb = smem + L::off_V + (u & 1) * 2 * L::kV;
                 if (ok)
                     stage_hilo<D, VT>(rv, reinterpret_cast<const uint16_t*>(rv + FV::kRawCodes + shift), tu.count,
-                                        smem + L::off_Vhi, smem + L::off_Vlo, st);
+                                        vb, vb + L::kV, st);
                 mbar_arrive(bars + kVFree0 + (u & 1));  // raw V buffer of this parity released
                 fence_proxy_async_smem();
-                mbar_arrive(bars + kVReady);
+                mbar_arrive(bars + kVReady0 + (u & 1));
             }
             // a failure is seen by every stage thread at the same iteration
             const bool bad = named_barrier_or(kStageBarrier, kStageThreads, !ok || failed());
@@ -587,51 +573,56 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
         cp_async_wait<0>();  // this lane's copies have landed before the CTA moves on
     } else if (lane == 0) {
         // ================================================ MMA issue (one thread)
-        const uint32_t qa = smem_u32(Q_s);
         constexpr uint32_t SBO = (D / 8) * 128;
         constexpr uint32_t idesc_qk = tc::idesc_f16(kRows, 2 * kTK, false);  // K_lo follows K_hi
         constexpr uint32_t idesc_pv = tc::idesc_f16(kRows, D, true);
-        constexpr uint32_t P_SBO = (kTK / 8) * 128, V_LBO = (D / 8) * 128;
+        constexpr uint32_t V_LBO = (D / 8) * 128;
+        // [S_hi | S_lo] of tile t = Q (tensor memory) [K_hi ; K_lo]^T
         auto issue_qk = [&](int t) {
             const uint32_t kb = smem_u32(smem + L::off_K + (t & 1) * L::kK);
-            const uint32_t ts = tmem + D + (uint32_t)((t & 1) * 2 * kTK);
+            const uint32_t ts = tmem + L::kScol + (uint32_t)((t & 1) * 2 * kTK);
 #pragma unroll 4
             for (int ks = 0; ks < D / 16; ++ks)
-                tc::mma_f16(ts, tc::smem_desc(qa + ks * 256, 128, SBO), tc::smem_desc(kb + ks * 256, 128, SBO),
-                            idesc_qk, ks > 0);
+                tc::mma_f16_ts(ts, tmem + L::kQcol + (uint32_t)(ks * 8), tc::smem_desc(kb + ks * 256, 128, SBO),
+                               idesc_qk, ks > 0);
             tc::commit(bars + kSFull0 + (t & 1));
         };
         bool ok = true;
-        if (T > 0) {
-            ok = wait_phase(bars + kKReady0, 0);
+        for (int t = 0; t < min(T, 2) && ok; ++t) {
+            ok = wait_phase(bars + kKReady0 + t, 0);
             if (ok) {
                 tc::fence_after_sync();
-                issue_qk(0);
+                issue_qk(t);
             }
         }
         for (int t = 0; t < T && ok; ++t) {
-            if (t + 1 < T) {
-                ok = wait_phase(bars + kKReady0 + ((t + 1) & 1), ((t + 1) >> 1) & 1);
-                if (!ok) break;
-                tc::fence_after_sync();
-                issue_qk(t + 1);
-            }
-            ok = wait_phase(bars + kPReady, t & 1) && wait_phase(bars + kVReady, t & 1);
+            ok = wait_phase(bars + kPReady0 + (t & 1), (t >> 1) & 1) &&
+                 wait_phase(bars + kVReady0 + (t & 1), (t >> 1) & 1);
             if (!ok) break;
             tc::fence_after_sync();
-            const uint32_t ph = smem_u32(smem + L::off_Phi), pl = smem_u32(smem + L::off_Plo);
-            const uint32_t vh = smem_u32(smem + L::off_Vhi), vl = smem_u32(smem + L::off_Vlo);
+            // O += P_hi V_hi + P_hi V_lo + P_lo V_hi, P (tensor memory) over
+            // this tile's S buffer: P_hi in its columns [0, kTK/2), P_lo after
+            const uint32_t ps = tmem + L::kScol + (uint32_t)((t & 1) * 2 * kTK);
+            const uint32_t vh = smem_u32(smem + L::off_V + (t & 1) * 2 * L::kV), vl = vh + (uint32_t)L::kV;
 #pragma unroll
             for (int ks = 0; ks < kTK / 16; ++ks) {
-                const uint64_t ah = tc::smem_desc(ph + ks * 256, 128, P_SBO);
-                const uint64_t al = tc::smem_desc(pl + ks * 256, 128, P_SBO);
                 const uint64_t bh = tc::smem_desc(vh + ks * 2 * V_LBO, V_LBO, 128);
                 const uint64_t bl = tc::smem_desc(vl + ks * 2 * V_LBO, V_LBO, 128);
-                tc::mma_f16(tmem_O, ah, bh, idesc_pv, t > 0 || ks > 0);
-                tc::mma_f16(tmem_O, ah, bl, idesc_pv, true);
-                tc::mma_f16(tmem_O, al, bh, idesc_pv, true);
+                const uint32_t ah = ps + (uint32_t)(ks * 8), al = ps + (uint32_t)(kTK / 2 + ks * 8);
+                tc::mma_f16_ts(tmem_O, ah, bh, idesc_pv, t > 0 || ks > 0);
+                tc::mma_f16_ts(tmem_O, ah, bl, idesc_pv, true);
+                tc::mma_f16_ts(tmem_O, al, bh, idesc_pv, true);
             }
-            tc::commit(bars + kODone);
+            tc::commit(bars + kODone0 + (t & 1));
+            // the scores of tile t + 2 go into this buffer once these
+            // products (which read P from it) have completed
+            if (t + 2 < T) {
+                ok = wait_phase(bars + kKReady0 + (t & 1), ((t + 2) >> 1) & 1) &&
+                     wait_phase(bars + kODone0 + (t & 1), (t >> 1) & 1);
+                if (!ok) break;
+                tc::fence_after_sync();
+                issue_qk(t + 2);
+            }
         }
         if (!ok) atomicOr(fail_s, 1);
         // every MMA issued above has completed before TMEM or smem is reused
