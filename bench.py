@@ -313,6 +313,10 @@ class GpuStep:
                                         1.0 / np.sqrt(ATT["D"]))
         self.attn_desc_next = dflv.attn_desc(1, N, ATT["Hq"], ATT["Hkv"], ATT["D"], cap, WINDOW, dflv.DFLV_KV_Q8_0,
                                              1.0 / np.sqrt(ATT["D"]), early)
+        # one merge workspace for every attention layer (the calls are
+        # ordered on one stream)
+        self.attn_ws_bytes = dflv.dflv_attn_workspace_size(self.attn_desc)
+        self.attn_ws = t.empty(max(self.attn_ws_bytes, 16), dtype=t.uint8, device=dev)
         self.layers = []
         self.states, self.factors, self.caches = [], [], []
         self.state0 = []
@@ -377,15 +381,18 @@ class GpuStep:
             L["beta"], L["log_alpha"], L["state"], L["fac"][1 - par], self.path, self.path_len, L["out"],
             L["fac"][par], self.status)
 
+    def attn_verify(self, L, desc=None):
+        return self.dflv.dflv_tree_attn_verify(desc or self.attn_desc_next, self.parent, self.n_nodes, self.n_past,
+                                               L["q"], L["k_new"], L["v_new"], L["kv"], L["out"], self.status,
+                                               self.attn_ws, self.attn_ws_bytes)
+
     def step(self, par):
         dflv, chk = self.dflv, self.dflv.check
         for li, L in enumerate(self.layers):
             if L["kind"] == "gdn":
                 chk(self.gdn_verify(li, L, par), "gdn verify")
             else:
-                chk(dflv.dflv_tree_attn_verify(self.attn_desc_next, self.parent, self.n_nodes, self.n_past, L["q"],
-                                               L["k_new"], L["v_new"], L["kv"], L["out"], self.status),
-                    "attn verify")
+                chk(self.attn_verify(L), "attn verify")
         chk(dflv.dflv_accept_greedy(1, BUDGET, VOCAB, self.logits, self.tokens, self.parent, self.n_nodes,
                                     self.path, self.path_len, self.next_token, self.best, self.status), "accept")
         chk(dflv.dflv_commit_rollback(None, 0, [], [], self.attn_desc, len(self.caches), self.caches, self.path,
@@ -468,8 +475,7 @@ def kernel_chain_ms(S, torch, stream, steps, warmup, flush):
     def attn_chain():
         for L in S.layers:
             if L["kind"] == "attn":
-                chk(dflv.dflv_tree_attn_verify(S.attn_desc_next, S.parent, S.n_nodes, S.n_past, L["q"],
-                                               L["k_new"], L["v_new"], L["kv"], L["out"], S.status), "attn verify")
+                chk(S.attn_verify(L), "attn verify")
 
     def accept():
         chk(dflv.dflv_accept_greedy(1, BUDGET, VOCAB, S.logits, S.tokens, S.parent, S.n_nodes, S.path,
@@ -628,8 +634,10 @@ def scale_measure(torch, dflv, flush, reps=8, rounds=10):
     kv = dflv.kv_layer(kq, vq, ks, vs)
     descs = [dflv.attn_desc(B, N, Hq, Hkv, D, cap, 0, dflv.DFLV_KV_Q4_0, 1.0 / np.sqrt(D), f)
              for f in (0, dflv.DFLV_FLAG_EARLY_PREFETCH)]
+    wsb = dflv.dflv_attn_workspace_size(descs[0])
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
     ms = timed(lambda r: dflv.check(dflv.dflv_tree_attn_verify(descs[r > 0], par_d, nn_d, n_past, q, kn, vn, kv, o,
-                                                             status)))
+                                                             status, ws, wsb)))
     byt, flops = scale_bytes_attn(), scale_flops_attn()
     tpk, tkind = bf16_peak()
     tf = flops / (ms * 1e-3) / 1e12
@@ -975,8 +983,7 @@ def profile_one(kind, launches):
         if kind == "gdn":
             dflv.check(S.gdn_verify(li, L, 0))
         elif kind == "attn":
-            dflv.check(dflv.dflv_tree_attn_verify(S.attn_desc, S.parent, S.n_nodes, S.n_past, L["q"], L["k_new"],
-                                                  L["v_new"], L["kv"], L["out"], S.status))
+            dflv.check(S.attn_verify(L, S.attn_desc))
         elif kind == "accept":
             dflv.check(dflv.dflv_accept_greedy(1, BUDGET, VOCAB, S.logits, S.tokens, S.parent, S.n_nodes, S.path,
                                                S.path_len, S.next_token, S.best, S.status))

@@ -334,7 +334,14 @@ typedef struct {
  *          fp32 reciprocal of the fp32 d, clamped to [-127, 127] resp.
  *          [-8, 7] (+8); slots < P are only read)
  *   out    [B][N_max][Hq][D] f32
- *   workspace reserved: dflv_attn_workspace_size() returns 0; may be NULL
+ *   workspace, ws_bytes: optional device scratch (16-byte aligned).  With
+ *          at least dflv_attn_workspace_size(desc) bytes, the partial
+ *          results of the key splits are merged through it (global memory);
+ *          with less, or NULL, through the thread-block cluster's shared
+ *          memory, which is slower.  The results are the same either way.
+ *          Its contents on entry do not matter.  Calls on one stream may
+ *          share one workspace; calls that can run at the same time need
+ *          their own.
  * Every node attends to the cached positions j < P inside its window and to
  * the tree slots of its ancestors-or-self, reading the quantised values, so
  * a chain tree reproduces sequential decode. */
@@ -345,6 +352,10 @@ dflv_status dflv_tree_attn_verify(const dflv_attn_desc* desc, const int32_t* par
                                   int32_t* status_dev, void* workspace, size_t ws_bytes,
                                   dflv_stream_t stream);
 
+/* Bytes of workspace with which dflv_tree_attn_verify merges through global
+ * memory for this descriptor (0: the shape never uses one; also 0 for an
+ * invalid descriptor).  The launch plan behind it follows the current
+ * device, so query it with the device current that will run the calls. */
 size_t dflv_attn_workspace_size(const dflv_attn_desc* desc);
 
 /* ------------------------------------------------------------------------ */

@@ -123,7 +123,19 @@ const char* dflv_status_string(dflv_status s) {
 }
 
 size_t dflv_gdn_workspace_size(const dflv_gdn_desc*) { return 0; }
-size_t dflv_attn_workspace_size(const dflv_attn_desc*) { return 0; }
+size_t dflv_attn_workspace_size(const dflv_attn_desc* desc) {
+    if (check_attn_desc(desc) != DFLV_OK) return 0;
+    dflv::AttnVerifyArgs a = {};
+    a.B = desc->B;
+    a.N_max = desc->N_max;
+    a.Hq = desc->Hq;
+    a.Hkv = desc->Hkv;
+    a.D = desc->D;
+    a.cap = desc->cap;
+    a.window = desc->window;
+    a.type = desc->type;
+    return dflv::attn_workspace_bytes(a);
+}
 
 dflv_status dflv_tree_gdn_verify(const dflv_gdn_desc* desc, const int32_t* parent,
                                  const int32_t* n_nodes, const uint16_t* q, const uint16_t* k,
@@ -176,8 +188,6 @@ dflv_status dflv_tree_attn_verify(const dflv_attn_desc* desc, const int32_t* par
                                   const uint16_t* v_new, const dflv_kv_layer* cache, float* out,
                                   int32_t* status_dev, void* workspace, size_t ws_bytes,
                                   dflv_stream_t stream) {
-    (void)workspace;
-    (void)ws_bytes;
     dflv_status s = check_attn_desc(desc);
     if (s != DFLV_OK) return s;
     if (!parent || !n_nodes || !n_past || !q || !k_new || !v_new || !out || !status_dev)
@@ -185,9 +195,9 @@ dflv_status dflv_tree_attn_verify(const dflv_attn_desc* desc, const int32_t* par
     s = check_kv_layer(desc, cache);
     if (s != DFLV_OK) return s;
     if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(out) || !aligned4(parent) ||
-        !aligned4(n_nodes) || !aligned4(n_past) || !aligned4(status_dev))
+        !aligned4(n_nodes) || !aligned4(n_past) || !aligned4(status_dev) || (workspace && !aligned16(workspace)))
         return DFLV_ERR_INVALID_ARG;
-    dflv::AttnVerifyArgs a;
+    dflv::AttnVerifyArgs a = {};
     a.B = desc->B;
     a.N_max = desc->N_max;
     a.Hq = desc->Hq;
@@ -210,6 +220,8 @@ dflv_status dflv_tree_attn_verify(const dflv_attn_desc* desc, const int32_t* par
     a.vs = cache->vs;
     a.out = out;
     a.status = status_dev;
+    a.ws = workspace;
+    a.ws_bytes = workspace ? ws_bytes : 0;
     return from_cuda(dflv::launch_attn_tree_verify(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -623,6 +623,11 @@ cudaError_t launch_main(const AttnVerifyArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
+size_t attn_workspace_bytes(const AttnVerifyArgs& a) {
+    if (a.type == DFLV_KV_F32) return 0;
+    return (a.D == 128 || a.D == 256) ? attn_workspace_bytes_tc(a) : 0;
+}
+
 cudaError_t launch_attn_tree_verify(const AttnVerifyArgs& a, cudaStream_t stream) {
     if (a.type == DFLV_KV_F32) {
         cudaError_t e = launch_pdl(attn_store_tree_f32_kernel, dim3(a.N_max, a.Hkv, a.B), dim3(64), 0, stream, 1, a);

@@ -636,20 +636,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
     grid_launch_dependents();
 
     // ---- partial results to the CTA that finalises each row: rank q of the
-    //      cluster owns rows q, q + CS, ...  Every CTA first leaves its tile
-    //      loop (the receiving region reuses the tile buffers), then each
-    //      softmax thread stores its row's (O, max, sum) straight into the
-    //      owner's shared memory (posted stores: no round trip), and one more
-    //      cluster barrier publishes them.  Slot (s, q) of an owner holds the
-    //      partial of its s-th row from peer q: O in [0, D), max at D, sum at
-    //      D + 1.
+    //      cluster owns rows q, q + CS, ...  Each row's partial is (O, max,
+    //      sum), and one cluster barrier publishes them:
+    //      * with a workspace, through global memory: each CTA, as soon as
+    //        its loop ends, stages its rows' partials in its own shared
+    //        memory (slot r: O in [0, D), max at D, sum at D + 1) and writes
+    //        them to its block of the workspace with one bulk copy; the
+    //        owners read their rows' partials back from the L2;
+    //      * without one, into the owner's shared memory by posted cluster
+    //        stores, once every CTA has left its tile loop (the receiving
+    //        region reuses the tile buffers).  Slot (s, q) of an owner holds
+    //        peer q's partial of its s-th row.
     float* Rcv = reinterpret_cast<float*>(smem + L::off_Om);
-    cluster_sync_all();
+    const bool gmerge = a.ws != nullptr;  // uniform over the launch
+    float* wsb = gmerge ? reinterpret_cast<float*>(a.ws) +
+                              (((size_t)b * a.Hkv + kvh) * (gridDim.y / a.Hkv) + rt) * CS * RT * OS
+                        : nullptr;
+    const int rows_here = min(RT, rows_valid - row0);  // rows 0 .. rows_here-1 are valid
+    if (!gmerge) cluster_sync_all();
     if (warp < kSoftWarps) {
         const int r = tid;
-        const bool valid = r < RT && row0 + r < rows_valid;
+        const bool valid = r < rows_here;
         const int owner = valid ? r % CS : 0, slot = valid ? r / CS : 0;
-        const uint32_t dst = map_to_rank(smem_u32(Rcv + (size_t)(slot * CS + rank) * OS), (uint32_t)owner);
+        const uint32_t dst =
+            gmerge ? smem_u32(Rcv + (size_t)r * OS)
+                   : map_to_rank(smem_u32(Rcv + (size_t)(slot * CS + rank) * OS), (uint32_t)owner);
         const bool have_o = T > 0 && !any_fail;  // uniform over the CTA
         if (have_o) {
             // the TMEM loads are warp-collective: every lane loads, only
@@ -661,12 +672,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
                 tc::ld32(tmem_O + lane_off + c0o, o);
                 if (valid) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        st_dsmem_f4(dst + (uint32_t)(c0o + e) * 4, o[e], o[e + 1], o[e + 2], o[e + 3]);
+                    for (int e = 0; e < 32; e += 4) {
+                        if (gmerge)
+                            *reinterpret_cast<float4*>(Rcv + (size_t)r * OS + c0o + e) =
+                                make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+                        else
+                            st_dsmem_f4(dst + (uint32_t)(c0o + e) * 4, o[e], o[e + 1], o[e + 2], o[e + 3]);
+                    }
                 }
             }
         }
-        if (valid) st_dsmem_f2(dst + (uint32_t)D * 4, have_o ? m_run : -INFINITY, have_o ? l_run : 0.f);
+        if (valid) {
+            const float mv = have_o ? m_run : -INFINITY, lv = have_o ? l_run : 0.f;
+            if (gmerge) *reinterpret_cast<float2*>(Rcv + (size_t)r * OS + D) = make_float2(mv, lv);
+            else st_dsmem_f2(dst + (uint32_t)D * 4, mv, lv);
+        }
+        if (gmerge) fence_proxy_async_smem();  // the staged rows go out through the bulk-copy engine
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -674,21 +695,84 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
         tc::fence_after_sync();
         tc::dealloc(tmem, L::kTmemCols);
     }
-    cluster_sync_all();  // every pushed partial is visible to its owner
+    if (gmerge && tid == 0 && rows_here > 0) {
+        bulk_s2g(wsb + (size_t)rank * RT * OS, Rcv, (uint32_t)(rows_here * OS * 4));
+        bulk_s2g_wait();
+    }
+    cluster_sync_all();  // every partial is visible to its owner
 
-    // ---- merge the owned rows from local shared memory, one warp per row
+    // ---- merge the owned rows
     constexpr int nwarps = kThreads / 32;
-    constexpr int PL = D / 32;  // output floats per lane
+    constexpr int PL = D / 32;  // output floats per lane when a warp takes a whole row
+    if (gmerge) {
+        // an item is half of an owned row (D / 2 dims, D / 64 per lane);
+        // every peer's partial of it is requested at once (CS <= 16), then
+        // merged in peer order
+        constexpr int HL = D / 64;  // floats per lane
+        const int n_own = (rank < rows_here) ? (rows_here - 1 - rank) / CS + 1 : 0;
+        for (int item = warp; item < 2 * n_own; item += nwarps) {
+            const int slot = item >> 1, half = item & 1;
+            const int r = rank + slot * CS, rho = row0 + r;
+            const int c0 = half * (D / 2) + lane * HL;
+            float2 ml[16];
+            float ov[16][HL];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                ml[q] = make_float2(-INFINITY, 0.f);
+#pragma unroll
+                for (int e = 0; e < HL; ++e) ov[q][e] = 0.f;
+                if (q < CS) {
+                    const float* src = wsb + ((size_t)q * RT + r) * OS;
+                    ml[q] = __ldcg(reinterpret_cast<const float2*>(src + D));
+                    if constexpr (HL == 4) {
+                        const float4 x = __ldcg(reinterpret_cast<const float4*>(src + c0));
+                        ov[q][0] = x.x;
+                        ov[q][1] = x.y;
+                        ov[q][2] = x.z;
+                        ov[q][3] = x.w;
+                    } else {
+                        const float2 x = __ldcg(reinterpret_cast<const float2*>(src + c0));
+                        ov[q][0] = x.x;
+                        ov[q][1] = x.y;
+                    }
+                }
+            }
+            float M = -INFINITY;
+#pragma unroll
+            for (int q = 0; q < 16; ++q) M = fmaxf(M, ml[q].x);
+            const float bse = (M == -INFINITY) ? 0.f : M;
+            float Lt = 0.f, acc[HL];
+#pragma unroll
+            for (int e = 0; e < HL; ++e) acc[e] = 0.f;
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                // absent peers and peers without keys for this row: max -inf, weight 0
+                const float w = (ml[q].x == -INFINITY) ? 0.f : exp2f(ml[q].x - bse);
+                Lt = fmaf(w, ml[q].y, Lt);
+#pragma unroll
+                for (int e = 0; e < HL; ++e) acc[e] = (w == 0.f) ? acc[e] : fmaf(w, ov[q][e], acc[e]);
+            }
+            const float inv = 1.f / Lt;
+            const int i = rho / G, gh = rho % G;
+            float* dsto = a.out + (((size_t)b * N + i) * a.Hq + kvh * G + gh) * D + c0;
+            if constexpr (HL == 4)
+                *reinterpret_cast<float4*>(dsto) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+            else
+                *reinterpret_cast<float2*>(dsto) = make_float2(acc[0] * inv, acc[1] * inv);
+        }
+        return;
+    }
+    // one warp per row, from local shared memory
     for (int slot = warp; rank + slot * CS < RT; slot += nwarps) {
         const int r = rank + slot * CS, rho = row0 + r;
         if (rho >= rows_valid) continue;
+        float Lt = 0.f, acc[PL];
+#pragma unroll
+        for (int e = 0; e < PL; ++e) acc[e] = 0.f;
         const float* base = Rcv + (size_t)slot * CS * OS;
         float M = -INFINITY;
         for (int q = 0; q < CS; ++q) M = fmaxf(M, base[q * OS + D]);
         const float bse = (M == -INFINITY) ? 0.f : M;
-        float Lt = 0.f, acc[PL];
-#pragma unroll
-        for (int e = 0; e < PL; ++e) acc[e] = 0.f;
         for (int q = 0; q < CS; ++q) {
             const float mq = base[q * OS + D];
             if (mq == -INFINITY) continue;  // a peer without keys for this row sent no O
@@ -743,12 +827,14 @@ int active_clusters(int cs) {
     return cache[cs] > 0 ? cache[cs] : 0;
 }
 
+struct TcPlan {
+    int n_rt, RT, CS;
+};
+
+// Row tiles and cluster size of a launch (the device's cluster occupancy
+// enters, so the plan is per device).
 template <int D, int KT, int VT>
-cudaError_t launch_tc(const AttnVerifyArgs& a, cudaStream_t stream) {
-    using L = TcLayout<D, KT, VT>;
-    auto kern = attn_tc_kernel<D, KT, VT>;
-    cudaError_t e = ensure_smem(kern, L::total);
-    if (e != cudaSuccess) return e;
+TcPlan plan_tc(const AttnVerifyArgs& a) {
     const int rows = (a.Hq / a.Hkv) * a.N_max;
     const long range = (a.window > 0) ? (long)a.window - 1 : (long)a.cap;
     const long tiles = (range + kTK - 1) / kTK + 3;
@@ -795,8 +881,30 @@ cudaError_t launch_tc(const AttnVerifyArgs& a, cudaStream_t stream) {
             }
         }
     }
-    const int RT = (rows + n_rt - 1) / n_rt;
-    return launch_pdl(kern, dim3(cs, n_rt * a.Hkv, a.B), dim3(kThreads), L::total, stream, cs, a, RT, cs);
+    return TcPlan{n_rt, (rows + n_rt - 1) / n_rt, cs};
+}
+
+// Workspace of the global merge: one partial row (O, max, sum, two words
+// of padding) per (sequence, KV head, row tile, cluster rank, row).
+template <int D, int KT, int VT>
+size_t ws_bytes_tc(const AttnVerifyArgs& a) {
+    // the occupancy query behind the plan needs the kernel's shared-memory
+    // size granted first
+    if (ensure_smem(attn_tc_kernel<D, KT, VT>, TcLayout<D, KT, VT>::total) != cudaSuccess) return 0;
+    const TcPlan p = plan_tc<D, KT, VT>(a);
+    return (size_t)a.B * a.Hkv * p.n_rt * p.CS * p.RT * (D + 4) * sizeof(float);
+}
+
+template <int D, int KT, int VT>
+cudaError_t launch_tc(const AttnVerifyArgs& a, cudaStream_t stream) {
+    using L = TcLayout<D, KT, VT>;
+    auto kern = attn_tc_kernel<D, KT, VT>;
+    cudaError_t e = ensure_smem(kern, L::total);
+    if (e != cudaSuccess) return e;
+    const TcPlan p = plan_tc<D, KT, VT>(a);
+    AttnVerifyArgs b = a;
+    if (!b.ws || b.ws_bytes < (size_t)a.B * a.Hkv * p.n_rt * p.CS * p.RT * (D + 4) * sizeof(float)) b.ws = nullptr;
+    return launch_pdl(kern, dim3(p.CS, p.n_rt * a.Hkv, a.B), dim3(kThreads), L::total, stream, p.CS, b, p.RT, p.CS);
 }
 
 }  // namespace
@@ -818,6 +926,26 @@ cudaError_t launch_attn_tree_verify_tc(const AttnVerifyArgs& a, cudaStream_t str
         case 128: return launch_tc_d<128>(a, stream);
         case 256: return launch_tc_d<256>(a, stream);
         default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int D>
+size_t ws_bytes_tc_d(const AttnVerifyArgs& a) {
+    constexpr int Q8 = DFLV_KV_Q8_0, Q4 = DFLV_KV_Q4_0;
+    switch (a.type) {
+        case DFLV_KV_Q8_0: return ws_bytes_tc<D, Q8, Q8>(a);
+        case DFLV_KV_Q4_0: return ws_bytes_tc<D, Q4, Q4>(a);
+        case DFLV_KV_Q8_0_Q4_0: return ws_bytes_tc<D, Q8, Q4>(a);
+        case DFLV_KV_Q4_0_Q8_0: return ws_bytes_tc<D, Q4, Q8>(a);
+        default: return 0;
+    }
+}
+
+size_t attn_workspace_bytes_tc(const AttnVerifyArgs& a) {
+    switch (a.D) {
+        case 128: return ws_bytes_tc_d<128>(a);
+        case 256: return ws_bytes_tc_d<256>(a);
+        default: return 0;
     }
 }
 

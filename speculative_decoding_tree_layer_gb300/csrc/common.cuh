@@ -112,6 +112,21 @@ DFLV_DEVINL void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* 
         : "memory");
 }
 
+// One bulk (TMA engine) copy shared -> global; src, dst 16-byte aligned,
+// bytes a multiple of 16.  bulk_s2g_wait() then waits until every such copy
+// of this thread has written its data and orders those writes before this
+// thread's later generic accesses (and so before a later release).
+DFLV_DEVINL void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst), "r"(smem_u32(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+DFLV_DEVINL void bulk_s2g_wait() {
+    asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
+    asm volatile("fence.proxy.async.global;\n" ::: "memory");
+}
+
 DFLV_DEVINL bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(

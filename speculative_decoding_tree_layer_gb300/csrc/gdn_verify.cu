@@ -58,16 +58,21 @@ struct GdnSmemLayout {
         off_M = off_A + (size_t)NP * NP * 4;     // dense [NP][NP], zero off the ancestors-or-self
         off_R = off_M + (size_t)NP * NP * 4;     // [node][RB]: S_0 k, then u
         off_SQ = off_R + (size_t)NP * RB * 4;    // [node][RB]: S_0 q
-        off_PK = off_SQ + (size_t)NP * RB * 4;   // deferred commit: k of the pending path, [m][KS]
-        off_PU = off_PK + (size_t)NP * KS * 2;   // u of the pending path for this CTA's rows, [m][RB]
-        off_PC = off_PU + (size_t)NP * RB * 4;   // e^{g_e - g_{p_m}} per m, then e^{g_e}
-        total = off_PC + (size_t)(64 + 4) * 4;
+        off_PK = off_SQ + (size_t)NP * RB * 4;   // deferred commit: the previous step's k, [node][KS]
+        off_PU = off_PK + (size_t)NP * KS * 2;   // its u for this CTA's rows, [node][RB]
+        off_PC = off_PU + (size_t)NP * RB * 4;   // its g per node, then e^{g_e - g_{p_m}} per m, then e^{g_e}
+        total = off_PC + (size_t)(2 * 64 + 4) * 4;
     }
 };
 
-// barrier over the first `count` threads of the block (whole warps), id != 0
+// barrier over `count` threads of the block (whole warps), id != 0
 DFLV_DEVINL void named_barrier_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// the arriving half of such a barrier: does not wait (its writes before it
+// are visible to the threads that pass the matching bar.sync)
+DFLV_DEVINL void named_barrier_arrive(int id, int count) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // 4-5. [K ; Q] K^T on the tensor cores by the kHalfWarps warps of the first
@@ -80,8 +85,9 @@ DFLV_DEVINL void named_barrier_sync(int id, int count) {
 //    at once.  The MMA's k index is permuted consistently on both operands:
 //    thread tq of a quad holds columns 4tq .. 4tq+3 of each 16-wide k step,
 //    so one 8-byte load fills both halves of its fragment registers.  The
-//    cumulative decays g_s (written by the half before the call) are read
-//    only after the half's barrier, once the products are in registers.
+//    cumulative decays g_s (written by the other half, which arrives at
+//    barrier 1 when done) are read only after that barrier, once the
+//    products are in registers.
 template <int DK, int NPT>
 DFLV_DEVINL void gdn_gram_tiles(const uint16_t* K_s, const uint16_t* Q_s, float* A_s, float* M_s,
                                 const float* g_s, const float* beta_s, const uint64_t* amask_s, int n, int warp,
@@ -131,7 +137,7 @@ DFLV_DEVINL void gdn_gram_tiles(const uint16_t* K_s, const uint16_t* Q_s, float*
             mma_bf16_16816(d[t], af, bf);
         }
     }
-    named_barrier_sync(1, kGdnThreads / 2);  // g_s complete
+    named_barrier_sync(1, kGdnThreads);  // g_s complete (written by the other half)
 #pragma unroll
     for (int t = 0; t < TPW; ++t) {
 #pragma unroll
@@ -220,17 +226,18 @@ DFLV_DEVINL void gdn_state_products(const float* S_s, const uint16_t* K_s, const
 // Deferred commit, by the 128 threads of the second half (ht = 0..127):
 // S <- e^{g_e} S + sum_{m<PL} e^{g_e - g_{p_m}} u_{p_m} k_{p_m}^T on this CTA's
 // rows in shared memory, and the updated rows back to the state in HBM.
-// PC_s holds g_{p_m} on entry.
+// PK_s, PU_s and PC_s[0, 64) hold the previous step's k, u and g of every
+// node; p = path.
 template <int DK, int RB>
 DFLV_DEVINL void gdn_apply_pending(const GdnVerifyArgs& a, float* S_s, const uint16_t* PK_s, const float* PU_s,
-                                   float* PC_s, int PL, int b, int h, int r0, int ht) {
+                                   float* PC_s, const int32_t* path, int PL, int b, int h, int r0, int ht) {
     constexpr int KS = DK + 16;
-    const float ge = PC_s[PL - 1];  // g of the path's end node
-    named_barrier_sync(2, kGdnThreads / 2);  // every thread has read ge
-    if (ht < PL) PC_s[ht] = expf(ge - PC_s[ht]);
-    if (ht == 0) PC_s[kMaxNodes] = expf(ge);
+    float* PW_s = PC_s + kMaxNodes;  // e^{g_e - g_{p_m}} per m, then e^{g_e}
+    const float ge = PC_s[path[PL - 1]];  // g of the path's end node
+    if (ht < PL) PW_s[ht] = expf(ge - PC_s[path[ht]]);
+    if (ht == 0) PW_s[kMaxNodes] = expf(ge);
     named_barrier_sync(2, kGdnThreads / 2);
-    const float Ge = PC_s[kMaxNodes];
+    const float Ge = PW_s[kMaxNodes];
     float* dst = a.state_out + (((size_t)b * a.Hv + h) * a.dv + r0) * DK;
     for (int e4 = ht; e4 < RB * DK / 4; e4 += kGdnThreads / 2) {
         const int r = (e4 * 4) / DK, c = (e4 * 4) % DK;
@@ -240,8 +247,9 @@ DFLV_DEVINL void gdn_apply_pending(const GdnVerifyArgs& a, float* S_s, const uin
         x.z *= Ge;
         x.w *= Ge;
         for (int m = 0; m < PL; ++m) {
-            const float w = PC_s[m] * PU_s[m * RB + r];
-            const uint2 kk = *reinterpret_cast<const uint2*>(PK_s + m * KS + c);
+            const int p = path[m];
+            const float w = PW_s[m] * PU_s[p * RB + r];
+            const uint2 kk = *reinterpret_cast<const uint2*>(PK_s + p * KS + c);
             x.x = fmaf(w, bf16_bits_to_float((uint16_t)(kk.x & 0xffff)), x.x);
             x.y = fmaf(w, bf16_bits_to_float((uint16_t)(kk.x >> 16)), x.y);
             x.z = fmaf(w, bf16_bits_to_float((uint16_t)(kk.y & 0xffff)), x.z);
@@ -312,9 +320,25 @@ __global__ void __launch_bounds__(kGdnThreads, (NPT == 32 && RB <= 32) ? 3 : 2)
     }
     for (int i = tid; i < N; i += kGdnThreads) cp_async4(par_s + i, a.parent + (size_t)b * N + i);
     const bool pending = a.pend_path != nullptr;
+    constexpr int CH = DK / 8;  // 16-byte chunks per bf16 row
     if (pending) {
-        for (int i = tid; i < N; i += kGdnThreads) cp_async4(ppath_s + i, a.pend_path + (size_t)b * N + i);
+        // the pending path and the previous step's k, u (this CTA's rows)
+        // and g of every node, all in the same round trip: the path picks
+        // its rows from them in shared memory
+        for (int i = tid; i < N; i += kGdnThreads) {
+            cp_async4(ppath_s + i, a.pend_path + (size_t)b * N + i);
+            cp_async4(PC_s + i, a.pend_g + ((size_t)b * N + i) * a.Hv + h);
+        }
         if (tid == 0) cp_async4(misc_s + 2, a.pend_len + b);
+        constexpr int UCH = RB / 4;  // 16-byte chunks of this CTA's u row block
+        for (int idx = tid; idx < N * (CH + UCH); idx += kGdnThreads) {
+            const int i = idx / (CH + UCH), c = idx % (CH + UCH);
+            if (c < CH)
+                cp_async16(PK_s + i * KS + c * 8, a.pend_k + (((size_t)b * N + i) * a.Hk + hk) * DK + c * 8);
+            else
+                cp_async16(PU_s + i * RB + (c - CH) * 4,
+                           a.pend_u + (((size_t)b * N + i) * a.Hv + h) * a.dv + r0 + (c - CH) * 4);
+        }
     }
     cp_async_commit();
     // The first half (warps 0-3) requests this layer's inputs; the second
@@ -324,7 +348,6 @@ __global__ void __launch_bounds__(kGdnThreads, (NPT == 32 && RB <= 32) ? 3 : 2)
     const bool gram_half = warp < kHalfWarps;
     const int ht = gram_half ? tid : tid - kGdnThreads / 2;  // thread index within the half
     constexpr int kHalf = kGdnThreads / 2;
-    constexpr int CH = DK / 8;  // 16-byte chunks per bf16 row
     auto issue_layer_inputs = [&]() {
         for (int idx = ht; idx < N * CH; idx += kHalf) {
             const int i = idx / CH, c = idx % CH;
@@ -382,27 +405,11 @@ __global__ void __launch_bounds__(kGdnThreads, (NPT == 32 && RB <= 32) ? 3 : 2)
         }
     }
     if (!gram_half) {
-        // the pending path's k rows, this CTA's u rows and the path's decays
-        if (PL > 0) {
-            constexpr int UCH = RB / 4;  // 16-byte chunks of this CTA's u row block
-            for (int idx = ht; idx < PL * (CH + UCH); idx += kHalf) {
-                const int m = idx / (CH + UCH), c = idx % (CH + UCH), p = ppath_s[m];
-                if (c < CH)
-                    cp_async16(PK_s + m * KS + c * 8, a.pend_k + (((size_t)b * N + p) * a.Hk + hk) * DK + c * 8);
-                else
-                    cp_async16(PU_s + m * RB + (c - CH) * 4,
-                               a.pend_u + (((size_t)b * N + p) * a.Hv + h) * a.dv + r0 + (c - CH) * 4);
-            }
-            for (int m = ht; m < PL; m += kHalf)
-                cp_async4(PC_s + m, a.pend_g + ((size_t)b * N + ppath_s[m]) * a.Hv + h);
-            cp_async_commit();
-            cp_async_wait<0>();
-            named_barrier_sync(2, kHalf);
-        }
+        // the previous step's rows landed with the parent array
         if (!mbar_wait_bounded(bar, 0, a.status)) {
             if (lane == 0) atomicOr(misc_s + 1, 1);
         } else if (PL > 0) {
-            gdn_apply_pending<DK, RB>(a, S_s, PK_s, PU_s, PC_s, PL, b, h, r0, ht);
+            gdn_apply_pending<DK, RB>(a, S_s, PK_s, PU_s, PC_s, ppath_s, PL, b, h, r0, ht);
         }
         if (early) grid_dependency_wait();  // before any output is written
     } else {
@@ -417,10 +424,15 @@ __global__ void __launch_bounds__(kGdnThreads, (NPT == 32 && RB <= 32) ? 3 : 2)
     if (misc_s[1]) return;  // the state copy never landed (status already raised)
 
     if (warp < kHalfWarps) {
-        // 3. cumulative log decay over the ancestors-or-self: a masked sum
-        //    over all NPT slots with a fixed trip count (the loads are the
-        //    same address across the warp and need no data-dependent loop)
-        for (int i = tid; i < n; i += kGdnThreads / 2) {
+        gdn_gram_tiles<DK, NPT>(K_s, Q_s, A_s, M_s, g_s, beta_s, amask_s, n, warp, gq, tq);
+    } else {
+        // 3. cumulative log decay over the ancestors-or-self, by this half
+        //    (which has slack: its state products end before the Gram tiles
+        //    do): a masked sum over all NPT slots with a fixed trip count
+        //    (the loads are the same address across the warp).  The Gram
+        //    half's epilogue waits for it at barrier 1.
+        const int ht2 = tid - kGdnThreads / 2;
+        for (int i = ht2; i < n; i += kGdnThreads / 2) {
             const uint64_t am = amask_s[i];
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -429,18 +441,21 @@ __global__ void __launch_bounds__(kGdnThreads, (NPT == 32 && RB <= 32) ? 3 : 2)
             g_s[i] = g;
             G_s[i] = expf(g);
         }
-        gdn_gram_tiles<DK, NPT>(K_s, Q_s, A_s, M_s, g_s, beta_s, amask_s, n, warp, gq, tq);
-    } else {
+        named_barrier_arrive(1, kGdnThreads);
         // 6. S_0[rows] . [K | Q]
         gdn_state_products<DK, RB, NPT>(S_s, K_s, Q_s, R_s, SQ_s, warp - kHalfWarps, gq, tq);
     }
     __syncthreads();
 
-    // 7-8. Rows are independent: lane r of the first RB threads solves
+    // 7-9. Rows are independent: lane r of the first RB threads solves
     //    u_i = R_i - sum_{l < i} A_il u_l,  R_i = beta_i (v_i - e^{g_i} S_0 k_i),
     //    for all nodes in index order (a node's ancestors precede it) with
-    //    u in registers.  A is zero off the ancestors in every tile read, so every
-    //    trip count is fixed; the rows of A are read by all lanes at once.
+    //    u in registers, and forms each output as soon as the u it needs are
+    //    known:  o_i = e^{g_i} SQ_i + sum_{l <= i} M_il u_l.  The output
+    //    products depend on no later node, so they fill the gaps of the
+    //    solve's dependence chain.  A and M are zero off the ancestors in
+    //    every tile read, so every trip count is fixed; their rows are read
+    //    by all lanes at once.
     if (tid < RB) {
         const int r = tid;
         float u[NPT];
@@ -448,9 +463,9 @@ __global__ void __launch_bounds__(kGdnThreads, (NPT == 32 && RB <= 32) ? 3 : 2)
         for (int i = 0; i < NPT; ++i) u[i] = 0.f;
         // Nodes go in chunks of 8 with no branch inside a chunk, so the loads
         // of a chunk (rows of A, v, S_0 k) are scheduled ahead of the FMA
-        // chain.  Nodes n .. chunk end compute values that are never read:
-        // a valid node i reads u_l for l < 4 ceil(i/4) only, and u_l with
-        // l > i is still zero when node i is solved.
+        // chain.  Nodes n .. chunk end are set to zero and never stored: a
+        // valid node i reads u_l for l < 4 ceil(i/4) only, u_l with l > i is
+        // still zero when node i is solved, and M_il is zero for l > i.
 #pragma unroll
         for (int c = 0; c < NPT / 8; ++c) {
             if (8 * c < n) {
@@ -467,32 +482,30 @@ __global__ void __launch_bounds__(kGdnThreads, (NPT == 32 && RB <= 32) ? 3 : 2)
                         acc[2] = fmaf(-w.z, u[4 * l4 + 2], acc[2]);
                         acc[3] = fmaf(-w.w, u[4 * l4 + 3], acc[3]);
                     }
-                    u[i] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+                    // padded nodes keep u = 0: the output products below
+                    // read whole groups of four nodes
+                    u[i] = (i < n) ? (acc[0] + acc[1]) + (acc[2] + acc[3]) : 0.f;
+                }
+#pragma unroll
+                for (int i = 8 * c; i < 8 * c + 8; ++i) {
+                    const float4* Mr = reinterpret_cast<const float4*>(M_s + i * NPT);
+                    float acc0 = G_s[i] * SQ_s[i * RB + r], acc1 = 0.f;
+#pragma unroll
+                    for (int l4 = 0; l4 <= i / 4; ++l4) {
+                        const float4 w = Mr[l4];
+                        acc0 = fmaf(w.x, u[4 * l4], acc0);
+                        acc1 = fmaf(w.y, u[4 * l4 + 1], acc1);
+                        acc0 = fmaf(w.z, u[4 * l4 + 2], acc0);
+                        acc1 = fmaf(w.w, u[4 * l4 + 3], acc1);
+                    }
+                    if (i < n) {
+                        const size_t off = (((size_t)b * N + i) * a.Hv + h) * a.dv + r0 + r;
+                        a.u[off] = u[i];
+                        a.out[off] = acc0 + acc1;
+                    }
                 }
             }
         }
-#pragma unroll
-        for (int i = 0; i < NPT; ++i)
-            if (i < n) R_s[i * RB + r] = u[i];
-    }
-    __syncthreads();
-
-    // 9. o_i = e^{g_i} SQ_i + sum_{l <= i} M_il u_l; u and o to global.
-    for (int idx = tid; idx < n * RB; idx += kGdnThreads) {
-        const int i = idx / RB, r = idx % RB;
-        const float4* Mr = reinterpret_cast<const float4*>(M_s + i * NPT);
-        float acc0 = G_s[i] * SQ_s[i * RB + r], acc1 = 0.f;
-        for (int l4 = 0; l4 <= i / 4; ++l4) {
-            const float4 w = Mr[l4];
-            const int l = 4 * l4;
-            acc0 = fmaf(w.x, R_s[l * RB + r], acc0);
-            acc1 = fmaf(w.y, R_s[(l + 1) * RB + r], acc1);
-            acc0 = fmaf(w.z, R_s[(l + 2) * RB + r], acc0);
-            acc1 = fmaf(w.w, R_s[(l + 3) * RB + r], acc1);
-        }
-        const size_t off = (((size_t)b * N + i) * a.Hv + h) * a.dv + r0 + r;
-        a.u[off] = R_s[i * RB + r];
-        a.out[off] = acc0 + acc1;
     }
 
     // 10. The remaining factors, once per (sequence, head) / (sequence, q/k head).

@@ -55,10 +55,19 @@ struct AttnVerifyArgs {
     uint16_t* vs;
     float* out;
     int32_t* status;
+    // caller's workspace (may be null): when it holds at least
+    // attn_workspace_bytes(), the key splits merge through it
+    void* ws;
+    size_t ws_bytes;
 };
 
 cudaError_t launch_attn_tree_verify(const AttnVerifyArgs& a, cudaStream_t stream);
 cudaError_t launch_attn_tree_verify_tc(const AttnVerifyArgs& a, cudaStream_t stream);
+// Bytes of workspace with which a call of this shape merges its key splits
+// through global memory (0: the shape never uses one).  Depends on the
+// current device (the launch plan follows its cluster occupancy).
+size_t attn_workspace_bytes(const AttnVerifyArgs& a);
+size_t attn_workspace_bytes_tc(const AttnVerifyArgs& a);
 
 // Code bytes of one cache row of plane `plane` (0: keys, 1: values) for a
 // dflv_kv_type (the asymmetric types differ between the planes).

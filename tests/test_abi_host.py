@@ -78,7 +78,11 @@ def test_attn_host_validation(lib):
     assert call(d(), cache=dflv.dflv_kv_layer(16, 16, None, 16)) == dflv.DFLV_ERR_INVALID_ARG
     assert call(d(), cache=dflv.dflv_kv_layer(16, 16, 18, 16)) == dflv.DFLV_ERR_INVALID_ARG  # scale rows
     assert call(d(), q=None) == dflv.DFLV_ERR_INVALID_ARG
-    assert dflv.dflv_attn_workspace_size(d()) == 0
+    assert call(d(), workspace=24, ws_bytes=1 << 20) == dflv.DFLV_ERR_INVALID_ARG  # misaligned workspace
+    # the workspace size follows the device's launch plan (a GPU test checks
+    # it is positive there); an invalid descriptor needs none
+    assert dflv.dflv_attn_workspace_size(d(N_max=65)) == 0
+    assert dflv.dflv_attn_workspace_size(d()) >= 0
 
 
 def test_accept_and_commit_host_validation(lib):

@@ -35,7 +35,9 @@ def _plane_np_dtype(key, kv_type):
 
 
 def gpu_attn(dflv, parent, n_nodes, n_past, inp, cache, window, kv_type, Hq, Hkv, D, expect_status=0,
-             rows_only=None):
+             rows_only=None, ws=False):
+    """ws: merge the key splits through a workspace of the queried size
+    (else through the cluster's shared memory)."""
     B, N = parent.shape
     cap = cache["kq"].shape[2]
     keep = {k: dev(v) for k, v in inp.items()}
@@ -44,9 +46,14 @@ def gpu_attn(dflv, parent, n_nodes, n_past, inp, cache, window, kv_type, Hq, Hkv
     out = torch.full((B, N, Hq, D), float("nan"), dtype=torch.float32, device="cuda")
     st = zeros_status()
     desc = dflv.attn_desc(B, N, Hq, Hkv, D, cap, window, kv_type, 1.0 / np.sqrt(D))
+    wsb = dflv.dflv_attn_workspace_size(desc) if ws else 0
+    if ws:
+        assert wsb > 0 or D not in (128, 256) or kv_type == synth.KV_F32
+    # stale contents must not matter: the workspace starts as NaN bytes
+    wst = torch.full((max(wsb, 16) // 4,), float("nan"), device="cuda") if ws else None
     rc = dflv.dflv_tree_attn_verify(desc, keep["parent"], keep["n_nodes"], keep["n_past"], keep["q"],
                                     keep["k_new"], keep["v_new"], dflv.kv_layer(dc["kq"], dc["vq"], dc["ks"], dc["vs"]),
-                                    out, st)
+                                    out, st, wst, wsb)
     dflv.check(rc, "dflv_tree_attn_verify")
     torch.cuda.synchronize()
     assert int(st.item()) == expect_status
@@ -71,8 +78,8 @@ def make_case(rng, kv_type, ns, P, cap, Hq, Hkv, D, tree="ddtree", scale_std=0.0
     return parent, n_nodes, n_past, inp, cache
 
 
-def check_against_oracle(dflv, orc, parent, n_nodes, n_past, inp, cache, window, kv_type, Hq, Hkv, D):
-    out, planes = gpu_attn(dflv, parent, n_nodes, n_past, inp, cache, window, kv_type, Hq, Hkv, D)
+def check_against_oracle(dflv, orc, parent, n_nodes, n_past, inp, cache, window, kv_type, Hq, Hkv, D, ws=False):
+    out, planes = gpu_attn(dflv, parent, n_nodes, n_past, inp, cache, window, kv_type, Hq, Hkv, D, ws=ws)
     ref_cache = synth.copy_cache(cache)
     ref = orc.tree_attn_verify(parent, n_nodes, n_past, inp["q"], inp["k_new"], inp["v_new"], ref_cache,
                                window, kv_type)
@@ -104,12 +111,13 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("ws", [False, True], ids=["cluster_merge", "workspace_merge"])
 @pytest.mark.parametrize("case", SMALL)
-def test_attn_tree_verify_matches_oracle(dflv, orc, case):
+def test_attn_tree_verify_matches_oracle(dflv, orc, case, ws):
     kv_type, ns, P, cap, Hq, Hkv, D, window, tree = case
     rng = np.random.default_rng(len(ns) * 1000 + cap + D + window)
     args = make_case(rng, kv_type, ns, P, cap, Hq, Hkv, D, tree)
-    check_against_oracle(dflv, orc, *args, window, kv_type, Hq, Hkv, D)
+    check_against_oracle(dflv, orc, *args, window, kv_type, Hq, Hkv, D, ws=ws)
 
 
 def test_attn_f32_cache_tiny_case(dflv, orc):
@@ -119,13 +127,14 @@ def test_attn_f32_cache_tiny_case(dflv, orc):
     check_against_oracle(dflv, orc, *args, 0, synth.KV_F32, 1, 1, 16)
 
 
-def test_attn_full_size_32k_q8_window(dflv, orc):
+@pytest.mark.parametrize("ws", [False, True], ids=["cluster_merge", "workspace_merge"])
+def test_attn_full_size_32k_q8_window(dflv, orc, ws):
     # full-attention layer of a 27B-class target: 24 query heads, 4 KV heads,
     # head size 256, q8_0 cache of 32,768 tokens, window 2048, 22-node tree
     rng = np.random.default_rng(1236)
     args = make_case(rng, synth.KV_Q8_0, [22], 32768, 32768 + 64, 24, 4, 256, "ddtree")
-    e = check_against_oracle(dflv, orc, *args, 2048, synth.KV_Q8_0, 24, 4, 256)
-    print(f"full-size attention max rel err {e:.2e}")
+    e = check_against_oracle(dflv, orc, *args, 2048, synth.KV_Q8_0, 24, 4, 256, ws=ws)
+    print(f"full-size attention max rel err {e:.2e} ({'workspace' if ws else 'cluster'} merge)")
 
 
 @pytest.mark.parametrize("n", [8, 22, 64])
@@ -139,7 +148,7 @@ def test_attn_long_context_q4_full_attention(dflv, orc, n):
     inp = synth.attn_inputs(rng, B, n, Hq, Hkv, D)
     cache = synth.kv_cache(rng, B, Hkv, P + 64, D, synth.KV_Q4_0)
     n_past = np.full(B, P, np.int32)
-    out, planes = gpu_attn(dflv, parent, n_nodes, n_past, inp, cache, 0, synth.KV_Q4_0, Hq, Hkv, D)
+    out, planes = gpu_attn(dflv, parent, n_nodes, n_past, inp, cache, 0, synth.KV_Q4_0, Hq, Hkv, D, ws=n != 8)
     # every row of one whole sequence (all nodes x all query heads: every row
     # tile, KV head and key split of that sequence's launch blocks), plus
     # sampled rows of three other sequences
@@ -204,8 +213,12 @@ def test_attn_layers_back_to_back_with_early_prefetch(dflv, orc):
             torch.mul(src[k], 1, out=dst[k])
         flags = 0 if li == 0 else dflv.DFLV_FLAG_EARLY_PREFETCH
         desc = dflv.attn_desc(1, 22, Hq, Hkv, D, P + 64, W, synth.KV_Q8_0, 1.0 / np.sqrt(D), flags)
+        if li == 0:  # one workspace shared by the three calls on the stream
+            wsb = dflv.dflv_attn_workspace_size(desc)
+            wst = torch.empty(wsb, dtype=torch.uint8, device="cuda")
         dflv.check(dflv.dflv_tree_attn_verify(desc, dp, dn, dP, dst["q"], dst["k_new"], dst["v_new"],
-                                              dflv.kv_layer(dc["kq"], dc["vq"], dc["ks"], dc["vs"]), out, st))
+                                              dflv.kv_layer(dc["kq"], dc["vq"], dc["ks"], dc["vs"]), out, st, wst,
+                                              wsb))
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     for inp, cache, src, dst, dc, out in layers:
