@@ -239,24 +239,51 @@ DFLV_DEVINL void gdn_apply_pending(const GdnVerifyArgs& a, float* S_s, const uin
     named_barrier_sync(2, kGdnThreads / 2);
     const float Ge = PW_s[kMaxNodes];
     float* dst = a.state_out + (((size_t)b * a.Hv + h) * a.dv + r0) * DK;
-    for (int e4 = ht; e4 < RB * DK / 4; e4 += kGdnThreads / 2) {
-        const int r = (e4 * 4) / DK, c = (e4 * 4) % DK;
-        float4 x = *reinterpret_cast<const float4*>(S_s + r * DK + c);
-        x.x *= Ge;
-        x.y *= Ge;
-        x.z *= Ge;
-        x.w *= Ge;
-        for (int m = 0; m < PL; ++m) {
-            const int p = path[m];
-            const float w = PW_s[m] * PU_s[p * RB + r];
-            const uint2 kk = *reinterpret_cast<const uint2*>(PK_s + p * KS + c);
-            x.x = fmaf(w, bf16_bits_to_float((uint16_t)(kk.x & 0xffff)), x.x);
-            x.y = fmaf(w, bf16_bits_to_float((uint16_t)(kk.x >> 16)), x.y);
-            x.z = fmaf(w, bf16_bits_to_float((uint16_t)(kk.y & 0xffff)), x.z);
-            x.w = fmaf(w, bf16_bits_to_float((uint16_t)(kk.y >> 16)), x.w);
+    // Thread ht owns the float4 at column c = 4 (ht % (DK/4)) of rows
+    // r_j = ht / (DK/4) + j * 128 / (DK/4): the same four columns in every
+    // row, so each path node's k contributes one 8-byte load per thread, and
+    // the rows' values stay in registers across the path.
+    constexpr int C4 = DK / 4;                       // float4 per row
+    constexpr int TOT = RB * C4;                     // float4 in the row block
+    constexpr int J = (TOT + kGdnThreads / 2 - 1) / (kGdnThreads / 2);
+    constexpr int RSTEP = (kGdnThreads / 2) / C4;    // rows between a thread's items
+    static_assert((kGdnThreads / 2) % C4 == 0, "a thread keeps one column group");
+    const int c = (ht % C4) * 4, rr = ht / C4;
+    float4 x[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        x[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (ht + j * (kGdnThreads / 2) < TOT) {
+            x[j] = *reinterpret_cast<const float4*>(S_s + (rr + j * RSTEP) * DK + c);
+            x[j].x *= Ge;
+            x[j].y *= Ge;
+            x[j].z *= Ge;
+            x[j].w *= Ge;
         }
-        *reinterpret_cast<float4*>(S_s + r * DK + c) = x;
-        *reinterpret_cast<float4*>(dst + r * DK + c) = x;
+    }
+    for (int m = 0; m < PL; ++m) {
+        const int p = path[m];
+        const float wm = PW_s[m];
+        const uint2 kk = *reinterpret_cast<const uint2*>(PK_s + p * KS + c);
+        const float k0 = bf16_bits_to_float((uint16_t)(kk.x & 0xffff)), k1 = bf16_bits_to_float((uint16_t)(kk.x >> 16));
+        const float k2 = bf16_bits_to_float((uint16_t)(kk.y & 0xffff)), k3 = bf16_bits_to_float((uint16_t)(kk.y >> 16));
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            const int r = min(rr + j * RSTEP, RB - 1);
+            const float w = wm * PU_s[p * RB + r];
+            x[j].x = fmaf(w, k0, x[j].x);
+            x[j].y = fmaf(w, k1, x[j].y);
+            x[j].z = fmaf(w, k2, x[j].z);
+            x[j].w = fmaf(w, k3, x[j].w);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        if (ht + j * (kGdnThreads / 2) < TOT) {
+            const int r = rr + j * RSTEP;
+            *reinterpret_cast<float4*>(S_s + r * DK + c) = x[j];
+            *reinterpret_cast<float4*>(dst + r * DK + c) = x[j];
+        }
     }
     named_barrier_sync(2, kGdnThreads / 2);  // every row is updated before the products read them
 }
