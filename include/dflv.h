@@ -37,7 +37,9 @@
  *
  * General conventions
  *   - Every array argument is a DEVICE pointer unless marked "host".  The
- *     caller owns every buffer; the library never allocates or frees memory.
+ *     caller owns every buffer; the library never allocates or frees memory
+ *     (dflv_tree_attn_verify_noalloc uses one fixed scratch array of the
+ *     library's own instead, below).
  *   - bf16 and fp16 values are passed as uint16_t bit patterns.
  *   - All calls are asynchronous on the given stream (0 = legacy default
  *     stream) and never synchronise it, so a whole step can be captured in a
@@ -52,7 +54,9 @@
  *     caller zeroes and reads back when it wants to check.
  *   - Pointers to bf16/f32/int8/u8 arrays and to the fp16 scale planes of a
  *     KV cache must be 16-byte aligned.
- *   - No global state: calls are re-entrant on distinct buffers.
+ *   - No global state: calls are re-entrant on distinct buffers (except
+ *     dflv_tree_attn_verify_noalloc, whose calls on one device share its
+ *     scratch array).
  *   - Padded nodes (i >= n_nodes[b]) are ignored; their outputs are
  *     unspecified.
  */
@@ -351,6 +355,37 @@ dflv_status dflv_tree_attn_verify(const dflv_attn_desc* desc, const int32_t* par
                                   const uint16_t* v_new, const dflv_kv_layer* cache, float* out,
                                   int32_t* status_dev, void* workspace, size_t ws_bytes,
                                   dflv_stream_t stream);
+
+/* Attention tree verify that allocates nothing, for callers that cannot
+ * allocate device memory (the pages have no counterpart: this is a
+ * deployment aid).  Some hosts forbid device allocation on the path that
+ * runs a step: a serving runtime that hands each plugin a fixed memory pool,
+ * an allocator that must not be entered while a CUDA graph is being
+ * captured, or a latency-bound loop that cannot afford the implicit
+ * synchronisation of cudaMalloc.  Such callers use this entry point instead
+ * of passing a workspace to dflv_tree_attn_verify.
+ *   Arguments and results: exactly those of dflv_tree_attn_verify without
+ *   workspace / ws_bytes.  Its merge scratch is one array of
+ *   DFLV_NOALLOC_SCRATCH_BYTES in the library's own device memory, which every
+ *   GPU that loads the library holds until the process exits.
+ *   - A descriptor whose merge needs more scratch than that
+ *     (dflv_attn_workspace_size(desc) > DFLV_NOALLOC_SCRATCH_BYTES) returns
+ *     DFLV_ERR_CAPACITY and launches nothing.
+ *   - It calls no cudaMalloc / cudaFree and no allocating library routine.
+ *     The first call on a device looks up the scratch's device address for
+ *     that device (with it current); make that first call before any stream
+ *     capture.
+ *   - Every call on a device shares the one scratch array, which keeps the
+ *     last call's contents.  Nothing in it needs to start at zero (each
+ *     call writes every value it reads), but calls whose kernels can
+ *     overlap on the GPU (other streams, or other host threads) race on it:
+ *     run them on one stream, one after the other. */
+#define DFLV_NOALLOC_SCRATCH_BYTES (16u << 20)
+dflv_status dflv_tree_attn_verify_noalloc(const dflv_attn_desc* desc, const int32_t* parent,
+                                          const int32_t* n_nodes, const int32_t* n_past,
+                                          const uint16_t* q, const uint16_t* k_new,
+                                          const uint16_t* v_new, const dflv_kv_layer* cache, float* out,
+                                          int32_t* status_dev, dflv_stream_t stream);
 
 /* Bytes of workspace with which dflv_tree_attn_verify merges through global
  * memory for this descriptor (0: the shape never uses one; also 0 for an

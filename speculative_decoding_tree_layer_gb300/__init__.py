@@ -13,7 +13,8 @@ from .dflv import (DFLV_DEV_CAPACITY, DFLV_DEV_PATH, DFLV_DEV_TIMEOUT, DFLV_DEV_
                    attn_desc, check, dflv_accept_greedy, dflv_attn_workspace_size, dflv_commit_rollback,
                    dflv_gdn_workspace_size, dflv_status_string, dflv_tree_attn_verify, dflv_tree_gdn_verify,
                    dflv_tree_gdn_verify_pending, dflv_tree_conv_verify, dflv_conv_commit, DFLV_MAX_CONV_LAYERS,
-                   dflv_ddtree_build, conv_desc, ddtree_desc, gdn_desc, gdn_factors, kv_layer, load)
+                   dflv_ddtree_build, conv_desc, ddtree_desc, gdn_desc, gdn_factors, kv_layer, load,
+                   dflv_tree_attn_verify_noalloc, DFLV_NOALLOC_SCRATCH_BYTES)
 
 __all__ = [n for n in dir() if n.startswith(("dflv", "DFLV", "Dflv")) or n in (
     "attn_desc", "conv_desc", "ddtree_desc", "gdn_desc", "gdn_factors", "kv_layer", "load", "build", "check")]

@@ -17,7 +17,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libdflv.so")
-SOURCES = ["api.cu", "gdn_verify.cu", "attn_verify.cu", "attn_verify_tc.cu", "accept.cu", "commit.cu", "conv_tree.cu", "ddtree.cu"]
+SOURCES = ["api.cu", "gdn_verify.cu", "attn_verify.cu", "attn_verify_tc.cu", "accept.cu", "commit.cu", "conv_tree.cu", "ddtree.cu",
+           "attn_noalloc.cu"]
 HEADERS = ["common.cuh", "tree.cuh", "kernels.h", "attn_common.cuh", "tcgen05.cuh", "cluster.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -82,6 +82,8 @@ def load():
         [ctypes.POINTER(dflv_gdn_factors), P, P, P, ctypes.POINTER(dflv_gdn_factors), P, P, S, P]
     lib.dflv_tree_attn_verify.argtypes = [ctypes.POINTER(dflv_attn_desc)] + [P] * 6 + \
         [ctypes.POINTER(dflv_kv_layer), P, P, P, S, P]
+    lib.dflv_tree_attn_verify_noalloc.argtypes = [ctypes.POINTER(dflv_attn_desc)] + [P] * 6 + \
+        [ctypes.POINTER(dflv_kv_layer), P, P, P]
     lib.dflv_accept_greedy.argtypes = [_c_i32, _c_i32, _c_i32] + [P] * 10
     lib.dflv_commit_rollback.argtypes = [ctypes.POINTER(dflv_gdn_desc), _c_i32, P, ctypes.POINTER(dflv_gdn_factors),
                                          ctypes.POINTER(dflv_attn_desc), _c_i32, ctypes.POINTER(dflv_kv_layer),
@@ -95,7 +97,8 @@ def load():
     lib.dflv_attn_workspace_size.restype = S
     lib.dflv_status_string.argtypes = [ctypes.c_int]
     lib.dflv_status_string.restype = ctypes.c_char_p
-    for f in ("dflv_tree_gdn_verify", "dflv_tree_gdn_verify_pending", "dflv_tree_attn_verify", "dflv_accept_greedy",
+    for f in ("dflv_tree_gdn_verify", "dflv_tree_gdn_verify_pending", "dflv_tree_attn_verify",
+              "dflv_tree_attn_verify_noalloc", "dflv_accept_greedy",
               "dflv_commit_rollback", "dflv_tree_conv_verify", "dflv_conv_commit", "dflv_ddtree_build"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
@@ -187,6 +190,16 @@ def dflv_tree_attn_verify(desc, parent, n_nodes, n_past, q, k_new, v_new, cache,
         ctypes.byref(desc), _ptr(parent), _ptr(n_nodes), _ptr(n_past), _ptr(q), _ptr(k_new),
         _ptr(v_new), ctypes.byref(cache), _ptr(out), _ptr(status_dev), _ptr(workspace), ws_bytes,
         _stream(stream))
+
+
+def dflv_tree_attn_verify_noalloc(desc, parent, n_nodes, n_past, q, k_new, v_new, cache, out, status_dev,
+                                  stream=None) -> int:
+    return load().dflv_tree_attn_verify_noalloc(
+        ctypes.byref(desc), _ptr(parent), _ptr(n_nodes), _ptr(n_past), _ptr(q), _ptr(k_new),
+        _ptr(v_new), ctypes.byref(cache), _ptr(out), _ptr(status_dev), _stream(stream))
+
+
+DFLV_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 def dflv_accept_greedy(B, N_max, vocab, logits, tokens, parent, n_nodes, path, path_len, next_token,

@@ -184,3 +184,10 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
         dflv.load()
     with pytest.raises(RuntimeError, match="not built"):
         dflv.dflv_accept_greedy(1, 2, 4, 16, 16, 16, 16, 16, 16, 16, 16, 16)
+
+
+def test_noalloc_scratch_size_matches_the_header():
+    import re
+    with open(dflv.HEADER) as f:
+        m = re.search(r"#define DFLV_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", f.read())
+    assert m and int(m.group(1)) << int(m.group(2)) == dflv.DFLV_NOALLOC_SCRATCH_BYTES
