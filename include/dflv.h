@@ -97,7 +97,17 @@ typedef enum {
     /* Asymmetric caches ([README] "Asymmetric K/V quantization": keys and
      * values quantised independently), head sizes 128 and 256: */
     DFLV_KV_Q8_0_Q4_0 = 3, /* keys q8_0, values q4_0 */
-    DFLV_KV_Q4_0_Q8_0 = 4  /* keys q4_0, values q8_0 */
+    DFLV_KV_Q4_0_Q8_0 = 4, /* keys q4_0, values q8_0 */
+    /* TQ3_0 ([README] "Results" KV note: TQ3_0 at 3.5 bits per value, the
+     * default; "Asymmetric K/V quantization": a fast Walsh-Hadamard rotation
+     * applied to the query and undone on the attention output when the keys
+     * are TQ3_0).  Keys and values both: each cached row is the orthonormal
+     * Walsh-Hadamard transform (Sylvester order, over the whole head) of the
+     * bf16 row, in blocks of 32 with one fp16 scale d = amax / 3 and 32
+     * three-bit codes c = clamp(round-half-away(x * (1/d)), -4, 3) + 4, code j
+     * in bits 3j .. 3j+2 of the block's 12 little-endian bytes; x = d * (c - 4)
+     * in the rotated basis.  Head sizes 128 and 256. */
+    DFLV_KV_TQ3_0 = 5
 } dflv_kv_type;
 
 /* Launch overlap.  Every kernel of this library is launched with
@@ -305,8 +315,8 @@ dflv_status dflv_ddtree_build(const dflv_ddtree_desc* desc, const float* draft_l
  * to a node at position p iff j <= p and (W == 0 or j > p - W).  Node i sits
  * at position P + depth(i).  scale multiplies q.k (usually 1/sqrt(D)).
  * Supported: 1 <= N_max <= 64; q8_0/q4_0 with D in {64, 128, 256}; the
- * asymmetric types with D in {128, 256}; f32 with D a multiple of 4,
- * D <= 256. */
+ * asymmetric types and TQ3_0 with D in {128, 256}; f32 with D a multiple of
+ * 4, D <= 256. */
 typedef struct {
     int32_t B, N_max, Hq, Hkv, D, cap, window;
     dflv_kv_type type;
@@ -318,7 +328,9 @@ typedef struct {
  * own format for the asymmetric types):
  *   kq, vq : q8_0: int8 [B][Hkv][cap][D]; q4_0: uint8 [B][Hkv][cap][D/2]
  *            (element j < 16 of a 32-block in the low nibble of byte j,
- *            element j+16 in its high nibble); f32: float [B][Hkv][cap][D]
+ *            element j+16 in its high nibble); TQ3_0: uint8
+ *            [B][Hkv][cap][3D/8] (12 bytes per 32-block); f32: float
+ *            [B][Hkv][cap][D]
  *   ks, vs : fp16 [B][Hkv][cap][D/32] block scales (NULL for f32) */
 typedef struct {
     void* kq;

@@ -8,7 +8,7 @@ from ._build import build
 from .dflv import (DFLV_DEV_CAPACITY, DFLV_DEV_PATH, DFLV_DEV_TIMEOUT, DFLV_DEV_TOPOLOGY,
                    DFLV_ERR_CAPACITY, DFLV_ERR_CUDA, DFLV_ERR_INVALID_ARG, DFLV_ERR_TOPOLOGY,
                    DFLV_ERR_UNSUPPORTED, DFLV_FLAG_EARLY_PREFETCH, DFLV_KV_F32, DFLV_KV_Q4_0, DFLV_KV_Q8_0, DFLV_KV_Q8_0_Q4_0,
-                   DFLV_KV_Q4_0_Q8_0, DFLV_OK,
+                   DFLV_KV_Q4_0_Q8_0, DFLV_KV_TQ3_0, DFLV_OK,
                    DflvError,
                    attn_desc, check, dflv_accept_greedy, dflv_attn_workspace_size, dflv_commit_rollback,
                    dflv_gdn_workspace_size, dflv_status_string, dflv_tree_attn_verify, dflv_tree_gdn_verify,

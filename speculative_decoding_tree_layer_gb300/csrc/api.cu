@@ -44,6 +44,7 @@ dflv_status check_attn_desc(const dflv_attn_desc* d) {
             break;
         case DFLV_KV_Q8_0_Q4_0:
         case DFLV_KV_Q4_0_Q8_0:
+        case DFLV_KV_TQ3_0:
             if (d->D != 128 && d->D != 256) return DFLV_ERR_UNSUPPORTED;
             break;
         default:

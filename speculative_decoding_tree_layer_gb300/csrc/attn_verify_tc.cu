@@ -67,7 +67,7 @@ constexpr int kTreeCost = 3;                         // a tree tile (quantise + 
 template <int D, int T>
 struct PlaneFmt {
     static constexpr int NB = D / 32;
-    static constexpr int KB = (T == DFLV_KV_Q8_0) ? D : D / 2;  // code bytes per key row
+    static constexpr int KB = (T == DFLV_KV_Q8_0) ? D : (T == DFLV_KV_TQ3_0) ? D / 32 * 12 : D / 2;  // code bytes per key row
     static constexpr int RSK = KB + 16;                            // padded raw row stride
     static constexpr size_t kRawCodes = (size_t)kTK * RSK;
     static constexpr size_t kRawScales = (size_t)kTK * NB * 2 + 16;  // + room for a misaligned start
@@ -90,7 +90,11 @@ struct TcLayout {
     static constexpr size_t off_V = off_K + 2 * kK;          // two buffers of V_hi then V_lo
     static constexpr size_t off_rawK = off_V + 4 * kV;           // two buffers
     static constexpr size_t off_rawV = off_rawK + 2 * FK::kRaw;  // two buffers
-    static constexpr size_t loop_total = off_rawV + 2 * FV::kRaw;
+    // TQ3_0: the rotated query rows of one half of the row tile, fp16
+    static constexpr bool kRotated = KT == DFLV_KV_TQ3_0;
+    static constexpr size_t off_QS = off_rawV + 2 * FV::kRaw;
+    static constexpr size_t kQS = kRotated ? (size_t)(kRows / 2) * (D + 8) * 2 : 0;  // row stride D + 8 halves
+    static constexpr size_t loop_total = off_QS + kQS;
     // merge: CS x ceil(RT / CS) <= kRows + 15 received partial rows
     static constexpr size_t off_Om = kHeader;
     static constexpr size_t merge_total = off_Om + (size_t)(kRows + 16) * OS * 4;
@@ -112,6 +116,112 @@ DFLV_DEVINL bool wait_phase(uint64_t* bar, uint32_t parity) {
     for (uint32_t it = 0; it < kWaitLimit; ++it)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
+}
+
+// ---------------------------------------------------------------- TQ3_0
+// Eight three-bit codes (bits 3j .. 3j+2 of `bits`) -> value - 4 as exact
+// fp16 pairs: 0x6400 | c is 1024 + c.
+DFLV_DEVINL void u3x8_to_f16x2(uint32_t bits, uint32_t (&cv)[4]) {
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6404), __ushort_as_half(0x6404));  // 1028
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const uint32_t c0 = (bits >> (6 * e)) & 7u, c1 = (bits >> (6 * e + 3)) & 7u;
+        const uint32_t w = 0x64006400u | c0 | (c1 << 16);
+        const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&w), bias);
+        cv[e] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+}
+
+// Orthonormal Walsh-Hadamard transform (Sylvester order) of one row of D
+// values held by a warp, D/32 consecutive values per lane: the butterflies
+// (a + b, a - b on the pair (j, j + h)) with strides h = 1, 2, ..., D/2 in
+// that order, then the product with fl(1/sqrt(D)).  These are the fp32
+// operations of the plain serial loop, in its order for every element, so
+// the result is bit-identical to it.
+template <int D>
+DFLV_DEVINL void fwht_warp(float (&v)[D / 32], int lane) {
+    constexpr int V = D / 32;
+#pragma unroll
+    for (int h = 1; h < V; h *= 2)
+#pragma unroll
+        for (int j = 0; j < V; ++j)
+            if ((j & h) == 0) {
+                const float x = v[j], y = v[j + h];
+                v[j] = __fadd_rn(x, y);
+                v[j + h] = __fsub_rn(x, y);
+            }
+#pragma unroll
+    for (int hl = 1; hl < 32; hl *= 2) {  // stride h = hl * V: the partner lane holds the other element
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const float o = __shfl_xor_sync(0xffffffffu, v[j], hl);
+            v[j] = (lane & hl) ? __fsub_rn(o, v[j]) : __fadd_rn(v[j], o);
+        }
+    }
+    const float s = (float)(1.0 / sqrt((double)D));
+#pragma unroll
+    for (int j = 0; j < V; ++j) v[j] = __fmul_rn(v[j], s);
+}
+
+// A bf16 row of D values -> the warp's registers (D/32 consecutive per lane).
+template <int D>
+DFLV_DEVINL void load_row_warp(const uint16_t* src, float (&v)[D / 32], int lane) {
+    constexpr int V = D / 32;
+    uint32_t w[V / 2];
+    if constexpr (V == 8) {
+        const uint4 x = __ldg(reinterpret_cast<const uint4*>(src) + lane);
+        w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
+    } else {
+        const uint2 x = __ldg(reinterpret_cast<const uint2*>(src) + lane);
+        w[0] = x.x; w[1] = x.y;
+    }
+#pragma unroll
+    for (int e = 0; e < V / 2; ++e) {
+        v[2 * e] = bf16_bits_to_float((uint16_t)(w[e] & 0xffff));
+        v[2 * e + 1] = bf16_bits_to_float((uint16_t)(w[e] >> 16));
+    }
+}
+
+// One rotated tree row into the TQ3_0 cache: the warp's D values (after
+// fwht_warp) in blocks of 32 (32 / V lanes each): d = amax / 3 stored as
+// fp16, codes = clamp(round-half-away(x * fl(1/d)), -4, 3) + 4 packed as a
+// little-endian bit stream of 3 bits per value, 12 bytes per block.
+template <int D>
+DFLV_DEVINL void quantize_tq3_warp(const float (&v)[D / 32], uint8_t* __restrict__ codes,
+                                   uint16_t* __restrict__ scales, int lane) {
+    constexpr int V = D / 32, LPB = 32 / V;  // values per lane, lanes per block
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < V; ++j) amax = fmaxf(amax, fabsf(v[j]));
+#pragma unroll
+    for (int o = 1; o < LPB; o *= 2) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float d = __fdiv_rn(amax, 3.f);
+    const float id = (d != 0.f) ? __frcp_rn(d) : 0.f;
+    uint32_t bits = 0;
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        const int c = (int)fminf(fmaxf(roundf(__fmul_rn(v[j], id)), -4.f), 3.f) + 4;
+        bits |= (uint32_t)c << (3 * j);
+    }
+    const int blk = lane / LPB, q = lane % LPB;
+    if constexpr (V == 4) {
+        // 12 bits per lane: even lanes take their odd neighbour's bits and
+        // write the pair's 3 bytes
+        const uint32_t nb = __shfl_down_sync(0xffffffffu, bits, 1);
+        if ((q & 1) == 0) {
+            bits |= nb << 12;
+            uint8_t* p = codes + blk * 12 + 3 * (q / 2);
+            p[0] = (uint8_t)bits;
+            p[1] = (uint8_t)(bits >> 8);
+            p[2] = (uint8_t)(bits >> 16);
+        }
+    } else {
+        uint8_t* p = codes + blk * 12 + 3 * q;
+        p[0] = (uint8_t)bits;
+        p[1] = (uint8_t)(bits >> 8);
+        p[2] = (uint8_t)(bits >> 16);
+    }
+    if (q == 0) scales[blk] = __half_as_ushort(__float2half_rn(d));
 }
 
 // Expand one raw tile (codes + scales of `count` keys) into fp16 hi + lo with
@@ -140,6 +250,10 @@ DFLV_DEVINL void stage_hilo(const uint8_t* __restrict__ codes, const uint16_t* _
             sbv[j] = scales[c * L::NB + (d8 * 8) / 32];
             if constexpr (TYPE == DFLV_KV_Q8_0) {
                 wv[j] = *reinterpret_cast<const uint2*>(codes + c * L::RSK + d8 * 8);
+            } else if constexpr (TYPE == DFLV_KV_TQ3_0) {
+                // the 8 three-bit codes of this chunk: 3 whole bytes
+                const uint8_t* p = codes + c * L::RSK + (d8 / 4) * 12 + 3 * (d8 % 4);
+                wv[j].x = (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16);
             } else {
                 const int blk = (d8 * 8) / 32, off = (d8 * 8) % 32;
                 wv[j] = *reinterpret_cast<const uint2*>(codes + c * L::RSK + blk * 16 + (off & 15));
@@ -159,6 +273,8 @@ DFLV_DEVINL void stage_hilo(const uint8_t* __restrict__ codes, const uint16_t* _
             if constexpr (TYPE == DFLV_KV_Q8_0) {
                 i8x4_to_f16x2(w.x, cv[0], cv[1]);
                 i8x4_to_f16x2(w.y, cv[2], cv[3]);
+            } else if constexpr (TYPE == DFLV_KV_TQ3_0) {
+                u3x8_to_f16x2(w.x, cv);
             } else {
                 // element j < 16 of a 32-block in the low nibble of byte j,
                 // element j + 16 in its high nibble
@@ -348,8 +464,60 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
 
     // ---- Q rows -> fp16 pairs in tensor memory: softmax thread r writes row
     //      r into its own lane (rows past the tile are zero); every load of a
-    //      thread is issued before the first is used
-    if (warp < kSoftWarps) {
+    //      thread is issued before the first is used.  With a TQ3_0 cache the
+    //      query goes into the keys' rotated basis first: the prep warps
+    //      rotate the rows (one warp per row, fp32) into shared memory, half
+    //      of the row tile at a time, and the softmax threads of that half
+    //      copy their rows from there.
+    const int pw = warp < kSoftWarps ? warp : warp - kStageWarps;  // prep warp index
+    constexpr int kPrepWarps = kPrepThreads / 32;
+    if constexpr (L::kRotated) {
+        if (!stage_warp) {
+            constexpr int QSS = D + 8;  // fp16 row stride (bank-conflict free row reads)
+            __half* QS = reinterpret_cast<__half*>(smem + L::off_QS);
+#pragma unroll 1
+            for (int hf = 0; hf < 2; ++hf) {
+                for (int rr = pw; rr < kRows / 2; rr += kPrepWarps) {
+                    const int r = hf * (kRows / 2) + rr, rho = row0 + r;
+                    float v[D / 32];
+                    if (r < RT && rho < rows_valid) {
+                        load_row_warp<D>(a.q + (((size_t)b * N + rho / G) * a.Hq + kvh * G + rho % G) * D, v, lane);
+                        fwht_warp<D>(v, lane);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < D / 32; ++j) v[j] = 0.f;
+                    }
+                    uint32_t hv[D / 64];
+#pragma unroll
+                    for (int j = 0; j < D / 64; ++j) hv[j] = pack_f16x2(v[2 * j], v[2 * j + 1]);
+                    if constexpr (D / 64 == 4)
+                        *reinterpret_cast<uint4*>(QS + rr * QSS + lane * (D / 32)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                    else
+                        *reinterpret_cast<uint2*>(QS + rr * QSS + lane * (D / 32)) = make_uint2(hv[0], hv[1]);
+                }
+                named_barrier_sync_n(kPrepBarrier, kPrepThreads);
+                if (warp == 2 * hf || warp == 2 * hf + 1) {
+                    const int rr = tid - hf * (kRows / 2);
+                    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c) {  // 64 dims = 32 columns per store
+                        uint32_t v[32];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const uint4 x = *reinterpret_cast<const uint4*>(QS + rr * QSS + c * 64 + j * 8);
+                            v[4 * j] = x.x;
+                            v[4 * j + 1] = x.y;
+                            v[4 * j + 2] = x.z;
+                            v[4 * j + 3] = x.w;
+                        }
+                        tc::st32u(tmem + lane_off + L::kQcol + (uint32_t)(c * 32), v);
+                    }
+                    tc::fence_before_sync();
+                }
+                named_barrier_sync_n(kPrepBarrier, kPrepThreads);  // the staging rows are free again
+            }
+        }
+    } else if (warp < kSoftWarps) {
         const int r = tid, rho = row0 + r;
         const bool on = r < RT && rho < rows_valid;
         const uint4* src = on ? reinterpret_cast<const uint4*>(a.q + (((size_t)b * N + rho / G) * a.Hq + kvh * G + rho % G) * D)
@@ -382,15 +550,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
         const int r_lo = max(0, g0 - n_cache_tiles) * kTK;
         const int r_hi = min(n, (g0 + T - n_cache_tiles) * kTK);
         const int nblk = (r_hi > r_lo) ? (r_hi - r_lo) * NB : 0;
-        for (int k = pt; k < 2 * nblk; k += kPrepThreads) {
+        if constexpr (L::kRotated) {
+            // TQ3_0: each tree row is rotated as a whole before it is
+            // quantised (one warp per row and plane)
+            const int nrow = (r_hi > r_lo) ? r_hi - r_lo : 0;
+            for (int k = pw; k < 2 * nrow; k += kPrepWarps) {
+                const bool vplane = k & 1;
+                const int row = r_lo + k / 2;
+                float v[D / 32];
+                load_row_warp<D>((vplane ? a.v_new : a.k_new) + (((size_t)b * N + row) * a.Hkv + kvh) * D, v, lane);
+                fwht_warp<D>(v, lane);
+                const size_t slot = plane_row0 + P + row;
+                quantize_tq3_warp<D>(v, (vplane ? vq : kq) + slot * FK::KB, (vplane ? a.vs : a.ks) + slot * NB, lane);
+            }
+        }
+        for (int k = pt; k < (L::kRotated ? 0 : 2 * nblk); k += kPrepThreads) {
             const bool vplane = k >= nblk;
             const int kk = vplane ? k - nblk : k, row = r_lo + kk / NB, blk = kk % NB;
             const uint16_t* src = (vplane ? a.v_new : a.k_new) + (((size_t)b * N + row) * a.Hkv + kvh) * D + blk * 32;
             const size_t slot = plane_row0 + P + row;
-            if (vplane)
-                quantize_block<VT>(src, vq + slot * FV::KB + blk * (FV::KB / NB), a.vs + slot * NB + blk);
-            else
-                quantize_block<KT>(src, kq + slot * FK::KB + blk * (FK::KB / NB), a.ks + slot * NB + blk);
+            if constexpr (!L::kRotated) {
+                if (vplane)
+                    quantize_block<VT>(src, vq + slot * FV::KB + blk * (FV::KB / NB), a.vs + slot * NB + blk);
+                else
+                    quantize_block<KT>(src, kq + slot * FK::KB + blk * (FK::KB / NB), a.ks + slot * NB + blk);
+            }
         }
         __threadfence();
         fence_proxy_async_smem();
@@ -704,6 +888,66 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
     // ---- merge the owned rows
     constexpr int nwarps = kThreads / 32;
     constexpr int PL = D / 32;  // output floats per lane when a warp takes a whole row
+    if (gmerge && L::kRotated) {
+        // TQ3_0: the output is rotated back after the merge, which needs a
+        // whole row in one warp: one warp per owned row, peers in batches
+        // of eight (every load of a batch in flight at once), merged online
+        const int n_own = (rank < rows_here) ? (rows_here - 1 - rank) / CS + 1 : 0;
+        for (int slot = warp; slot < n_own; slot += nwarps) {
+            const int r = rank + slot * CS, rho = row0 + r;
+            float Mr = -INFINITY, Lt = 0.f, acc[PL];
+#pragma unroll
+            for (int e = 0; e < PL; ++e) acc[e] = 0.f;
+            for (int q0 = 0; q0 < CS; q0 += 8) {
+                float2 ml[8];
+                float ov[8][PL];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    ml[q] = make_float2(-INFINITY, 0.f);
+#pragma unroll
+                    for (int e = 0; e < PL; ++e) ov[q][e] = 0.f;
+                    if (q0 + q < CS) {
+                        const float* src = wsb + ((size_t)(q0 + q) * RT + r) * OS;
+                        ml[q] = __ldcg(reinterpret_cast<const float2*>(src + D));
+#pragma unroll
+                        for (int e = 0; e < PL; e += 4) {
+                            const float4 x = __ldcg(reinterpret_cast<const float4*>(src + lane * PL + e));
+                            ov[q][e] = x.x;
+                            ov[q][e + 1] = x.y;
+                            ov[q][e + 2] = x.z;
+                            ov[q][e + 3] = x.w;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float mq = ml[q].x;
+                    if (mq == -INFINITY) continue;  // absent peer, or one without keys for this row
+                    if (mq > Mr) {
+                        const float sc = (Mr == -INFINITY) ? 0.f : exp2f(Mr - mq);
+                        Lt *= sc;
+#pragma unroll
+                        for (int e = 0; e < PL; ++e) acc[e] *= sc;
+                        Mr = mq;
+                    }
+                    const float w = exp2f(mq - Mr);
+                    Lt = fmaf(w, ml[q].y, Lt);
+#pragma unroll
+                    for (int e = 0; e < PL; ++e) acc[e] = fmaf(w, ov[q][e], acc[e]);
+                }
+            }
+            const float inv = 1.f / Lt;
+#pragma unroll
+            for (int e = 0; e < PL; ++e) acc[e] *= inv;
+            fwht_warp<D>(acc, lane);  // back from the values' rotated basis
+            const int i = rho / G, gh = rho % G;
+            float* dsto = a.out + (((size_t)b * N + i) * a.Hq + kvh * G + gh) * D + lane * PL;
+#pragma unroll
+            for (int e = 0; e < PL; e += 4)
+                *reinterpret_cast<float4*>(dsto + e) = make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
+        }
+        return;
+    }
     if (gmerge) {
         // an item is half of an owned row (D / 2 dims, D / 64 per lane);
         // every peer's partial of it is requested at once (CS <= 16), then
@@ -789,11 +1033,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
             }
         }
         const float inv = 1.f / Lt;
+#pragma unroll
+        for (int e = 0; e < PL; ++e) acc[e] *= inv;
+        if constexpr (L::kRotated) fwht_warp<D>(acc, lane);  // back from the values' rotated basis
         const int i = rho / G, gh = rho % G;
         float* dst = a.out + (((size_t)b * N + i) * a.Hq + kvh * G + gh) * D + lane * PL;
 #pragma unroll
         for (int e = 0; e < PL; e += 4)
-            *reinterpret_cast<float4*>(dst + e) = make_float4(acc[e] * inv, acc[e + 1] * inv, acc[e + 2] * inv, acc[e + 3] * inv);
+            *reinterpret_cast<float4*>(dst + e) = make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
     }
 }
 
@@ -917,6 +1164,7 @@ cudaError_t launch_tc_d(const AttnVerifyArgs& a, cudaStream_t stream) {
         case DFLV_KV_Q4_0: return launch_tc<D, Q4, Q4>(a, stream);
         case DFLV_KV_Q8_0_Q4_0: return launch_tc<D, Q8, Q4>(a, stream);
         case DFLV_KV_Q4_0_Q8_0: return launch_tc<D, Q4, Q8>(a, stream);
+        case DFLV_KV_TQ3_0: return launch_tc<D, DFLV_KV_TQ3_0, DFLV_KV_TQ3_0>(a, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -937,6 +1185,7 @@ size_t ws_bytes_tc_d(const AttnVerifyArgs& a) {
         case DFLV_KV_Q4_0: return ws_bytes_tc<D, Q4, Q4>(a);
         case DFLV_KV_Q8_0_Q4_0: return ws_bytes_tc<D, Q8, Q4>(a);
         case DFLV_KV_Q4_0_Q8_0: return ws_bytes_tc<D, Q4, Q8>(a);
+        case DFLV_KV_TQ3_0: return ws_bytes_tc<D, DFLV_KV_TQ3_0, DFLV_KV_TQ3_0>(a);
         default: return 0;
     }
 }

@@ -75,7 +75,7 @@ __host__ __device__ inline int kv_code_bytes(int type, int plane, int D) {
     int t = type;
     if (type == DFLV_KV_Q8_0_Q4_0) t = plane ? DFLV_KV_Q4_0 : DFLV_KV_Q8_0;
     else if (type == DFLV_KV_Q4_0_Q8_0) t = plane ? DFLV_KV_Q8_0 : DFLV_KV_Q4_0;
-    return t == DFLV_KV_Q8_0 ? D : t == DFLV_KV_Q4_0 ? D / 2 : D * 4;
+    return t == DFLV_KV_Q8_0 ? D : t == DFLV_KV_Q4_0 ? D / 2 : t == DFLV_KV_TQ3_0 ? D / 32 * 12 : D * 4;
 }
 
 struct AcceptArgs {

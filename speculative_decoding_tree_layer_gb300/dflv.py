@@ -20,7 +20,7 @@ HEADER = os.path.join(os.path.dirname(_HERE), "include", "dflv.h")
 
 DFLV_OK, DFLV_ERR_INVALID_ARG, DFLV_ERR_TOPOLOGY, DFLV_ERR_UNSUPPORTED, DFLV_ERR_CAPACITY, DFLV_ERR_CUDA = range(6)
 DFLV_DEV_TOPOLOGY, DFLV_DEV_CAPACITY, DFLV_DEV_PATH, DFLV_DEV_TIMEOUT = 1, 2, 4, 8
-DFLV_KV_Q8_0, DFLV_KV_Q4_0, DFLV_KV_F32, DFLV_KV_Q8_0_Q4_0, DFLV_KV_Q4_0_Q8_0 = 0, 1, 2, 3, 4
+DFLV_KV_Q8_0, DFLV_KV_Q4_0, DFLV_KV_F32, DFLV_KV_Q8_0_Q4_0, DFLV_KV_Q4_0_Q8_0, DFLV_KV_TQ3_0 = 0, 1, 2, 3, 4, 5
 DFLV_FLAG_EARLY_PREFETCH = 1
 DFLV_MAX_COMMIT_GDN_LAYERS, DFLV_MAX_COMMIT_ATTN_LAYERS = 128, 64
 DFLV_MAX_CONV_LAYERS = 128

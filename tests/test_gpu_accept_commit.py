@@ -138,11 +138,12 @@ def gpu_commit(dflv, gdn_layers, attn_layers, path, path_len, n_past, dims, expe
 
 
 @pytest.mark.parametrize("kv_type", [synth.KV_Q8_0, synth.KV_Q4_0, synth.KV_F32, synth.KV_Q8_0_Q4_0,
-                                     synth.KV_Q4_0_Q8_0])
+                                     synth.KV_Q4_0_Q8_0, synth.KV_TQ3_0])
 def test_commit_gdn_and_kv(dflv, orc, kv_type):
     rng = np.random.default_rng(40 + kv_type)
     Hk, Hv, dk, dv = 2, 6, 128, 64
-    Hq, Hkv, D = 4, 2, {synth.KV_F32: 16, synth.KV_Q8_0_Q4_0: 128, synth.KV_Q4_0_Q8_0: 128}.get(kv_type, 64)
+    Hq, Hkv, D = 4, 2, {synth.KV_F32: 16, synth.KV_Q8_0_Q4_0: 128, synth.KV_Q4_0_Q8_0: 128,
+                        synth.KV_TQ3_0: 128}.get(kv_type, 64)
     B, N = 3, 9
     parents = [np.array([-1, 0, 0, 2, 3, 1, 4, 6, 6], np.int32),  # accepted path 0, 2, 3 aliases
                synth.chain_tree(9), np.array([-1, 0, 1, 1], np.int32)]

@@ -31,7 +31,8 @@ def _plane_np_dtype(key, kv_type):
         kv_type = synth.KV_Q8_0 if key == "kq" else synth.KV_Q4_0
     elif kv_type == synth.KV_Q4_0_Q8_0:
         kv_type = synth.KV_Q4_0 if key == "kq" else synth.KV_Q8_0
-    return {synth.KV_Q8_0: np.int8, synth.KV_Q4_0: np.uint8, synth.KV_F32: np.float32}[kv_type]
+    return {synth.KV_Q8_0: np.int8, synth.KV_Q4_0: np.uint8, synth.KV_F32: np.float32,
+            synth.KV_TQ3_0: np.uint8}[kv_type]
 
 
 def gpu_attn(dflv, parent, n_nodes, n_past, inp, cache, window, kv_type, Hq, Hkv, D, expect_status=0,
@@ -108,6 +109,11 @@ SMALL = [
     (synth.KV_Q4_0_Q8_0, [22, 9], [300, 57], 400, 6, 1, 256, 64, "ddtree"),
     (synth.KV_Q8_0_Q4_0, [64, 3], [1000, 5], 1100, 12, 2, 128, 0, "ddtree"),
     (synth.KV_Q4_0_Q8_0, [22], 4096, 4200, 24, 4, 256, 2048, "ddtree"),
+    # TQ3_0: rotated 3.5-bit cache (query rotated in, output rotated back)
+    (synth.KV_TQ3_0, [22, 9], [300, 57], 400, 6, 1, 256, 64, "ddtree"),
+    (synth.KV_TQ3_0, [13], 200, 256, 8, 2, 128, 0, "uniform"),
+    (synth.KV_TQ3_0, [64], 513, 600, 6, 1, 256, 20, "chain"),
+    (synth.KV_TQ3_0, [64, 3], [1000, 5], 1100, 12, 2, 128, 0, "ddtree"),
 ]
 
 
@@ -135,6 +141,37 @@ def test_attn_full_size_32k_q8_window(dflv, orc, ws):
     args = make_case(rng, synth.KV_Q8_0, [22], 32768, 32768 + 64, 24, 4, 256, "ddtree")
     e = check_against_oracle(dflv, orc, *args, 2048, synth.KV_Q8_0, 24, 4, 256, ws=ws)
     print(f"full-size attention max rel err {e:.2e} ({'workspace' if ws else 'cluster'} merge)")
+
+
+@pytest.mark.parametrize("ws", [False, True], ids=["cluster_merge", "workspace_merge"])
+def test_attn_full_size_32k_tq3_window(dflv, orc, ws):
+    # the same layer over a TQ3_0 cache (the pages' default KV type)
+    rng = np.random.default_rng(1237)
+    args = make_case(rng, synth.KV_TQ3_0, [22], 32768, 32768 + 64, 24, 4, 256, "ddtree")
+    e = check_against_oracle(dflv, orc, *args, 2048, synth.KV_TQ3_0, 24, 4, 256, ws=ws)
+    print(f"full-size TQ3_0 attention max rel err {e:.2e} ({'workspace' if ws else 'cluster'} merge)")
+
+
+def test_attn_long_context_tq3_full_attention(dflv, orc):
+    # 2 sequences over a 131,072-token TQ3_0 cache, full attention: every
+    # row of one whole sequence against the oracle, and the tree slots of both
+    rng = np.random.default_rng(1301)
+    B, n, P, Hq, Hkv, D = 2, 22, 131072, 24, 4, 256
+    parents = [synth.ddtree(rng, n, 151936)[0] for _ in range(B)]
+    parent, n_nodes = synth.batch_trees(parents, n)
+    inp = synth.attn_inputs(rng, B, n, Hq, Hkv, D)
+    cache = synth.kv_cache(rng, B, Hkv, P + 64, D, synth.KV_TQ3_0)
+    n_past = np.full(B, P, np.int32)
+    out, planes = gpu_attn(dflv, parent, n_nodes, n_past, inp, cache, 0, synth.KV_TQ3_0, Hq, Hkv, D, ws=True)
+    rows = np.arange(1 * n * Hq, 2 * n * Hq, dtype=np.int32)
+    ref_cache = synth.copy_cache(cache)
+    ref = orc.tree_attn_verify(parent, n_nodes, n_past, inp["q"], inp["k_new"], inp["v_new"], ref_cache, 0,
+                               synth.KV_TQ3_0, rows=rows)
+    e = assert_close(out[1], ref[1], what="every row of sequence 1")
+    print(f"131K TQ3_0 full attention max rel err {e:.2e}")
+    for key in ("kq", "vq", "ks", "vs"):
+        sl = np.s_[:, :, P:P + n]
+        assert np.array_equal(planes[key][sl], ref_cache[key][sl]), key
 
 
 @pytest.mark.parametrize("n", [8, 22, 64])
