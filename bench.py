@@ -303,7 +303,7 @@ class GpuStep:
         self.path_len = t.zeros(1, dtype=t.int32, device=dev)
         self.next_token = t.zeros(1, dtype=t.int32, device=dev)
         self.best = t.zeros((1, N), dtype=t.int32, device=dev)
-        self.h_out = t.empty(N + 2, dtype=t.int32, pin_memory=True)
+        self.h_out = t.empty((2, N + 2), dtype=t.int32, pin_memory=True)   # two slots: steps t and t+1
         # every layer but the first follows a kernel that writes neither its
         # committed state / cache prefix nor the tree: those may be read early
         early = dflv.DFLV_FLAG_EARLY_PREFETCH
@@ -525,17 +525,23 @@ def kernel_chain_ms(S, torch, stream, steps, warmup, flush):
 SCALE_B, SCALE_N, SCALE_CTX = 8, 64, 131072
 
 
-def scale_bytes_attn():
-    Hq, Hkv, D, B, N, P = ATT["Hq"], ATT["Hkv"], ATT["D"], SCALE_B, SCALE_N, SCALE_CTX
-    row = D // 2 + D // 32 * 2                 # q4_0: codes + fp16 scales per (token, head)
+SCALE_ATTN = ((synth.KV_Q4_0, 8), (synth.KV_Q4_0, 22), (synth.KV_Q4_0, 64), (synth.KV_TQ3_0, 64))
+
+
+def scale_bytes_attn(N=SCALE_N, kv=synth.KV_Q4_0):
+    """Attention at the stress shape: every cached key and value read once,
+    q read, o written, the tree's new K/V read and its slots written and read."""
+    Hq, Hkv, D, B, P = ATT["Hq"], ATT["Hkv"], ATT["D"], SCALE_B, SCALE_CTX
+    code = D // 32 * 12 if kv == synth.KV_TQ3_0 else D // 2
+    row = code + D // 32 * 2                   # codes + fp16 scales per (token, head)
     kv = B * 2 * P * Hkv * row
     return kv + B * N * (Hq * D * 2 + Hq * D * 4 + 2 * Hkv * D * 2) + B * 2 * 2 * N * Hkv * row
 
 
-def scale_flops_attn():
+def scale_flops_attn(N=SCALE_N):
     """Q K^T and P V over every (node, query head, visible key): 2 * 2 * D
     flops each (the kernel's hi/lo operand split adds passes, not counted)."""
-    Hq, D, B, N, P = ATT["Hq"], ATT["D"], SCALE_B, SCALE_N, SCALE_CTX
+    Hq, D, B, P = ATT["Hq"], ATT["D"], SCALE_B, SCALE_CTX
     return 2 * 2 * D * B * N * Hq * (P + N)
 
 
@@ -554,11 +560,11 @@ def scale_bytes_gdn():
                 N * Hv * 4 + N * Hk * dk * 2)
 
 
-def scale_trees(torch):
-    """The stress shapes' trees: SCALE_B DDTree-shaped trees of SCALE_N nodes."""
-    rng = np.random.default_rng(SEED + 37)
-    pars = [synth.ddtree(rng, SCALE_N, VOCAB)[0] for _ in range(SCALE_B)]
-    parent, n_nodes = synth.batch_trees(pars, SCALE_N)
+def scale_trees(torch, n=SCALE_N):
+    """The stress shapes' trees: SCALE_B DDTree-shaped trees of n nodes."""
+    rng = np.random.default_rng(SEED + 37 + (n if n != SCALE_N else 0))
+    pars = [synth.ddtree(rng, n, VOCAB)[0] for _ in range(SCALE_B)]
+    parent, n_nodes = synth.batch_trees(pars, n)
     return torch.from_numpy(parent).to("cuda"), torch.from_numpy(n_nodes).to("cuda")
 
 
@@ -623,31 +629,49 @@ def scale_measure(torch, dflv, flush, reps=8, rounds=10):
         torch.cuda.synchronize()
         return float(np.sum(cold_replays(torch, graph, rounds, flush, stream))) / (rounds * reps)
 
-    # attention: q4_0 cache, full attention
-    kq = torch.randint(0, 256, (B, Hkv, cap, D // 2), generator=g, device=dev, dtype=torch.uint8)
-    vq = torch.randint(0, 256, (B, Hkv, cap, D // 2), generator=g, device=dev, dtype=torch.uint8)
-    ks = (torch.rand(B, Hkv, cap, D // 32, generator=g, device=dev) * 0.02).to(torch.float16).view(torch.int16)
-    vs = (torch.rand(B, Hkv, cap, D // 32, generator=g, device=dev) * 0.02).to(torch.float16).view(torch.int16)
-    q, kn, vn = bf16(B, N, Hq, D), bf16(B, N, Hkv, D), bf16(B, N, Hkv, D)
-    n_past = torch.full((B,), P, dtype=torch.int32, device=dev)
-    o = torch.empty((B, N, Hq, D), device=dev)
-    kv = dflv.kv_layer(kq, vq, ks, vs)
-    descs = [dflv.attn_desc(B, N, Hq, Hkv, D, cap, 0, dflv.DFLV_KV_Q4_0, 1.0 / np.sqrt(D), f)
-             for f in (0, dflv.DFLV_FLAG_EARLY_PREFETCH)]
-    wsb = dflv.dflv_attn_workspace_size(descs[0])
-    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
-    ms = timed(lambda r: dflv.check(dflv.dflv_tree_attn_verify(descs[r > 0], par_d, nn_d, n_past, q, kn, vn, kv, o,
-                                                             status, ws, wsb)))
-    byt, flops = scale_bytes_attn(), scale_flops_attn()
+    # attention, full attention over a 131,072-token cache: the budget sweep
+    # over q4_0 (8 nodes: below the ridge, HBM-bound; 22 and 64: tensor-bound)
+    # and the TQ3_0 cache at 64 nodes
     tpk, tkind = bf16_peak()
-    tf = flops / (ms * 1e-3) / 1e12
-    out["attn_q4_131k_b8_n64"] = {"ms_per_launch": ms, "nodes_per_s_per_layer": B * N / (ms * 1e-3),
-                                  "algorithmic_bytes_per_launch": byt,
-                                  "achieved": byt / (ms * 1e-3) / 1e9, "unit": "GB/s",
-                                  "algorithmic_flops_per_launch": flops, "tflops": tf,
-                                  "tensor_peak_tflops": tpk, "tensor_frac": tf / tpk,
-                                  "tensor_peak_source": tkind + " bf16_tflops"}
-    del kq, vq, ks, vs
+    n_past = torch.full((B,), P, dtype=torch.int32, device=dev)
+    for kvt in (synth.KV_Q4_0, synth.KV_TQ3_0):
+        code = D // 32 * 12 if kvt == synth.KV_TQ3_0 else D // 2
+        kq = torch.randint(0, 256, (B, Hkv, cap, code), generator=g, device=dev, dtype=torch.uint8)
+        vq = torch.randint(0, 256, (B, Hkv, cap, code), generator=g, device=dev, dtype=torch.uint8)
+        ks = (torch.rand(B, Hkv, cap, D // 32, generator=g, device=dev) * 0.02).to(torch.float16).view(torch.int16)
+        vs = (torch.rand(B, Hkv, cap, D // 32, generator=g, device=dev) * 0.02).to(torch.float16).view(torch.int16)
+        kv = dflv.kv_layer(kq, vq, ks, vs)
+        for kind, Nn in SCALE_ATTN:
+            if kind != kvt:
+                continue
+            par_n, nn_n = scale_trees(torch, Nn)
+            q, kn, vn = bf16(B, Nn, Hq, D), bf16(B, Nn, Hkv, D), bf16(B, Nn, Hkv, D)
+            o = torch.empty((B, Nn, Hq, D), device=dev)
+            descs = [dflv.attn_desc(B, Nn, Hq, Hkv, D, cap, 0, kvt, 1.0 / np.sqrt(D), f)
+                     for f in (0, dflv.DFLV_FLAG_EARLY_PREFETCH)]
+            wsb = dflv.dflv_attn_workspace_size(descs[0])
+            ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+
+            def attn(r):
+                # every launch attends at the same position: n_past does not
+                # move, and the tree's slots are rewritten in place
+                dflv.check(dflv.dflv_tree_attn_verify(descs[r > 0], par_n, nn_n, n_past, q, kn, vn, kv, o,
+                                                      status, ws, wsb))
+
+            ms = timed(attn)
+            byt, flops = scale_bytes_attn(Nn, kvt), scale_flops_attn(Nn)
+            tf = flops / (ms * 1e-3) / 1e12
+            gbs = byt / (ms * 1e-3) / 1e9
+            name = f"attn_{'tq3' if kvt == synth.KV_TQ3_0 else 'q4'}_131k_b8_n{Nn}"
+            out[name] = {"ms_per_launch": ms, "nodes_per_s_per_layer": B * Nn / (ms * 1e-3),
+                         "algorithmic_bytes_per_launch": byt, "achieved": gbs, "unit": "GB/s",
+                         "flop_per_byte": flops / byt,
+                         "algorithmic_flops_per_launch": flops, "tflops": tf,
+                         "tensor_peak_tflops": tpk, "tensor_frac": tf / tpk,
+                         "tensor_peak_source": tkind + " bf16_tflops",
+                         "bound": "hbm" if flops / byt < tpk * 1e12 / (hbm_peak()[0] * 1e9) else "tensor"}
+            del q, kn, vn, o, ws
+        del kq, vq, ks, vs, kv
     # GDN: 27B shape, batch 8, 64-node trees
     Hk, Hv, dk, dv = GDN["Hk"], GDN["Hv"], GDN["dk"], GDN["dv"]
     sets = [scale_gdn_set(torch, dflv, g) for _ in range(reps)]
@@ -781,27 +805,60 @@ def run_gpu(args, rank, world):
     assert status == 0, f"device status {status} after the per-kernel chains"
     scale = scale_measure(torch, dflv, flush) if not args.no_scale else {}
     del flush
-    # ---- end to end: pinned host inputs -> device, step, result -> host, every step
+    # ---- end to end: pinned host inputs -> device, step, result -> host, every
+    #      step, through the same captured C-ABI calls.  Step t+1's inputs are
+    #      copied on a second stream into a device staging buffer while step t
+    #      runs (the copy engines work beside the SMs); each step then moves
+    #      them into the buffer its captured calls read (a device-to-device
+    #      copy).  The accepted path goes to one of two pinned host slots; the
+    #      host reads step t's path once step t+1 is enqueued, so its wait
+    #      overlaps the next step (the path feeds the host's output, not the
+    #      next step's inputs, which the device produces), and the last
+    #      step's path is read inside the timed region.
     S.reset()
     count[0] = 0
+    d_stage = torch.empty_like(S.d_in)
+    copy_stream = torch.cuda.Stream()
+    copied = torch.cuda.Event()
+    consumed = torch.cuda.Event()
+    result = [torch.cuda.Event(), torch.cuda.Event()]
     torch.cuda.synchronize()
-    for _ in range(args.warmup):
-        S.d_in.copy_(S.h_in, non_blocking=True)
-        replay()
-        S.h_out[: BUDGET].copy_(S.path[0], non_blocking=True)
-        torch.cuda.synchronize()
+
+    def e2e_steps(n):
+        with torch.cuda.stream(copy_stream):
+            d_stage.copy_(S.h_in, non_blocking=True)
+            copied.record(copy_stream)
+        for t in range(n):
+            with torch.cuda.stream(stream):
+                stream.wait_event(copied)
+                S.d_in.copy_(d_stage, non_blocking=True)
+                consumed.record(stream)
+            if t + 1 < n:
+                with torch.cuda.stream(copy_stream):
+                    copy_stream.wait_event(consumed)
+                    d_stage.copy_(S.h_in, non_blocking=True)   # the next step's inputs
+                    copied.record(copy_stream)
+            slot = S.h_out[t % 2]
+            with torch.cuda.stream(stream):
+                replay()
+                slot[: BUDGET].copy_(S.path[0], non_blocking=True)
+                slot[BUDGET].copy_(S.path_len[0], non_blocking=True)
+                slot[BUDGET + 1].copy_(S.next_token[0], non_blocking=True)
+                result[t % 2].record(stream)
+            if t > 0:                         # the host reads the previous step's accepted path
+                result[(t - 1) % 2].synchronize()
+                _ = int(S.h_out[(t - 1) % 2, BUDGET])
+        if n > 0:
+            result[(n - 1) % 2].synchronize()
+            _ = int(S.h_out[(n - 1) % 2, BUDGET])
+
+    e2e_steps(args.warmup)
+    torch.cuda.synchronize()
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.steps):
-        S.d_in.copy_(S.h_in, non_blocking=True)
-        replay()
-        S.h_out[: BUDGET].copy_(S.path[0], non_blocking=True)
-        S.h_out[BUDGET].copy_(S.path_len[0], non_blocking=True)
-        S.h_out[BUDGET + 1].copy_(S.next_token[0], non_blocking=True)
-        torch.cuda.synchronize()          # the host reads the accepted path every step
-        _ = int(S.h_out[BUDGET])
-    e1.record()
+    e0.record(stream)
+    e2e_steps(args.steps)
+    e1.record(stream)
     torch.cuda.synchronize()
     status = int(S.status.item())
     assert status == 0, f"device status {status} after the end-to-end steps"
@@ -1094,10 +1151,10 @@ def main():
         "step_ms_p10_p50_p90": r["step_pct"],
         "nodes_per_s_per_layer": {"step": value / world,
                                   **{k: BUDGET / (per[k] * 1e-3) for k in ("gdn", "attn") if per.get(k)}},
-        "at_scale": {"what": "the stress shapes beside the step: 8 sequences with 64-node trees; attention over a "
-                             "131,072-token q4_0 cache, full attention; GDN of the 27B shape; 8 launches back to "
-                             "back per CUDA graph (the GDN launches on 8 distinct input sets), an L2 flush before "
-                             "each replay, CUDA events",
+        "at_scale": {"what": "the stress shapes beside the step: 8 sequences; attention over a 131,072-token "
+                             "cache with full attention, q4_0 at 8, 22 and 64 nodes per tree and TQ3_0 at 64; GDN "
+                             "of the 27B shape at 64 nodes; 8 launches back to back per CUDA graph (the GDN "
+                             "launches on 8 distinct input sets), an L2 flush before each replay, CUDA events",
                      **{k: dict(v, peak=peak, frac=v["achieved"] / peak) for k, v in r["scale"].items()}},
         "beside_the_step": {"what": "the short convolution in front of each GDN layer (48 tree-conv launches "
                                     "back to back, C=10240, K=4), the commit of its window (one launch, 48 "
@@ -1106,7 +1163,12 @@ def main():
                                     "kernel and a best-first kernel); timed like the step's kernels, not part "
                                     "of the step",
                             **beside},
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
+                "how": "every step: the step's inputs from pinned host memory (copied on a second stream while the "
+                       "previous step runs, then moved into the captured calls' input buffer), one replay of the "
+                       "captured C-ABI calls of the step, the accepted path copied to pinned host memory; the host "
+                       "reads step t's path once step t+1 is enqueued (two host slots), and the last step's path "
+                       "inside the timed region"},
         "gpu_launches": r["launches"] * args.steps,
         "clocks": r["clocks"],
     }

@@ -477,12 +477,16 @@ __global__ void __launch_bounds__(kGdnThreads, (NPT == 32 && RB <= 32) ? 3 : 2)
     // 7-9. Rows are independent: lane r of the first RB threads solves
     //    u_i = R_i - sum_{l < i} A_il u_l,  R_i = beta_i (v_i - e^{g_i} S_0 k_i),
     //    for all nodes in index order (a node's ancestors precede it) with
-    //    u in registers, and forms each output as soon as the u it needs are
-    //    known:  o_i = e^{g_i} SQ_i + sum_{l <= i} M_il u_l.  The output
-    //    products depend on no later node, so they fill the gaps of the
-    //    solve's dependence chain.  A and M are zero off the ancestors in
-    //    every tile read, so every trip count is fixed; their rows are read
-    //    by all lanes at once.
+    //    u in registers.  The outputs are o_i = e^{g_i} SQ_i + sum_{l <= i}
+    //    M_il u_l.  For trees of up to 32 nodes the solving lane forms each
+    //    output as soon as the u it needs are known: those products depend on
+    //    no later node, so they fill the gaps of the solve's dependence chain.
+    //    Larger trees have too many output products for RB lanes; there the u
+    //    go to shared memory and every thread of the block takes a share of
+    //    the outputs.  A and M are zero off the ancestors in every tile read,
+    //    so every trip count is fixed; their rows are read by all lanes at
+    //    once.
+    constexpr bool kFusedOut = NPT <= 32;
     if (tid < RB) {
         const int r = tid;
         float u[NPT];
@@ -515,23 +519,48 @@ __global__ void __launch_bounds__(kGdnThreads, (NPT == 32 && RB <= 32) ? 3 : 2)
                 }
 #pragma unroll
                 for (int i = 8 * c; i < 8 * c + 8; ++i) {
-                    const float4* Mr = reinterpret_cast<const float4*>(M_s + i * NPT);
-                    float acc0 = G_s[i] * SQ_s[i * RB + r], acc1 = 0.f;
+                    if constexpr (kFusedOut) {
+                        const float4* Mr = reinterpret_cast<const float4*>(M_s + i * NPT);
+                        float acc0 = G_s[i] * SQ_s[i * RB + r], acc1 = 0.f;
 #pragma unroll
-                    for (int l4 = 0; l4 <= i / 4; ++l4) {
-                        const float4 w = Mr[l4];
-                        acc0 = fmaf(w.x, u[4 * l4], acc0);
-                        acc1 = fmaf(w.y, u[4 * l4 + 1], acc1);
-                        acc0 = fmaf(w.z, u[4 * l4 + 2], acc0);
-                        acc1 = fmaf(w.w, u[4 * l4 + 3], acc1);
-                    }
-                    if (i < n) {
-                        const size_t off = (((size_t)b * N + i) * a.Hv + h) * a.dv + r0 + r;
-                        a.u[off] = u[i];
-                        a.out[off] = acc0 + acc1;
+                        for (int l4 = 0; l4 <= i / 4; ++l4) {
+                            const float4 w = Mr[l4];
+                            acc0 = fmaf(w.x, u[4 * l4], acc0);
+                            acc1 = fmaf(w.y, u[4 * l4 + 1], acc1);
+                            acc0 = fmaf(w.z, u[4 * l4 + 2], acc0);
+                            acc1 = fmaf(w.w, u[4 * l4 + 3], acc1);
+                        }
+                        if (i < n) {
+                            const size_t off = (((size_t)b * N + i) * a.Hv + h) * a.dv + r0 + r;
+                            a.u[off] = u[i];
+                            a.out[off] = acc0 + acc1;
+                        }
+                    } else if (i < n) {
+                        R_s[i * RB + r] = u[i];
                     }
                 }
             }
+        }
+    }
+    if constexpr (!kFusedOut) {
+        __syncthreads();
+        // o_i = e^{g_i} SQ_i + sum_{l <= i} M_il u_l over all threads; rows of
+        // R_s past n hold S_0 k (finite) and meet zero entries of M
+        for (int idx = tid; idx < n * RB; idx += kGdnThreads) {
+            const int i = idx / RB, r = idx % RB;
+            const float4* Mr = reinterpret_cast<const float4*>(M_s + i * NPT);
+            float acc0 = G_s[i] * SQ_s[i * RB + r], acc1 = 0.f;
+            for (int l4 = 0; l4 <= i / 4; ++l4) {
+                const float4 w = Mr[l4];
+                const int l = 4 * l4;
+                acc0 = fmaf(w.x, R_s[l * RB + r], acc0);
+                acc1 = fmaf(w.y, R_s[(l + 1) * RB + r], acc1);
+                acc0 = fmaf(w.z, R_s[(l + 2) * RB + r], acc0);
+                acc1 = fmaf(w.w, R_s[(l + 3) * RB + r], acc1);
+            }
+            const size_t off = (((size_t)b * N + i) * a.Hv + h) * a.dv + r0 + r;
+            a.u[off] = R_s[i * RB + r];
+            a.out[off] = acc0 + acc1;
         }
     }
 
