@@ -99,9 +99,10 @@ struct TcLayout {
     static constexpr size_t off_Om = kHeader;
     static constexpr size_t merge_total = off_Om + (size_t)(kRows + 16) * OS * 4;
     static constexpr size_t total = loop_total > merge_total ? loop_total : merge_total;
-    // tensor memory: O in columns [0, D), two S / P buffers of 2 kTK columns
-    // at kScol, Q (fp16 pairs) in D / 2 columns at kQcol
-    static constexpr uint32_t kScol = D, kQcol = D + 4 * kTK;
+    // tensor memory: O in columns [0, D), the S buffer ([S_hi | S_lo], 2 kTK
+    // columns) at kScol, two P buffers of kTK columns (P_hi | P_lo as fp16
+    // pairs) at kPcol, Q (fp16 pairs) in D / 2 columns at kQcol
+    static constexpr uint32_t kScol = D, kPcol = D + 2 * kTK, kQcol = D + 4 * kTK;
     static constexpr uint32_t kTmemCols = (kQcol + D / 2 <= 256) ? 256 : 512;
     static_assert(kQcol + D / 2 <= 512, "O, the S buffers and Q fit in tensor memory");
 };
@@ -109,7 +110,7 @@ struct TcLayout {
 // header offsets
 constexpr int kHdrDepth = 256, kHdrMask = 512, kHdrBar = 1024, kHdrSlot = 1280, kHdrFail = 1284;
 enum Bar { kRawK0, kRawK1, kRawV0, kRawV1, kKFree0, kKFree1, kVFree0, kVFree1, kKReady0, kKReady1, kVReady0,
-           kVReady1, kSFull0, kSFull1, kPReady0, kPReady1, kODone0, kODone1, kMmaFin, kNumBars };
+           kVReady1, kSFull0, kSFull1, kSFree0, kSFree1, kPReady0, kPReady1, kODone0, kODone1, kMmaFin, kNumBars };
 static_assert(kHdrBar + kNumBars * 8 <= kHdrSlot, "barriers fit below the TMEM slot");
 
 DFLV_DEVINL bool wait_phase(uint64_t* bar, uint32_t parity) {
@@ -422,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
     if (tid == 0) {
         for (int i = 0; i < kNumBars; ++i) {
             const bool by_stagers = i >= kKFree0 && i <= kVReady1;
-            const bool by_softmax = i == kPReady0 || i == kPReady1;
+            const bool by_softmax = i == kPReady0 || i == kPReady1 || i == kSFree0 || i == kSFree1;
             const int count = i <= kRawV1 ? 32 : by_stagers ? kStageThreads : by_softmax ? kSoftWarps * 32 : 1;
             mbar_init(bars + i, count);
         }
@@ -609,6 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
                 if (lane == 0) atomicOr(fail_s, 1);
                 break;
             }
+            mbar_arrive(bars + kSFree0 + (t & 1));
             mbar_arrive(bars + kPReady0 + (t & 1));
         }
         for (int t = 0; t < T && warp_active; ++t) {
@@ -621,14 +623,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
             }
             tc::fence_after_sync();
             float s[kTK];
-            const uint32_t ts = tmem + L::kScol + (uint32_t)((t & 1) * 2 * kTK);  // this tile's S / P buffer
             {
                 float sh[32], sl[32];
-                tc::ld32(ts + lane_off, sh);
-                tc::ld32(ts + lane_off + kTK, sl);
+                tc::ld32(tmem + L::kScol + lane_off, sh);
+                tc::ld32(tmem + L::kScol + lane_off + kTK, sl);
 #pragma unroll
                 for (int c = 0; c < kTK; ++c) s[c] = sh[c] + sl[c];
             }
+            // the S buffer is read: the next tile's scores may go into it
+            tc::fence_before_sync();
+            mbar_arrive(bars + kSFree0 + (t & 1));
             float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
             if (ti.tree) {
 #pragma unroll
@@ -688,10 +692,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
                 pl[j / 2] = *reinterpret_cast<const uint32_t*>(&l2);
             }
             l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            // P over the scores just read: P_hi in the buffer's columns
-            // [0, kTK/2), P_lo in [kTK/2, kTK)
-            tc::st16u(ts + lane_off, ph);
-            tc::st16u(ts + lane_off + kTK / 2, pl);
+            // P buffer t & 1 was last read by the products of tile t - 2
+            if (t >= 2) {
+                const bool okp = __all_sync(0xffffffffu, wait_phase(bars + kODone0 + (t & 1), ((t - 2) >> 1) & 1));
+                if (!okp) {
+                    if (lane == 0) atomicOr(fail_s, 1);
+                    break;
+                }
+                tc::fence_after_sync();
+            }
+            // P_hi in the buffer's columns [0, kTK/2), P_lo in [kTK/2, kTK)
+            const uint32_t tp = tmem + L::kPcol + (uint32_t)((t & 1) * kTK);
+            tc::st16u(tp + lane_off, ph);
+            tc::st16u(tp + lane_off + kTK / 2, pl);
             tc::fence_before_sync();
             mbar_arrive(bars + kPReady0 + (t & 1));
         }
@@ -764,29 +777,37 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
         // [S_hi | S_lo] of tile t = Q (tensor memory) [K_hi ; K_lo]^T
         auto issue_qk = [&](int t) {
             const uint32_t kb = smem_u32(smem + L::off_K + (t & 1) * L::kK);
-            const uint32_t ts = tmem + L::kScol + (uint32_t)((t & 1) * 2 * kTK);
+            const uint32_t ts = tmem + L::kScol;
 #pragma unroll 4
             for (int ks = 0; ks < D / 16; ++ks)
                 tc::mma_f16_ts(ts, tmem + L::kQcol + (uint32_t)(ks * 8), tc::smem_desc(kb + ks * 256, 128, SBO),
                                idesc_qk, ks > 0);
             tc::commit(bars + kSFull0 + (t & 1));
         };
-        bool ok = true;
-        for (int t = 0; t < min(T, 2) && ok; ++t) {
-            ok = wait_phase(bars + kKReady0 + t, 0);
-            if (ok) {
-                tc::fence_after_sync();
-                issue_qk(t);
-            }
+        // Per tile t: the scores of tile t + 1 as soon as the softmax has
+        // read those of tile t (one S buffer; P goes to its own buffers), so
+        // they are formed while the softmax works; then the products of tile
+        // t once its P is written.
+        bool ok = T <= 0 || wait_phase(bars + kKReady0, 0);
+        if (ok && T > 0) {
+            tc::fence_after_sync();
+            issue_qk(0);
         }
         for (int t = 0; t < T && ok; ++t) {
+            if (t + 1 < T) {
+                ok = wait_phase(bars + kKReady0 + ((t + 1) & 1), ((t + 1) >> 1) & 1) &&
+                     wait_phase(bars + kSFree0 + (t & 1), (t >> 1) & 1);
+                if (!ok) break;
+                tc::fence_after_sync();
+                issue_qk(t + 1);
+            }
             ok = wait_phase(bars + kPReady0 + (t & 1), (t >> 1) & 1) &&
                  wait_phase(bars + kVReady0 + (t & 1), (t >> 1) & 1);
             if (!ok) break;
             tc::fence_after_sync();
-            // O += P_hi V_hi + P_hi V_lo + P_lo V_hi, P (tensor memory) over
-            // this tile's S buffer: P_hi in its columns [0, kTK/2), P_lo after
-            const uint32_t ps = tmem + L::kScol + (uint32_t)((t & 1) * 2 * kTK);
+            // O += P_hi V_hi + P_hi V_lo + P_lo V_hi, P (tensor memory) in
+            // buffer t & 1: P_hi in its columns [0, kTK/2), P_lo after
+            const uint32_t ps = tmem + L::kPcol + (uint32_t)((t & 1) * kTK);
             const uint32_t vh = smem_u32(smem + L::off_V + (t & 1) * 2 * L::kV), vl = vh + (uint32_t)L::kV;
 #pragma unroll
             for (int ks = 0; ks < kTK / 16; ++ks) {
@@ -798,15 +819,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
                 tc::mma_f16_ts(tmem_O, al, bh, idesc_pv, true);
             }
             tc::commit(bars + kODone0 + (t & 1));
-            // the scores of tile t + 2 go into this buffer once these
-            // products (which read P from it) have completed
-            if (t + 2 < T) {
-                ok = wait_phase(bars + kKReady0 + (t & 1), ((t + 2) >> 1) & 1) &&
-                     wait_phase(bars + kODone0 + (t & 1), (t >> 1) & 1);
-                if (!ok) break;
-                tc::fence_after_sync();
-                issue_qk(t + 2);
-            }
         }
         if (!ok) atomicOr(fail_s, 1);
         // every MMA issued above has completed before TMEM or smem is reused

@@ -75,6 +75,22 @@ DFLV_DEVINL void named_barrier_arrive(int id, int count) {
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Where A_il and M_il sit in shared memory.  Trees of up to 32 nodes are
+// solved by every thread of the block, TPR = 256 / RB threads per state row,
+// thread q of a row owning nodes q, q + TPR, q + 2 TPR, ...: there both
+// matrices are stored by column l, with each thread's nodes contiguous, so
+// a thread reads its share of a column with vector loads.  Larger trees
+// keep row-major [i][l].
+template <int NPT, int RB>
+DFLV_DEVINL int amat_at(int i, int l) {
+    if constexpr (NPT <= 32) {
+        constexpr int TPR = kGdnThreads / RB, NPN = NPT / TPR;
+        return l * NPT + (i % TPR) * NPN + i / TPR;
+    } else {
+        return i * NPT + l;
+    }
+}
+
 // 4-5. [K ; Q] K^T on the tensor cores by the kHalfWarps warps of the first
 //    half, with the decays and the ancestor mask applied to the accumulators:
 //      A_il = beta_i e^{g_i-g_l} k_i.k_l for strict ancestors l of i,
@@ -88,7 +104,7 @@ DFLV_DEVINL void named_barrier_arrive(int id, int count) {
 //    cumulative decays g_s (written by the other half, which arrives at
 //    barrier 1 when done) are read only after that barrier, once the
 //    products are in registers.
-template <int DK, int NPT>
+template <int DK, int NPT, int RB>
 DFLV_DEVINL void gdn_gram_tiles(const uint16_t* K_s, const uint16_t* Q_s, float* A_s, float* M_s,
                                 const float* g_s, const float* beta_s, const uint64_t* amask_s, int n, int warp,
                                 int gq, int tq) {
@@ -148,7 +164,7 @@ DFLV_DEVINL void gdn_gram_tiles(const uint16_t* K_s, const uint16_t* Q_s, float*
                 const float dec = expf(g_s[i] - g_s[l]);
                 v = isM[t] ? dec * d[t][e] : beta_s[i] * dec * d[t][e];
             }
-            (isM[t] ? M_s : A_s)[i * NPT + l] = v;
+            (isM[t] ? M_s : A_s)[amat_at<NPT, RB>(i, l)] = v;
         }
     }
 }
@@ -451,7 +467,7 @@ __global__ void __launch_bounds__(kGdnThreads, (NPT == 32 && RB <= 32) ? 3 : 2)
     if (misc_s[1]) return;  // the state copy never landed (status already raised)
 
     if (warp < kHalfWarps) {
-        gdn_gram_tiles<DK, NPT>(K_s, Q_s, A_s, M_s, g_s, beta_s, amask_s, n, warp, gq, tq);
+        gdn_gram_tiles<DK, NPT, RB>(K_s, Q_s, A_s, M_s, g_s, beta_s, amask_s, n, warp, gq, tq);
     } else {
         // 3. cumulative log decay over the ancestors-or-self, by this half
         //    (which has slack: its state products end before the Gram tiles
@@ -467,85 +483,129 @@ __global__ void __launch_bounds__(kGdnThreads, (NPT == 32 && RB <= 32) ? 3 : 2)
             const float g = (acc[0] + acc[1]) + (acc[2] + acc[3]);
             g_s[i] = g;
             G_s[i] = expf(g);
+            if (blockIdx.x == 0) a.g[((size_t)b * N + i) * a.Hv + h] = g;
         }
         named_barrier_arrive(1, kGdnThreads);
+        // the factors kept once per (sequence, head) / (sequence, q/k head),
+        // written here, off the end of the launch: g above, the keys here
+        if (blockIdx.x == 0 && h % (a.Hv / a.Hk) == 0)
+            for (int idx = ht2; idx < n * CH; idx += kGdnThreads / 2) {
+                const int i = idx / CH, c = idx % CH;
+                *reinterpret_cast<uint4*>(a.kcopy + (((size_t)b * N + i) * a.Hk + hk) * DK + c * 8) =
+                    *reinterpret_cast<const uint4*>(K_s + i * KS + c * 8);
+            }
         // 6. S_0[rows] . [K | Q]
         gdn_state_products<DK, RB, NPT>(S_s, K_s, Q_s, R_s, SQ_s, warp - kHalfWarps, gq, tq);
     }
     __syncthreads();
 
-    // 7-9. Rows are independent: lane r of the first RB threads solves
-    //    u_i = R_i - sum_{l < i} A_il u_l,  R_i = beta_i (v_i - e^{g_i} S_0 k_i),
-    //    for all nodes in index order (a node's ancestors precede it) with
-    //    u in registers.  The outputs are o_i = e^{g_i} SQ_i + sum_{l <= i}
-    //    M_il u_l.  For trees of up to 32 nodes the solving lane forms each
-    //    output as soon as the u it needs are known: those products depend on
-    //    no later node, so they fill the gaps of the solve's dependence chain.
-    //    Larger trees have too many output products for RB lanes; there the u
-    //    go to shared memory and every thread of the block takes a share of
-    //    the outputs.  A and M are zero off the ancestors in every tile read,
-    //    so every trip count is fixed; their rows are read by all lanes at
-    //    once.
-    constexpr bool kFusedOut = NPT <= 32;
-    if (tid < RB) {
-        const int r = tid;
-        float u[NPT];
+    // 7-9. Rows are independent: with R_i = beta_i (v_i - e^{g_i} S_0 k_i),
+    //      u_i = R_i - sum_{l < i} A_il u_l   (a node's ancestors precede it),
+    //      o_i = e^{g_i} SQ_i + sum_{l <= i} M_il u_l.
+    //    A and M are zero off the ancestors, so every trip count is fixed.
+    if constexpr (NPT <= 32) {
+        // TPR threads per state row, each owning NPN nodes.  Column by
+        // column: once u_l is final (in the thread that owns node l) it is
+        // broadcast to the row's threads, and each subtracts A_il u_l from
+        // its later nodes and adds M_il u_l to their outputs.  The dependence
+        // chain per node is one shuffle and one FMA; the rest of a column's
+        // work is spread over all 256 threads.
+        constexpr int TPR = kGdnThreads / RB;
+        constexpr int NPN = NPT / TPR;
+        constexpr int VW = NPN >= 4 ? 4 : NPN;  // vector width of a column share
+        static_assert(TPR <= 32 && NPN % VW == 0 && (VW == 2 || VW == 4), "row threads within a warp");
+        const int r = tid / TPR, q = tid % TPR;
+        const int src0 = lane & ~(TPR - 1);
+        float x[NPN], o[NPN];  // R_i, then u_i; the output o_i
 #pragma unroll
-        for (int i = 0; i < NPT; ++i) u[i] = 0.f;
-        // Nodes go in chunks of 8 with no branch inside a chunk, so the loads
-        // of a chunk (rows of A, v, S_0 k) are scheduled ahead of the FMA
-        // chain.  Nodes n .. chunk end are set to zero and never stored: a
-        // valid node i reads u_l for l < 4 ceil(i/4) only, u_l with l > i is
-        // still zero when node i is solved, and M_il is zero for l > i.
+        for (int j = 0; j < NPN; ++j) {
+            const int i = q + TPR * j;
+            x[j] = 0.f;  // padded nodes keep u = 0
+            o[j] = 0.f;
+            if (i < n) {
+                x[j] = beta_s[i] * (bf16_bits_to_float(V_s[i * RB + r]) - G_s[i] * R_s[i * RB + r]);
+                o[j] = G_s[i] * SQ_s[i * RB + r];
+            }
+        }
+        const float* At = A_s + q * NPN;
+        const float* Mt = M_s + q * NPN;
 #pragma unroll
-        for (int c = 0; c < NPT / 8; ++c) {
-            if (8 * c < n) {
+        for (int l = 0; l < NPT; ++l) {
+            if (l >= n) break;  // u_l = 0 from here on
+            const int jl = l / TPR;  // a constant once unrolled
+            const float ul = __shfl_sync(0xffffffffu, x[jl], src0 | (l % TPR));
 #pragma unroll
-                for (int i = 8 * c; i < 8 * c + 8; ++i) {
-                    float acc[4] = {beta_s[i] * (bf16_bits_to_float(V_s[i * RB + r]) - G_s[i] * R_s[i * RB + r]),
-                                    0.f, 0.f, 0.f};
-                    const float4* Ar = reinterpret_cast<const float4*>(A_s + i * NPT);
-#pragma unroll
-                    for (int l4 = 0; l4 < (i + 3) / 4; ++l4) {
-                        const float4 w = Ar[l4];
-                        acc[0] = fmaf(-w.x, u[4 * l4], acc[0]);
-                        acc[1] = fmaf(-w.y, u[4 * l4 + 1], acc[1]);
-                        acc[2] = fmaf(-w.z, u[4 * l4 + 2], acc[2]);
-                        acc[3] = fmaf(-w.w, u[4 * l4 + 3], acc[3]);
-                    }
-                    // padded nodes keep u = 0: the output products below
-                    // read whole groups of four nodes
-                    u[i] = (i < n) ? (acc[0] + acc[1]) + (acc[2] + acc[3]) : 0.f;
+            for (int g = jl / VW; g < NPN / VW; ++g) {
+                float w[VW], m[VW];
+                if constexpr (VW == 4) {
+                    const float4 a4 = *reinterpret_cast<const float4*>(At + l * NPT + g * 4);
+                    const float4 m4 = *reinterpret_cast<const float4*>(Mt + l * NPT + g * 4);
+                    w[0] = a4.x, w[1] = a4.y, w[2] = a4.z, w[3] = a4.w;
+                    m[0] = m4.x, m[1] = m4.y, m[2] = m4.z, m[3] = m4.w;
+                } else {
+                    const float2 a2 = *reinterpret_cast<const float2*>(At + l * NPT + g * 2);
+                    const float2 m2 = *reinterpret_cast<const float2*>(Mt + l * NPT + g * 2);
+                    w[0] = a2.x, w[1] = a2.y;
+                    m[0] = m2.x, m[1] = m2.y;
                 }
 #pragma unroll
-                for (int i = 8 * c; i < 8 * c + 8; ++i) {
-                    if constexpr (kFusedOut) {
-                        const float4* Mr = reinterpret_cast<const float4*>(M_s + i * NPT);
-                        float acc0 = G_s[i] * SQ_s[i * RB + r], acc1 = 0.f;
-#pragma unroll
-                        for (int l4 = 0; l4 <= i / 4; ++l4) {
-                            const float4 w = Mr[l4];
-                            acc0 = fmaf(w.x, u[4 * l4], acc0);
-                            acc1 = fmaf(w.y, u[4 * l4 + 1], acc1);
-                            acc0 = fmaf(w.z, u[4 * l4 + 2], acc0);
-                            acc1 = fmaf(w.w, u[4 * l4 + 3], acc1);
-                        }
-                        if (i < n) {
-                            const size_t off = (((size_t)b * N + i) * a.Hv + h) * a.dv + r0 + r;
-                            a.u[off] = u[i];
-                            a.out[off] = acc0 + acc1;
-                        }
-                    } else if (i < n) {
-                        R_s[i * RB + r] = u[i];
+                for (int e = 0; e < VW; ++e) {
+                    const int j = g * VW + e;
+                    if (j >= jl) {  // earlier nodes of this thread are final
+                        x[j] = fmaf(-w[e], ul, x[j]);
+                        o[j] = fmaf(m[e], ul, o[j]);
                     }
                 }
             }
         }
-    }
-    if constexpr (!kFusedOut) {
+#pragma unroll
+        for (int j = 0; j < NPN; ++j) {
+            const int i = q + TPR * j;
+            if (i < n) {
+                const size_t off = (((size_t)b * N + i) * a.Hv + h) * a.dv + r0 + r;
+                a.u[off] = x[j];
+                a.out[off] = o[j];
+            }
+        }
+    } else {
+        // One lane per state row solves all nodes in index order with u in
+        // registers; then every thread of the block takes a share of the
+        // outputs.  Nodes go in chunks of 8 with no branch inside a chunk,
+        // so the loads of a chunk (rows of A, v, S_0 k) are scheduled ahead
+        // of the FMA chain.  Nodes n .. chunk end are set to zero and never
+        // stored: a valid node i reads u_l for l < 4 ceil(i/4) only, and u_l
+        // with l > i is still zero when node i is solved.
+        if (tid < RB) {
+            const int r = tid;
+            float u[NPT];
+#pragma unroll
+            for (int i = 0; i < NPT; ++i) u[i] = 0.f;
+#pragma unroll
+            for (int c = 0; c < NPT / 8; ++c) {
+                if (8 * c < n) {
+#pragma unroll
+                    for (int i = 8 * c; i < 8 * c + 8; ++i) {
+                        float acc[4] = {beta_s[i] * (bf16_bits_to_float(V_s[i * RB + r]) - G_s[i] * R_s[i * RB + r]),
+                                        0.f, 0.f, 0.f};
+                        const float4* Ar = reinterpret_cast<const float4*>(A_s + i * NPT);
+#pragma unroll
+                        for (int l4 = 0; l4 < (i + 3) / 4; ++l4) {
+                            const float4 w = Ar[l4];
+                            acc[0] = fmaf(-w.x, u[4 * l4], acc[0]);
+                            acc[1] = fmaf(-w.y, u[4 * l4 + 1], acc[1]);
+                            acc[2] = fmaf(-w.z, u[4 * l4 + 2], acc[2]);
+                            acc[3] = fmaf(-w.w, u[4 * l4 + 3], acc[3]);
+                        }
+                        u[i] = (i < n) ? (acc[0] + acc[1]) + (acc[2] + acc[3]) : 0.f;
+                    }
+#pragma unroll
+                    for (int i = 8 * c; i < 8 * c + 8; ++i)
+                        if (i < n) R_s[i * RB + r] = u[i];
+                }
+            }
+        }
         __syncthreads();
-        // o_i = e^{g_i} SQ_i + sum_{l <= i} M_il u_l over all threads; rows of
-        // R_s past n hold S_0 k (finite) and meet zero entries of M
+        // rows of R_s past n hold S_0 k (finite) and meet zero entries of M
         for (int idx = tid; idx < n * RB; idx += kGdnThreads) {
             const int i = idx / RB, r = idx % RB;
             const float4* Mr = reinterpret_cast<const float4*>(M_s + i * NPT);
@@ -564,16 +624,6 @@ __global__ void __launch_bounds__(kGdnThreads, (NPT == 32 && RB <= 32) ? 3 : 2)
         }
     }
 
-    // 10. The remaining factors, once per (sequence, head) / (sequence, q/k head).
-    if (blockIdx.x == 0) {
-        for (int i = tid; i < n; i += kGdnThreads) a.g[((size_t)b * N + i) * a.Hv + h] = g_s[i];
-        if (h % (a.Hv / a.Hk) == 0)
-            for (int idx = tid; idx < n * CH; idx += kGdnThreads) {
-                const int i = idx / CH, c = idx % CH;
-                *reinterpret_cast<uint4*>(a.kcopy + (((size_t)b * N + i) * a.Hk + hk) * DK + c * 8) =
-                    *reinterpret_cast<const uint4*>(K_s + i * KS + c * 8);
-            }
-    }
 }
 
 template <int DK, int RB, int NPT>

@@ -95,6 +95,59 @@ def test_accept_ties(dflv, orc):
     assert np.array_equal(best, rb) and nxt[0] == rn[0] == 7
 
 
+def test_accept_ties_across_ctas(dflv, orc):
+    """Equal maxima in different CTAs' shares of one row: the lowest index
+    wins wherever the split falls (a 22-node tree over 151,936 splits every
+    row 16 ways, 9,496 entries each); plus a row whose only maximum is the
+    last vocabulary entry."""
+    V, N = 151936, 22
+    rng = np.random.default_rng(17)
+    parent = np.array([[-1] + list(range(N - 1))], np.int32)
+    tokens = np.zeros((1, N), np.int32)
+    logits = synth.random_logits(rng, 1, N, V)
+    top = float(logits.max()) + 1.0
+    logits[0, 0, [9495, 9496, V - 1]] = top
+    logits[0, 1, [9496 * 5, 9496 * 5 - 1, 9496 * 11]] = top
+    logits[0, 2, [V - 1]] = top
+    logits[0, 3, [0, V - 1]] = top
+    logits[0, 4, [9496 * 15, V - 4]] = top
+    path, plen, nxt, best = gpu_accept(dflv, logits, tokens, parent, np.array([N], np.int32))
+    rp, rl, rn, rb = orc.accept_greedy(logits, tokens, parent, np.array([N], np.int32))
+    assert list(rb[0, :5]) == [9495, 9496 * 5 - 1, V - 1, 0, 9496 * 15]
+    assert np.array_equal(best, rb) and plen[0] == rl[0] and nxt[0] == rn[0]
+
+
+def test_accept_batch8_n64(dflv, orc):
+    """Eight 64-node trees over the full vocabulary: one CTA per row, several
+    load batches per thread; paths planted in every sequence."""
+    V, B = 151936, 8
+    rng = np.random.default_rng(64)
+    parent, n_nodes, tokens, parents = _trees(rng, [64, 64, 63, 64, 40, 64, 64, 1], V)
+    logits = synth.random_logits(rng, B, parent.shape[1], V)
+    for b, p in enumerate(parents):
+        synth.plant_path(logits, tokens, synth.deepest_path(p), b)
+    path, plen, nxt, best = gpu_accept(dflv, logits, tokens, parent, n_nodes)
+    rp, rl, rn, rb = orc.accept_greedy(logits, tokens, parent, n_nodes)
+    for b in range(B):
+        assert plen[b] == rl[b] and nxt[b] == rn[b]
+        assert np.array_equal(path[b, : rl[b]], rp[b, : rl[b]])
+        assert np.array_equal(best[b, : n_nodes[b]], rb[b, : n_nodes[b]])
+
+
+def test_accept_bad_topology_sets_status(dflv):
+    """A parent that does not precede its child, and a node count past N_max,
+    raise the topology bit; those sequences get path_len 0, the valid one is
+    walked."""
+    V, N = 4096, 6
+    rng = np.random.default_rng(5)
+    parent = np.array([[-1, 0, 0, 1, 2, 3], [-1, 0, 3, 1, 2, 3], [-1, 0, 1, 2, 3, 4]], np.int32)
+    n_nodes = np.array([6, 6, 7], np.int32)
+    tokens = np.zeros((3, N), np.int32)
+    logits = synth.random_logits(rng, 3, N, V)
+    path, plen, nxt, best = gpu_accept(dflv, logits, tokens, parent, n_nodes, expect_status=dflv.DFLV_DEV_TOPOLOGY)
+    assert plen[0] >= 1 and plen[1] == 0 and plen[2] == 0
+
+
 def test_accept_nan_logits(dflv, orc):
     """A NaN logit counts as -inf on both sides: rows with NaN before, after
     and instead of the maximum, an all-NaN row and a NaN/-inf row, at a
