@@ -863,18 +863,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
             // the lanes of valid rows store
             const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
 #pragma unroll 1
-            for (int c0o = 0; c0o < D; c0o += 32) {
-                float o[32];
-                tc::ld32(tmem_O + lane_off + c0o, o);
+            for (int c0o = 0; c0o < D; c0o += 64) {
+                // two loads in flight before one wait
+                uint32_t o[2][32];
+                tc::ld32_nowait(tmem_O + lane_off + c0o, o[0]);
+                tc::ld32_nowait(tmem_O + lane_off + c0o + 32, o[1]);
+                tc::wait_ld();
                 if (valid) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        if (gmerge)
-                            *reinterpret_cast<float4*>(Rcv + (size_t)r * OS + c0o + e) =
-                                make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
-                        else
-                            st_dsmem_f4(dst + (uint32_t)(c0o + e) * 4, o[e], o[e + 1], o[e + 2], o[e + 3]);
-                    }
+                    for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4) {
+                            const float4 v4 = make_float4(__uint_as_float(o[h2][e]), __uint_as_float(o[h2][e + 1]),
+                                                          __uint_as_float(o[h2][e + 2]), __uint_as_float(o[h2][e + 3]));
+                            const int cc = c0o + 32 * h2 + e;
+                            if (gmerge)
+                                *reinterpret_cast<float4*>(Rcv + (size_t)r * OS + cc) = v4;
+                            else
+                                st_dsmem_f4(dst + (uint32_t)cc * 4, v4.x, v4.y, v4.z, v4.w);
+                        }
                 }
             }
         }
@@ -961,60 +968,51 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
         return;
     }
     if (gmerge) {
-        // an item is half of an owned row (D / 2 dims, D / 64 per lane);
-        // every peer's partial of it is requested at once (CS <= 16), then
-        // merged in peer order
-        constexpr int HL = D / 64;  // floats per lane
-        const int n_own = (rank < rows_here) ? (rows_here - 1 - rank) / CS + 1 : 0;
-        for (int item = warp; item < 2 * n_own; item += nwarps) {
-            const int slot = item >> 1, half = item & 1;
-            const int r = rank + slot * CS, rho = row0 + r;
-            const int c0 = half * (D / 2) + lane * HL;
+        // The row tile's outputs are cut into items of four consecutive
+        // floats of a row, and the cluster's CTAs take consecutive ranges
+        // of them (one item per thread at the usual shapes), so every CTA
+        // merges about the same amount and each thread issues all of its
+        // peers' loads at once: one round trip to the L2.  Peers are merged
+        // in rank order.
+        constexpr int NCH = D / 4;
+        const int items = rows_here * NCH;
+        const int per = (items + CS - 1) / CS;
+        const int it0 = rank * per, it1 = min(items, it0 + per);
+        for (int item = it0 + tid; item < it1; item += kThreads) {
+            const int r = item / NCH, c0 = (item % NCH) * 4, rho = row0 + r;
             float2 ml[16];
-            float ov[16][HL];
+            float4 ov[16];
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
                 ml[q] = make_float2(-INFINITY, 0.f);
-#pragma unroll
-                for (int e = 0; e < HL; ++e) ov[q][e] = 0.f;
+                ov[q] = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (q < CS) {
                     const float* src = wsb + ((size_t)q * RT + r) * OS;
+                    ov[q] = __ldcg(reinterpret_cast<const float4*>(src + c0));
                     ml[q] = __ldcg(reinterpret_cast<const float2*>(src + D));
-                    if constexpr (HL == 4) {
-                        const float4 x = __ldcg(reinterpret_cast<const float4*>(src + c0));
-                        ov[q][0] = x.x;
-                        ov[q][1] = x.y;
-                        ov[q][2] = x.z;
-                        ov[q][3] = x.w;
-                    } else {
-                        const float2 x = __ldcg(reinterpret_cast<const float2*>(src + c0));
-                        ov[q][0] = x.x;
-                        ov[q][1] = x.y;
-                    }
                 }
             }
             float M = -INFINITY;
 #pragma unroll
             for (int q = 0; q < 16; ++q) M = fmaxf(M, ml[q].x);
             const float bse = (M == -INFINITY) ? 0.f : M;
-            float Lt = 0.f, acc[HL];
-#pragma unroll
-            for (int e = 0; e < HL; ++e) acc[e] = 0.f;
+            float Lt = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
                 // absent peers and peers without keys for this row: max -inf, weight 0
                 const float w = (ml[q].x == -INFINITY) ? 0.f : exp2f(ml[q].x - bse);
                 Lt = fmaf(w, ml[q].y, Lt);
-#pragma unroll
-                for (int e = 0; e < HL; ++e) acc[e] = (w == 0.f) ? acc[e] : fmaf(w, ov[q][e], acc[e]);
+                if (w != 0.f) {
+                    acc[0] = fmaf(w, ov[q].x, acc[0]);
+                    acc[1] = fmaf(w, ov[q].y, acc[1]);
+                    acc[2] = fmaf(w, ov[q].z, acc[2]);
+                    acc[3] = fmaf(w, ov[q].w, acc[3]);
+                }
             }
             const float inv = 1.f / Lt;
             const int i = rho / G, gh = rho % G;
             float* dsto = a.out + (((size_t)b * N + i) * a.Hq + kvh * G + gh) * D + c0;
-            if constexpr (HL == 4)
-                *reinterpret_cast<float4*>(dsto) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
-            else
-                *reinterpret_cast<float2*>(dsto) = make_float2(acc[0] * inv, acc[1] * inv);
+            *reinterpret_cast<float4*>(dsto) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
         }
         return;
     }
