@@ -849,48 +849,77 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
                               (((size_t)b * a.Hkv + kvh) * (gridDim.y / a.Hkv) + rt) * CS * RT * OS
                         : nullptr;
     const int rows_here = min(RT, rows_valid - row0);  // rows 0 .. rows_here-1 are valid
-    if (!gmerge) cluster_sync_all();
-    if (warp < kSoftWarps) {
-        const int r = tid;
-        const bool valid = r < rows_here;
-        const int owner = valid ? r % CS : 0, slot = valid ? r / CS : 0;
-        const uint32_t dst =
-            gmerge ? smem_u32(Rcv + (size_t)r * OS)
-                   : map_to_rank(smem_u32(Rcv + (size_t)(slot * CS + rank) * OS), (uint32_t)owner);
-        const bool have_o = T > 0 && !any_fail;  // uniform over the CTA
-        if (have_o) {
-            // the TMEM loads are warp-collective: every lane loads, only
-            // the lanes of valid rows store
-            const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const bool have_o = T > 0 && !any_fail;  // uniform over the CTA
+    if (gmerge) {
+        // Staged row-major in this CTA's shared memory (slot r: O in
+        // [0, D), max at D, sum at D + 1) by eight warps -- the softmax
+        // warps take O's first D/2 columns, the stage warps the same TMEM
+        // lanes' other half -- then written out by one bulk copy per 32-row
+        // quarter, issued by four threads at once.
+        if (warp < kMmaWarp) {
+            const int r = (warp & 3) * 32 + lane;
+            const bool valid = r < rows_here;
+            bool ok_o = have_o;
+            if (have_o && warp >= kSoftWarps) {
+                // the stage warps have not seen the last products complete
+                ok_o = __all_sync(0xffffffffu,
+                                  wait_phase(bars + kODone0 + ((T - 1) & 1), ((T - 1) >> 1) & 1));
+                tc::fence_after_sync();
+            }
+            if (ok_o) {
+                // the TMEM loads are warp-collective: every lane loads, only
+                // the lanes of valid rows store
+                const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+                const int cb = warp < kSoftWarps ? 0 : D / 2;
 #pragma unroll 1
-            for (int c0o = 0; c0o < D; c0o += 64) {
-                // two loads in flight before one wait
-                uint32_t o[2][32];
-                tc::ld32_nowait(tmem_O + lane_off + c0o, o[0]);
-                tc::ld32_nowait(tmem_O + lane_off + c0o + 32, o[1]);
-                tc::wait_ld();
-                if (valid) {
+                for (int c0o = cb; c0o < cb + D / 2; c0o += 32) {
+                    float o[32];
+                    tc::ld32(tmem_O + lane_off + c0o, o);
+                    if (valid) {
 #pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2)
+                        for (int e = 0; e < 32; e += 4)
+                            *reinterpret_cast<float4*>(Rcv + (size_t)r * OS + c0o + e) =
+                                make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+                    }
+                }
+            } else if (have_o && lane == 0) {
+                raise_status(a.status, DFLV_DEV_TIMEOUT);  // this CTA's O is not staged
+            }
+            if (warp < kSoftWarps && valid)
+                *reinterpret_cast<float2*>(Rcv + (size_t)r * OS + D) =
+                    make_float2(have_o ? m_run : -INFINITY, have_o ? l_run : 0.f);
+            fence_proxy_async_smem();  // the staged rows go out through the bulk-copy engine
+        }
+    } else {
+        // into the owners' shared memory (the tile buffers), once every CTA
+        // has left its loop
+        cluster_sync_all();
+        if (warp < kSoftWarps) {
+            const int r = tid;
+            const bool valid = r < rows_here;
+            const int owner = valid ? r % CS : 0, slot = valid ? r / CS : 0;
+            const uint32_t dst = map_to_rank(smem_u32(Rcv + (size_t)(slot * CS + rank) * OS), (uint32_t)owner);
+            if (have_o) {
+                const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+#pragma unroll 1
+                for (int c0o = 0; c0o < D; c0o += 64) {
+                    uint32_t o[2][32];  // two loads in flight before one wait
+                    tc::ld32_nowait(tmem_O + lane_off + c0o, o[0]);
+                    tc::ld32_nowait(tmem_O + lane_off + c0o + 32, o[1]);
+                    tc::wait_ld();
+                    if (valid) {
 #pragma unroll
-                        for (int e = 0; e < 32; e += 4) {
-                            const float4 v4 = make_float4(__uint_as_float(o[h2][e]), __uint_as_float(o[h2][e + 1]),
-                                                          __uint_as_float(o[h2][e + 2]), __uint_as_float(o[h2][e + 3]));
-                            const int cc = c0o + 32 * h2 + e;
-                            if (gmerge)
-                                *reinterpret_cast<float4*>(Rcv + (size_t)r * OS + cc) = v4;
-                            else
-                                st_dsmem_f4(dst + (uint32_t)cc * 4, v4.x, v4.y, v4.z, v4.w);
-                        }
+                        for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+                            for (int e = 0; e < 32; e += 4)
+                                st_dsmem_f4(dst + (uint32_t)(c0o + 32 * h2 + e) * 4, __uint_as_float(o[h2][e]),
+                                            __uint_as_float(o[h2][e + 1]), __uint_as_float(o[h2][e + 2]),
+                                            __uint_as_float(o[h2][e + 3]));
+                    }
                 }
             }
+            if (valid) st_dsmem_f2(dst + (uint32_t)D * 4, have_o ? m_run : -INFINITY, have_o ? l_run : 0.f);
         }
-        if (valid) {
-            const float mv = have_o ? m_run : -INFINITY, lv = have_o ? l_run : 0.f;
-            if (gmerge) *reinterpret_cast<float2*>(Rcv + (size_t)r * OS + D) = make_float2(mv, lv);
-            else st_dsmem_f2(dst + (uint32_t)D * 4, mv, lv);
-        }
-        if (gmerge) fence_proxy_async_smem();  // the staged rows go out through the bulk-copy engine
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -898,8 +927,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
         tc::fence_after_sync();
         tc::dealloc(tmem, L::kTmemCols);
     }
-    if (gmerge && tid == 0 && rows_here > 0) {
-        bulk_s2g(wsb + (size_t)rank * RT * OS, Rcv, (uint32_t)(rows_here * OS * 4));
+    if (gmerge && lane == 0 && warp < kSoftWarps && 32 * warp < rows_here) {
+        const int nr = min(32, rows_here - 32 * warp);
+        bulk_s2g(wsb + ((size_t)rank * RT + 32 * warp) * OS, Rcv + (size_t)32 * warp * OS, (uint32_t)(nr * OS * 4));
         bulk_s2g_wait();
     }
     cluster_sync_all();  // every partial is visible to its owner
