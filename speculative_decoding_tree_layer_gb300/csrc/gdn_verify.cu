@@ -75,15 +75,15 @@ DFLV_DEVINL void named_barrier_arrive(int id, int count) {
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-// Where A_il and M_il sit in shared memory.  Trees of up to 32 nodes are
-// solved by every thread of the block, TPR = 256 / RB threads per state row,
-// thread q of a row owning nodes q, q + TPR, q + 2 TPR, ...: there both
-// matrices are stored by column l, with each thread's nodes contiguous, so
-// a thread reads its share of a column with vector loads.  Larger trees
-// keep row-major [i][l].
+// Where A_il and M_il sit in shared memory.  Trees of up to 32 nodes, and
+// larger ones with 64-row blocks, are solved by every thread of the block,
+// TPR = 256 / RB threads per state row, thread q of a row owning nodes q,
+// q + TPR, q + 2 TPR, ...: there both matrices are stored by column l, with
+// each thread's nodes contiguous, so a thread reads its share of a column
+// with vector loads.  The remaining shapes keep row-major [i][l].
 template <int NPT, int RB>
 DFLV_DEVINL int amat_at(int i, int l) {
-    if constexpr (NPT <= 32) {
+    if constexpr (NPT <= 32 || RB == 64) {
         constexpr int TPR = kGdnThreads / RB, NPN = NPT / TPR;
         return l * NPT + (i % TPR) * NPN + i / TPR;
     } else {
@@ -503,7 +503,7 @@ __global__ void __launch_bounds__(kGdnThreads, (NPT == 32 && RB <= 32) ? 3 : 2)
     //      u_i = R_i - sum_{l < i} A_il u_l   (a node's ancestors precede it),
     //      o_i = e^{g_i} SQ_i + sum_{l <= i} M_il u_l.
     //    A and M are zero off the ancestors, so every trip count is fixed.
-    if constexpr (NPT <= 32) {
+    if constexpr (NPT <= 32 || RB == 64) {
         // TPR threads per state row, each owning NPN nodes.  Column by
         // column: once u_l is final (in the thread that owns node l) it is
         // broadcast to the row's threads, and each subtracts A_il u_l from
