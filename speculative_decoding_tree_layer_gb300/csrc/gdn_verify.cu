@@ -24,9 +24,11 @@
 // only) and apply the decays and the ancestor mask, giving dense
 // lower-triangular A and M; the other half form S_0[rows] . [K | Q] on the
 // tensor cores (fp32 state split into bf16 hi + lo, k and q exact in bf16).
-// Then one lane per row solves the unit lower-triangular system for u with
-// the node values in registers (nodes in index order: parent[i] < i), and
-// all warps mix the outputs.  The node count is padded to a compile-time
+// Then the unit lower-triangular system for u is solved in node order
+// (parent[i] < i) by all threads, several per state row, column by column
+// with each u broadcast by a warp shuffle, and the outputs are mixed in the
+// same pass (one lane per row and a separate output pass for blocks of
+// fewer than 64 rows with trees over 32 nodes).  The node count is padded to a compile-time
 // NPT (32 or 64) so every loop has a fixed trip count and the tensor-core
 // fragments of a step are loaded together.  With early prefetch the state
 // rows and the tree are fetched before the kernel waits for its predecessor.
