@@ -277,7 +277,9 @@ class GpuStep:
         cap = host["cap"]
         N = BUDGET
         self.ctx = host["ctx"]
-        # ---- per-step inputs: one packed pinned host buffer and its device twin
+        # ---- per-step inputs: one packed pinned host buffer and two device
+        #      twins (the step of factor-set parity p reads twin p, so the next
+        #      step's inputs can be copied in while a step runs)
         offs, total = {}, 0
         for name, a in step_inputs(host):
             total = (total + 255) // 256 * 256
@@ -286,14 +288,20 @@ class GpuStep:
         self.offs = offs
         self.in_bytes = total
         self.h_in = t.empty(total, dtype=t.uint8, pin_memory=True)
-        self.d_in = t.empty(total, dtype=t.uint8, device=dev)
+        self.d_ins = [t.empty(total, dtype=t.uint8, device=dev) for _ in range(2)]
         self.load_inputs(host)
 
-        def view(name):
+        def view_of(buf, name):
             o, a = offs[name]
             tdt = {np.dtype(np.uint16): t.int16, np.dtype(np.float32): t.float32,
                    np.dtype(np.int32): t.int32}[a.dtype]
-            return self.d_in[o:o + a.nbytes].view(tdt).view(*a.shape)
+            return buf[o:o + a.nbytes].view(tdt).view(*a.shape)
+
+        self._view_of = view_of
+        self.bound = 0
+
+        def view(name):
+            return view_of(self.d_ins[0], name)
 
         self.parent, self.n_nodes, self.tokens, self.logits = (view("parent"), view("n_nodes"), view("tokens"),
                                                                view("logits"))
@@ -364,13 +372,24 @@ class GpuStep:
 
     def load_inputs(self, host):
         """Packs a host input set of the same shapes into the pinned buffer
-        and copies it to the device buffer the captured step reads."""
+        and copies it to both device buffers the captured steps read."""
         hv = self.h_in.numpy()
         for name, a in step_inputs(host):
             o, a0 = self.offs[name]
             assert a.shape == a0.shape and a.dtype == a0.dtype, name
             hv[o:o + a.nbytes] = a.view(np.uint8).reshape(-1)
-        self.d_in.copy_(self.h_in)
+        for d in self.d_ins:
+            d.copy_(self.h_in)
+
+    def bind(self, which):
+        """Points every per-step input of the calls at device buffer `which`."""
+        v = lambda name: self._view_of(self.d_ins[which], name)
+        self.parent, self.n_nodes, self.tokens, self.logits = v("parent"), v("n_nodes"), v("tokens"), v("logits")
+        for li, L in enumerate(self.layers):
+            keys = ("q", "k", "v", "beta", "log_alpha") if L["kind"] == "gdn" else ("q", "k_new", "v_new")
+            for key in keys:
+                L[key] = v(f"{li}.{key}")
+        self.bound = which
 
     # one pass of the hot path: every layer's verify (the GDN layers first
     # commit the previous step's accepted path into their state: deferred
@@ -716,8 +735,10 @@ def capture_step(S, torch, stream):
     torch.cuda.synchronize()
     graphs = [torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()]
     for par in range(2):
+        S.bind(par)  # the step of parity par reads input buffer par
         with torch.cuda.graph(graphs[par], stream=stream):
             S.step(par)
+    S.bind(0)
     torch.cuda.synchronize()
     assert int(S.status.item()) == 0, f"device status {int(S.status.item())}"
     return graphs
@@ -817,41 +838,41 @@ def run_gpu(args, rank, world):
     scale = scale_measure(torch, dflv, flush) if not args.no_scale else {}
     del flush
     # ---- end to end: pinned host inputs -> device, step, result -> host, every
-    #      step, through the same captured C-ABI calls.  Step t+1's inputs are
-    #      copied on a second stream into a device staging buffer while step t
-    #      runs (the copy engines work beside the SMs); each step then moves
-    #      them into the buffer its captured calls read (a device-to-device
-    #      copy).  The accepted path goes to one of two pinned host slots; the
-    #      host reads step t's path once step t+1 is enqueued, so its wait
-    #      overlaps the next step (the path feeds the host's output, not the
-    #      next step's inputs, which the device produces), and the last
-    #      step's path is read inside the timed region.
+    #      step, through the same captured C-ABI calls.  The step of parity p
+    #      reads device input buffer p, so step t+1's inputs are copied on a
+    #      second stream straight into its buffer while step t runs (the copy
+    #      engines work beside the SMs), once step t-1 has finished reading
+    #      that buffer.  The accepted path goes to one of two pinned host
+    #      slots; the host reads step t's path once step t+1 is enqueued, so
+    #      its wait overlaps the next step (the path feeds the host's output,
+    #      not the next step's inputs, which the device produces), and the
+    #      last step's path is read inside the timed region.
     S.reset()
     count[0] = 0
-    d_stage = torch.empty_like(S.d_in)
     copy_stream = torch.cuda.Stream()
-    copied = torch.cuda.Event()
-    consumed = torch.cuda.Event()
+    copied = [torch.cuda.Event(), torch.cuda.Event()]
+    read_done = [torch.cuda.Event(), torch.cuda.Event()]
     result = [torch.cuda.Event(), torch.cuda.Event()]
     torch.cuda.synchronize()
 
     def e2e_steps(n):
+        t0 = count[0]  # replay() alternates the parity from here
         with torch.cuda.stream(copy_stream):
-            d_stage.copy_(S.h_in, non_blocking=True)
-            copied.record(copy_stream)
+            S.d_ins[t0 % 2].copy_(S.h_in, non_blocking=True)
+            copied[t0 % 2].record(copy_stream)
         for t in range(n):
-            with torch.cuda.stream(stream):
-                stream.wait_event(copied)
-                S.d_in.copy_(d_stage, non_blocking=True)
-                consumed.record(stream)
+            par = (t0 + t) % 2
             if t + 1 < n:
                 with torch.cuda.stream(copy_stream):
-                    copy_stream.wait_event(consumed)
-                    d_stage.copy_(S.h_in, non_blocking=True)   # the next step's inputs
-                    copied.record(copy_stream)
+                    if t >= 1:
+                        copy_stream.wait_event(read_done[1 - par])  # step t-1 read that buffer
+                    S.d_ins[1 - par].copy_(S.h_in, non_blocking=True)   # the next step's inputs
+                    copied[1 - par].record(copy_stream)
             slot = S.h_out[t % 2]
             with torch.cuda.stream(stream):
+                stream.wait_event(copied[par])
                 replay()
+                read_done[par].record(stream)
                 slot[: BUDGET].copy_(S.path[0], non_blocking=True)
                 slot[BUDGET].copy_(S.path_len[0], non_blocking=True)
                 slot[BUDGET + 1].copy_(S.next_token[0], non_blocking=True)
@@ -1176,11 +1197,12 @@ def main():
                                     "of the step",
                             **beside},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
-                "how": "every step: the step's inputs from pinned host memory (copied on a second stream while the "
-                       "previous step runs, then moved into the captured calls' input buffer), one replay of the "
-                       "captured C-ABI calls of the step, the accepted path copied to pinned host memory; the host "
-                       "reads step t's path once step t+1 is enqueued (two host slots), and the last step's path "
-                       "inside the timed region"},
+                "how": "every step: the step's inputs from pinned host memory, copied on a second stream while "
+                       "the previous step runs straight into the device buffer its captured calls read (two "
+                       "buffers, one captured graph per step parity), one replay of the captured C-ABI calls of "
+                       "the step, the accepted path copied to pinned host memory; the host reads step t's path "
+                       "once step t+1 is enqueued (two host slots), and the last step's path inside the timed "
+                       "region"},
         "gpu_launches": r["launches"] * args.steps,
         "clocks": r["clocks"],
     }
