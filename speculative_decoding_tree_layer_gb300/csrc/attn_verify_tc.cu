@@ -22,19 +22,22 @@
 //     with the block scale folded in (d * code is exact in fp32; hi =
 //     fp16(x), lo = fp16(x - hi)).  K and V tiles are double-buffered;
 //   * the MMA warp (1) issues tcgen05.mma: [S_hi | S_lo] = Q [K_hi ; K_lo]^T
-//     into one of two S buffers in tensor memory (M = 128, N = 64, K = head
-//     size), and O += P_hi V_hi + P_hi V_lo + P_lo V_hi with O resident in
-//     tensor memory.  Q and P are read from tensor memory, so the tensor
-//     core's shared-memory reads are only the K and V tiles;
+//     into the S buffer in tensor memory (M = 128, N = 64, K = head size),
+//     and O += P_hi V_hi + P_hi V_lo + P_lo V_hi with O resident in tensor
+//     memory.  Q and P are read from tensor memory, so the tensor core's
+//     shared-memory reads are only the K and V tiles.  Per tile t it issues
+//     tile t+1's scores as soon as the softmax has read tile t's, then tile
+//     t's products once P is written (two P buffers);
 //   * softmax warps (4): one thread per query row (its TMEM lane) writes the
 //     row's query into tensor memory once, then per tile reads the 32
 //     scores, applies the tree / window mask and an fp32 online softmax with
 //     a lazily updated running max (O is rescaled in tensor memory only when
-//     a row's max grows by more than 2^8), and writes P as fp16 hi + lo over
-//     the scores it has read.
-// Partial (max, sum, O) are merged across the cluster through distributed
-// shared memory.  Operands use the no-swizzle core-matrix layout described
-// in tcgen05.cuh.
+//     a row's max grows by more than 2^8), and writes P as fp16 hi + lo.
+// Partial (max, sum, O) are merged across the cluster: with a caller's
+// workspace through global memory (each CTA writes its rows' partials, one
+// cluster barrier, then every CTA merges an even share of the outputs), else
+// through distributed shared memory.  Operands use the no-swizzle
+// core-matrix layout described in tcgen05.cuh.
 #include <climits>
 
 #include "attn_common.cuh"
