@@ -322,17 +322,17 @@ template <int D, int TYPE>
 DFLV_DEVINL void issue_raw(const uint8_t* plane_codes, const uint16_t* plane_scales, size_t row0, int start,
                            int count, uint8_t* raw, uint64_t* bar, int st) {
     using L = PlaneFmt<D, TYPE>;
-    constexpr int CPR = L::KB / 16;  // 16-byte chunks per key row
-    for (int idx = st; idx < count * CPR; idx += 32) {
-        const int c = idx / CPR, ch = idx % CPR;
-        cp_async16(raw + c * L::RSK + ch * 16, plane_codes + (row0 + start + c) * L::KB + ch * 16);
-    }
+    // bulk copies (TMA engine): one per key row (into the padded row
+    // stride) by the warp's lanes, one for the scales; the barrier expects
+    // the warp's 32 arrivals and the bytes
     const uintptr_t sa = reinterpret_cast<uintptr_t>(plane_scales + (row0 + start) * L::NB);
     const int shift = (int)(sa & 15);
-    const int schunks = (shift + count * L::NB * 2 + 15) >> 4;
-    for (int idx = st; idx < schunks; idx += 32)
-        cp_async16(raw + L::kRawCodes + idx * 16, reinterpret_cast<const void*>(sa - shift + idx * 16));
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+    const uint32_t sbytes = (uint32_t)((shift + count * L::NB * 2 + 15) >> 4) * 16;
+    if (st == 0) mbar_arrive_expect_tx(bar, (uint32_t)(count * L::KB) + sbytes);
+    else mbar_arrive(bar);
+    for (int c = st; c < count; c += 32)
+        bulk_g2s(raw + c * L::RSK, plane_codes + (row0 + start + c) * L::KB, L::KB, bar);
+    if (st == 0) bulk_g2s(raw + L::kRawCodes, reinterpret_cast<const void*>(sa - shift), sbytes, bar);
 }
 
 // barrier over `count` threads (whole warps) under id
@@ -582,6 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
         }
         __threadfence();
         fence_proxy_async_smem();
+        asm volatile("fence.proxy.async.global;\n" ::: "memory");  // the tree rows are read back by bulk copies
         named_barrier_sync_n(kPrepBarrier, kPrepThreads);
     }
 
@@ -764,13 +765,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
         // One warp per plane, so a K request never waits behind a V buffer.
         const bool kside = warp == kLoadWarp;
         bool ok = true;
+        asm volatile("fence.proxy.async.global;\n" ::: "memory");
+        int issued = min(T, 2);  // tiles requested so far (the first two before the loop, tree tiles below)
         for (int u = 0; u < T && ok; ++u) {
             if (u < 2 && !tile(u).tree) continue;  // requested before the loop
             if (u >= 2) ok = wait_phase(bars + (kside ? kKFree0 : kVFree0) + (u & 1), ((u - 2) >> 1) & 1);
-            if (ok) issue_tile_raw(u, kside, !kside);
+            if (ok) {
+                issue_tile_raw(u, kside, !kside);
+                issued = max(issued, u + 1);
+            }
         }
         if (!__all_sync(0xffffffffu, ok) && lane == 0) atomicOr(fail_s, 1);
-        cp_async_wait<0>();  // this lane's copies have landed before the CTA moves on
+        // the last bulk copies into this plane's buffers have landed before
+        // the CTA moves on (the stage warps have normally seen them already)
+        for (int u = max(0, issued - 2); u < issued; ++u)
+            wait_phase(bars + (kside ? kRawK0 : kRawV0) + (u & 1), (u >> 1) & 1);
     } else if (lane == 0) {
         // ================================================ MMA issue (one thread)
         constexpr uint32_t SBO = (D / 8) * 128;
