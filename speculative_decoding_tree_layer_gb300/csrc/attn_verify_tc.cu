@@ -14,8 +14,8 @@
 // or two extra tiles.  Inside a CTA the tiles flow through a pipeline of
 // warp roles that hand over through mbarriers (every wait bounded):
 //   * load warps (2, one per plane): the raw codes and scales of each tile
-//     by 16-byte cp.async into double buffers, completion counted on an
-//     mbarrier; the first two tiles are requested before the kernel waits
+//     by bulk copies (TMA engine) into double buffers, completion counted in
+//     bytes on an mbarrier; the first two tiles are requested before the kernel waits
 //     for its predecessor when early prefetch is on.  The CTA that attends
 //     to a tree tile first quantises the tree's rows into the cache;
 //   * stage warps (4): each raw tile is expanded into fp16 hi + lo tiles
@@ -306,12 +306,11 @@ DFLV_DEVINL void stage_hilo(const uint8_t* __restrict__ codes, const uint16_t* _
     }
 }
 
-// Request one raw plane (codes + scales) of a cache tile with 16-byte
-// cp.async copies spread over the 32 lanes of the load warp; each lane then
-// arrives on bar (initialised for 32 arrivals) once its own copies have
-// landed.  The
-// scales are copied from the 16-byte boundary at or below the first one
-// (their byte offset in the buffer is returned by scale_shift).
+// One raw plane (codes + scales) of a cache tile is requested by the 32 lanes
+// of a load warp with bulk copies (see issue_raw); bar is initialised for
+// 32 arrivals and the copied bytes.  The scales are copied from the 16-byte
+// boundary at or below the first one (their byte offset in the buffer is
+// returned by scale_shift).
 template <int D, int TYPE>
 DFLV_DEVINL int scale_shift(const uint16_t* plane_scales, size_t row0, int start) {
     using L = PlaneFmt<D, TYPE>;
