@@ -421,6 +421,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
         ti.count = ti.tree ? min(kTK, P + n - ti.start) : min(kTK, P - ti.start);
         return ti;
     };
+    // With early prefetch the layer inputs this CTA reads after the
+    // dependency wait -- its query rows and, where it quantises tree rows,
+    // their new keys and values -- are first asked for in the L2 (in a model
+    // the layer before has just written them there); the loads after the
+    // wait read whatever the lines hold by then.
+    if (early) {
+        const int nq = min(RT, rows_valid - row0);
+        const int t_lo = max(0, g0 - n_cache_tiles) * kTK, t_hi = min(n, (g0 + T - n_cache_tiles) * kTK);
+        const int nt = t_hi > t_lo ? t_hi - t_lo : 0;
+        for (int k = tid; k < nq + 2 * nt; k += (int)blockDim.x) {
+            if (k < nq) {
+                const int rho = row0 + k;
+                prefetch_l2_bulk(a.q + (((size_t)b * N + rho / G) * a.Hq + kvh * G + rho % G) * D, D * 2);
+            } else {
+                const int kk = k - nq, row = t_lo + kk / 2;
+                prefetch_l2_bulk(((kk & 1) ? a.v_new : a.k_new) + (((size_t)b * N + row) * a.Hkv + kvh) * D, D * 2);
+            }
+        }
+    }
 
     if (tid == 0) {
         for (int i = 0; i < kNumBars; ++i) {

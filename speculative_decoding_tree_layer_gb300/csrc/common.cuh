@@ -112,6 +112,17 @@ DFLV_DEVINL void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* 
         : "memory");
 }
 
+// Requests [src, src + bytes) into the L2 (TMA engine; src 16-byte aligned,
+// bytes a multiple of 16) and the L2 line holding p.  Neither moves data into
+// the SM nor orders anything: a later load still reads whatever the line
+// holds when it is made, including writes that reach it after the request.
+DFLV_DEVINL void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
+}
+DFLV_DEVINL void prefetch_l2_line(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p) : "memory");
+}
+
 // One bulk (TMA engine) copy shared -> global; src, dst 16-byte aligned,
 // bytes a multiple of 16.  bulk_s2g_wait() then waits until every such copy
 // of this thread has written its data and orders those writes before this

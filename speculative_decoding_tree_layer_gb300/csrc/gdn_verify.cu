@@ -393,6 +393,22 @@ __global__ void __launch_bounds__(kGdnThreads, (NPT == 32 && RB <= 32) ? 3 : 2)
     const bool gram_half = warp < kHalfWarps;
     const int ht = gram_half ? tid : tid - kGdnThreads / 2;  // thread index within the half
     constexpr int kHalf = kGdnThreads / 2;
+    // With early prefetch the first half also asks for this layer's inputs
+    // in the L2 before the dependency wait (in a model the layer before has
+    // just written them there); the copies after the wait read them, so
+    // whatever the preceding kernel writes in between is what they get.
+    if (early && gram_half) {
+        constexpr int kPer = 5;  // k row, q row, v block, beta, log_alpha
+        for (int idx = ht; idx < N * kPer; idx += kHalf) {
+            const int i = idx / kPer, what = idx % kPer;
+            const size_t kqo = (((size_t)b * N + i) * a.Hk + hk) * DK;
+            const size_t sidx = ((size_t)b * N + i) * a.Hv + h;
+            if (what == 0) prefetch_l2_bulk(a.k + kqo, DK * 2);
+            else if (what == 1) prefetch_l2_bulk(a.q + kqo, DK * 2);
+            else if (what == 2) prefetch_l2_bulk(a.v + sidx * a.dv + r0, RB * 2);
+            else prefetch_l2_line((what == 3 ? a.beta : a.log_alpha) + sidx);
+        }
+    }
     auto issue_layer_inputs = [&]() {
         for (int idx = ht; idx < N * CH; idx += kHalf) {
             const int i = idx / CH, c = idx % CH;
