@@ -421,12 +421,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnVerifyArgs a, 
         ti.count = ti.tree ? min(kTK, P + n - ti.start) : min(kTK, P - ti.start);
         return ti;
     };
-    // With early prefetch the layer inputs this CTA reads after the
-    // dependency wait -- its query rows and, where it quantises tree rows,
-    // their new keys and values -- are first asked for in the L2 (in a model
-    // the layer before has just written them there); the loads after the
-    // wait read whatever the lines hold by then.
-    if (early) {
+    // With early prefetch in a launch whose clusters are all resident at
+    // once, the layer inputs this CTA reads after the dependency wait -- its
+    // query rows and, where it quantises tree rows, their new keys and
+    // values -- are first asked for in the L2 (in a model the layer before
+    // has just written them there); the loads after the wait read whatever
+    // the lines hold by then.
+    if (a.flags & kFlagPrefetchInputs) {
         const int nq = min(RT, rows_valid - row0);
         const int t_lo = max(0, g0 - n_cache_tiles) * kTK, t_hi = min(n, (g0 + T - n_cache_tiles) * kTK);
         const int nt = t_hi > t_lo ? t_hi - t_lo : 0;
@@ -1221,6 +1222,9 @@ cudaError_t launch_tc(const AttnVerifyArgs& a, cudaStream_t stream) {
     const TcPlan p = plan_tc<D, KT, VT>(a);
     AttnVerifyArgs b = a;
     if (!b.ws || b.ws_bytes < (size_t)a.B * a.Hkv * p.n_rt * p.CS * p.RT * (D + 4) * sizeof(float)) b.ws = nullptr;
+    b.flags &= ~kFlagPrefetchInputs;
+    if ((a.flags & DFLV_FLAG_EARLY_PREFETCH) && (long)p.n_rt * a.Hkv * a.B <= active_clusters<D, KT, VT>(p.CS))
+        b.flags |= kFlagPrefetchInputs;
     return launch_pdl(kern, dim3(p.CS, p.n_rt * a.Hkv, a.B), dim3(kThreads), L::total, stream, p.CS, b, p.RT, p.CS);
 }
 

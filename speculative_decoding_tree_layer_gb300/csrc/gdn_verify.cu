@@ -393,11 +393,12 @@ __global__ void __launch_bounds__(kGdnThreads, (NPT == 32 && RB <= 32) ? 3 : 2)
     const bool gram_half = warp < kHalfWarps;
     const int ht = gram_half ? tid : tid - kGdnThreads / 2;  // thread index within the half
     constexpr int kHalf = kGdnThreads / 2;
-    // With early prefetch the first half also asks for this layer's inputs
-    // in the L2 before the dependency wait (in a model the layer before has
-    // just written them there); the copies after the wait read them, so
-    // whatever the preceding kernel writes in between is what they get.
-    if (early && gram_half) {
+    // With early prefetch in a launch whose CTAs are all resident at once,
+    // the first half also asks for this layer's inputs in the L2 before the
+    // dependency wait (in a model the layer before has just written them
+    // there); the copies after the wait read them, so whatever the
+    // preceding kernel writes in between is what they get.
+    if ((a.flags & kFlagPrefetchInputs) && gram_half) {
         constexpr int kPer = 5;  // k row, q row, v block, beta, log_alpha
         for (int idx = ht; idx < N * kPer; idx += kHalf) {
             const int i = idx / kPer, what = idx % kPer;
@@ -644,6 +645,27 @@ __global__ void __launch_bounds__(kGdnThreads, (NPT == 32 && RB <= 32) ? 3 : 2)
 
 }
 
+// CTAs of this kernel the device holds at once at this shared-memory size
+// (queried once per instantiation, after its shared-memory limit is raised;
+// 0 when the query fails).
+template <int DK, int RB, int NPT>
+long resident_ctas(size_t smem) {
+    static std::atomic<int> cache{0};  // 0 unknown, -1 failed
+    int v = cache.load(std::memory_order_relaxed);
+    if (v == 0) {
+        int nb = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, gdn_tree_verify_kernel<DK, RB, NPT>, kGdnThreads,
+                                                          smem) != cudaSuccess ||
+            nb < 1) {
+            cudaGetLastError();
+            nb = -1;
+        }
+        cache.store(nb, std::memory_order_relaxed);
+        v = nb;
+    }
+    return v > 0 ? (long)v * sm_count_cached() : 0;
+}
+
 template <int DK, int RB, int NPT>
 cudaError_t launch_dk_rb(const GdnVerifyArgs& a, cudaStream_t stream) {
     const GdnSmemLayout L(NPT, DK, RB);
@@ -651,7 +673,11 @@ cudaError_t launch_dk_rb(const GdnVerifyArgs& a, cudaStream_t stream) {
     cudaError_t e = ensure_smem(kern, L.total);
     if (e != cudaSuccess) return e;
     dim3 grid(a.dv / RB, a.Hv, a.B);
-    return launch_pdl(kern, grid, dim3(kGdnThreads), L.total, stream, 1, a);
+    GdnVerifyArgs b = a;
+    b.flags &= ~kFlagPrefetchInputs;
+    if ((a.flags & DFLV_FLAG_EARLY_PREFETCH) && (long)grid.x * grid.y * grid.z <= resident_ctas<DK, RB, NPT>(L.total))
+        b.flags |= kFlagPrefetchInputs;
+    return launch_pdl(kern, grid, dim3(kGdnThreads), L.total, stream, 1, b);
 }
 
 template <int DK>

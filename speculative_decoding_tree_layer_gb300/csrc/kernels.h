@@ -10,6 +10,13 @@
 
 namespace dflv {
 
+// Set by a verify launcher, never by a caller (the C ABI accepts only
+// DFLV_FLAG_* bits): with early prefetch, and when every CTA of the launch
+// can be resident at once (so that they all start under the preceding
+// kernel), the kernel asks for its layer inputs in the L2 before its
+// dependency wait.
+constexpr unsigned kFlagPrefetchInputs = 1u << 16;
+
 struct GdnVerifyArgs {
     int B, N_max, Hk, Hv, dk, dv;
     unsigned flags;  // DFLV_FLAG_*
