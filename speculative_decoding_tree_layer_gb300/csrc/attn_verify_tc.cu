@@ -16,8 +16,10 @@
 //   * load warps (2, one per plane): the raw codes and scales of each tile
 //     by bulk copies (TMA engine) into double buffers, completion counted in
 //     bytes on an mbarrier; the first two tiles are requested before the kernel waits
-//     for its predecessor when early prefetch is on.  The CTA that attends
-//     to a tree tile first quantises the tree's rows into the cache;
+//     for its predecessor when early prefetch is on (and, when every cluster
+//     of the launch is resident at once, L2 requests for the layer's query
+//     rows and the tree's new keys and values).  The CTA that attends to a
+//     tree tile first quantises the tree's rows into the cache;
 //   * stage warps (4): each raw tile is expanded into fp16 hi + lo tiles
 //     with the block scale folded in (d * code is exact in fp32; hi =
 //     fp16(x), lo = fp16(x - hi)).  K and V tiles are double-buffered;

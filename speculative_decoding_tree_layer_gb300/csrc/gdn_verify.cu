@@ -31,7 +31,9 @@
 // fewer than 64 rows with trees over 32 nodes).  The node count is padded to a compile-time
 // NPT (32 or 64) so every loop has a fixed trip count and the tensor-core
 // fragments of a step are loaded together.  With early prefetch the state
-// rows and the tree are fetched before the kernel waits for its predecessor.
+// rows and the tree are fetched before the kernel waits for its predecessor,
+// and, when every CTA of the launch is resident at once, the layer's k, q, v
+// rows and node scalars are requested into the L2.
 // It writes u, g and a copy of k as the factors commit needs.  A plain
 // verify never writes S_0 (rollback is free); with a pending path (deferred
 // commit) a CTA first applies the previous step's accepted path to its rows
