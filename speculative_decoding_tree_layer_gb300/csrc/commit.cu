@@ -26,16 +26,6 @@ namespace {
 
 constexpr int kCommitThreads = 256;
 
-DFLV_DEVINL bool path_ok(const CommitArgs& a, int b, int& L) {
-    L = __ldg(a.path_len + b);
-    if (L < 1 || L > a.N_max) return false;
-    for (int m = 0; m < L; ++m) {
-        const int p = __ldg(a.path + (size_t)b * a.N_max + m);
-        if (p < 0 || p >= a.N_max) return false;
-    }
-    return true;
-}
-
 __device__ void commit_gdn_head(const CommitArgs& a, int layer, int b, int h, unsigned char* smem) {
     const int tid = threadIdx.x;
     const CommitGdnLayer ly = a.gdn[layer];
@@ -114,51 +104,65 @@ __device__ void commit_gdn_head(const CommitArgs& a, int layer, int b, int h, un
 
 __device__ void commit_kv_head(const CommitArgs& a, int layer, int b, int kvh, unsigned char* smem) {
     const int tid = threadIdx.x;
-    int L;
-    if (!path_ok(a, b, L)) {
+    const int N = a.N_max;  // <= 64 (the ancestor masks are 64-bit)
+    __shared__ int src_s[64];
+    // The path length, every path entry and the cache position in one round
+    // of loads, then the checks: the path (raised by the GDN heads when
+    // there are any) before the capacity.
+    const int L = __ldg(a.path_len + b);
+    const int P = __ldg(a.n_past + b);
+    const bool L_ok = L >= 1 && L <= N;
+    bool bad_path = !L_ok, bad_cap = false;
+    if (tid < N) {
+        const int p = __ldg(a.path + (size_t)b * N + tid);
+        if (L_ok && tid < L) {
+            if (p < 0 || p >= N) bad_path = true;
+            else bad_cap = P + p >= a.cap;
+            src_s[tid] = P + p;
+        }
+    }
+    if (__syncthreads_or(bad_path)) {
         if (tid == 0 && layer == 0 && kvh == 0 && a.n_gdn == 0) raise_status(a.status, DFLV_DEV_PATH);
         return;
     }
-    const int P = __ldg(a.n_past + b);
-    const int N = a.N_max;
-    __shared__ int src_s[64];
-    bool bad = P < 0 || P + L > a.cap;
-    for (int m = 0; m < L; ++m) bad |= P + __ldg(a.path + (size_t)b * N + m) >= a.cap;
-    if (bad) {
+    if (__syncthreads_or(bad_cap || P < 0 || P + L > a.cap)) {
         if (tid == 0 && kvh == 0) raise_status(a.status, DFLV_DEV_CAPACITY);
         return;
     }
-    for (int m = tid; m < L; m += kCommitThreads) src_s[m] = P + __ldg(a.path + (size_t)b * N + m);
-    __syncthreads();
     const CommitAttnLayer ly = a.attn[layer];
     const size_t row0 = ((size_t)b * a.Hkv + kvh) * a.cap;
-    const int nb = a.D / 32;
-    // four planes: K codes, V codes, K scales, V scales (no scales for f32)
-    for (int plane = 0; plane < 4; ++plane) {
-        uint8_t* base;
-        int rb;
-        if (plane < 2) {
-            base = plane == 0 ? ly.kq : ly.vq;
-            rb = kv_code_bytes(a.type, plane, a.D);
-        } else {
-            if (a.type == DFLV_KV_F32) break;
-            base = reinterpret_cast<uint8_t*>(plane == 2 ? ly.ks : ly.vs);
-            rb = nb * 2;
-        }
-        // rows are 4-byte multiples (scales: D/32 halves with D >= 64)
-        const int w = rb / 4;
-        uint32_t* tmp = reinterpret_cast<uint32_t*>(smem);
-        for (int idx = tid; idx < L * w; idx += kCommitThreads) {
-            const int m = idx / w, c = idx % w;
-            tmp[idx] = reinterpret_cast<const uint32_t*>(base + (row0 + src_s[m]) * rb)[c];
-        }
-        __syncthreads();
-        for (int idx = tid; idx < L * w; idx += kCommitThreads) {
-            const int m = idx / w, c = idx % w;
-            reinterpret_cast<uint32_t*>(base + (row0 + P + m) * rb)[c] = tmp[idx];
-        }
-        __syncthreads();
+    // four planes: K codes, V codes, K scales, V scales (no scales for f32);
+    // every row is a multiple of 4 bytes (scales: D/32 halves with D >= 64)
+    const int planes = a.type == DFLV_KV_F32 ? 2 : 4;
+    uint8_t* base[4];
+    int w[4], off[4], tot = 0;
+#pragma unroll
+    for (int pl = 0; pl < 4; ++pl) {
+        base[pl] = pl == 0 ? ly.kq : pl == 1 ? ly.vq : reinterpret_cast<uint8_t*>(pl == 2 ? ly.ks : ly.vs);
+        w[pl] = pl >= planes ? 0 : (pl < 2 ? kv_code_bytes(a.type, pl, a.D) : a.D / 32 * 2) / 4;
+        off[pl] = tot;
+        tot += L * w[pl];
     }
+    // Every source row of every plane reaches shared memory before any row
+    // is written (a destination can be another accepted node's source); the
+    // copies of all planes are in flight at once.
+    uint32_t* tmp = reinterpret_cast<uint32_t*>(smem);
+#pragma unroll
+    for (int pl = 0; pl < 4; ++pl)
+        for (int idx = tid; idx < L * w[pl]; idx += kCommitThreads) {
+            const int m = idx / w[pl], c = idx % w[pl];
+            cp_async4(tmp + off[pl] + idx,
+                      reinterpret_cast<const uint32_t*>(base[pl] + (row0 + src_s[m]) * (size_t)(4 * w[pl])) + c);
+        }
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+#pragma unroll
+    for (int pl = 0; pl < 4; ++pl)
+        for (int idx = tid; idx < L * w[pl]; idx += kCommitThreads) {
+            const int m = idx / w[pl], c = idx % w[pl];
+            reinterpret_cast<uint32_t*>(base[pl] + (row0 + P + m) * (size_t)(4 * w[pl]))[c] = tmp[off[pl] + idx];
+        }
 }
 
 __global__ void __launch_bounds__(kCommitThreads) commit_kernel(const __grid_constant__ CommitArgs a) {
@@ -192,8 +196,10 @@ cudaError_t launch_commit_rollback(const CommitArgs& a, cudaStream_t stream) {
         size_t smem = 0;
         if (a.n_gdn > 0) smem = (size_t)a.N_max * (a.dv + a.dk) * 4;
         if (a.n_attn > 0) {
-            const int code_bytes = max(kv_code_bytes(a.type, 0, a.D), kv_code_bytes(a.type, 1, a.D));
-            const size_t kv = (size_t)a.N_max * code_bytes;
+            // every plane's rows of the path at once
+            const int row_bytes = kv_code_bytes(a.type, 0, a.D) + kv_code_bytes(a.type, 1, a.D) +
+                                  (a.type == DFLV_KV_F32 ? 0 : 2 * (a.D / 32) * 2);
+            const size_t kv = (size_t)a.N_max * row_bytes;
             if (kv > smem) smem = kv;
         }
         cudaError_t e = ensure_smem(commit_kernel, smem);
