@@ -50,6 +50,15 @@ __global__ void __launch_bounds__(kArgmaxThreads) accept_argmax_kernel(AcceptArg
     const int i = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (CS > 1) cluster_arrive_relaxed();  // paired with the wait before the push
+    const int V = a.vocab;
+    const float* row = a.logits + ((size_t)b * a.N_max + i) * V;
+    // this CTA's share of the vocabulary, in multiples of 4
+    const int per = (((V + CS - 1) / CS) + 3) & ~3;
+    const int c0 = min(V, rank * per), c1 = min(V, c0 + per);
+    // The share is requested into the L2 before the dependency wait (in a
+    // model the LM head before has just written the logits there); the loads
+    // after the wait read whatever the lines hold by then.
+    if (tid == 0 && (V & 3) == 0 && c1 > c0) prefetch_l2_bulk(row + c0, (uint32_t)(c1 - c0) * 4u);
     grid_dependency_wait();
     grid_launch_dependents();
     const int n = __ldg(a.n_nodes + b);
@@ -58,11 +67,6 @@ __global__ void __launch_bounds__(kArgmaxThreads) accept_argmax_kernel(AcceptArg
         return;
     }
 
-    const int V = a.vocab;
-    const float* row = a.logits + ((size_t)b * a.N_max + i) * V;
-    // this CTA's share of the vocabulary, in multiples of 4
-    const int per = (((V + CS - 1) / CS) + 3) & ~3;
-    const int c0 = min(V, rank * per), c1 = min(V, c0 + per);
     float bv = -INFINITY;
     int bi = INT_MAX;
     if ((V & 3) == 0) {
