@@ -43,6 +43,10 @@ def test_gdn_host_validation(lib):
     assert _gdn_call(dflv.gdn_desc(1, 22, 16, 48, 96, 128)) == dflv.DFLV_ERR_UNSUPPORTED
     assert _gdn_call(dflv.gdn_desc(1, 22, 16, 40, 128, 128)) == dflv.DFLV_ERR_INVALID_ARG
     assert _gdn_call(dflv.gdn_desc(0, 22, 16, 48, 128, 128)) == dflv.DFLV_ERR_INVALID_ARG
+    # only DFLV_FLAG_EARLY_PREFETCH: the launchers keep higher bits for
+    # themselves (the layer-input prefetch), so no caller can set them
+    for flags in (2, 1 << 16, 1 | (1 << 16)):
+        assert _gdn_call(dflv.gdn_desc(1, 22, 16, 48, 128, 128, flags)) == dflv.DFLV_ERR_INVALID_ARG
     assert _gdn_call(ok, q=None) == dflv.DFLV_ERR_INVALID_ARG
     assert _gdn_call(ok, state=24) == dflv.DFLV_ERR_INVALID_ARG          # misaligned
     assert _gdn_call(ok, factors=dflv.dflv_gdn_factors(16, None, 16)) == dflv.DFLV_ERR_INVALID_ARG
@@ -75,6 +79,8 @@ def test_attn_host_validation(lib):
     assert call(d(kv_type=dflv.DFLV_KV_Q8_0_Q4_0, D=64)) == dflv.DFLV_ERR_UNSUPPORTED
     assert call(d(kv_type=dflv.DFLV_KV_Q4_0_Q8_0, D=64)) == dflv.DFLV_ERR_UNSUPPORTED
     assert call(d(scale=float("nan"))) == dflv.DFLV_ERR_INVALID_ARG
+    for flags in (2, 1 << 16, 1 | (1 << 16)):
+        assert call(d(flags=flags)) == dflv.DFLV_ERR_INVALID_ARG
     assert call(d(), cache=dflv.dflv_kv_layer(16, 16, None, 16)) == dflv.DFLV_ERR_INVALID_ARG
     assert call(d(), cache=dflv.dflv_kv_layer(16, 16, 18, 16)) == dflv.DFLV_ERR_INVALID_ARG  # scale rows
     assert call(d(), q=None) == dflv.DFLV_ERR_INVALID_ARG
