@@ -121,7 +121,14 @@ typedef enum {
  * that immediately precedes the call on the stream writes none of these
  * buffers -- in a verify step, every layer after the first.  (Each kernel
  * of the library releases its successor only after its own wait, so the
- * overlap never reaches past the immediate predecessor.) */
+ * overlap never reaches past the immediate predecessor.)  Before its wait a
+ * kernel may also ask for inputs the preceding kernel produces (a verify's
+ * q, k, v, beta, log_alpha and new keys/values; the acceptance's logits) to
+ * be brought into the L2, where a model's producing layer has just left
+ * them; such a request moves no data into the kernel and orders nothing, so
+ * the values it reads after the wait are the ones the predecessor wrote.
+ * The verify kernels do so only with the flag set and when all their CTAs
+ * fit on the device at once. */
 enum { DFLV_FLAG_EARLY_PREFETCH = 1 };
 
 /* ------------------------------------------------------------------------ */
